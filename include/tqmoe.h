@@ -1,0 +1,242 @@
+/*
+ * tqmoe.h — C ABI of the trellis-quantized MoE grouped GEMM for GB300 (sm_103a).
+ *
+ * The routed-expert (MoE) product over expert weights stored as 2-bit
+ * bitshift-trellis bitstreams, with the trellis decode fused into the multiply.
+ *
+ * Sources (pages; cited by title and section):
+ *  [P1] "fix(qtip): gate the trellis grouped GEMM on m-tile occupancy, not token
+ *       count" — "The cause is a threshold, not a kernel defect" (pairs sorted
+ *       by expert, sum_e ceil(count_e / TILE_M) m-tiles, each woken expert's
+ *       packed bytes staged once per m-tile; the tile-fill closed form), "The
+ *       fix" (the amortization predicate), "Tests", post-merge note (the
+ *       n <= 8 floor, the GEMV pin).
+ *  [P2] "perf(qtip): arch-specialise the trellis grouped GEMM (D16) + close the
+ *       silent-failure holes (D18)" — items 1 and 2 of the commit message
+ *       (m-tile size; contiguous-run decode seeded by the window identity),
+ *       "The two changes" (packed 2-bit bytes cross HBM, decode lands in a
+ *       shared-memory tile, full-size weights never materialise), "D18" (every
+ *       launcher returns a status, empty grids are errors, unsupported arch is
+ *       refused), "The arch witness".
+ *  [P3] "fix(ArcLab/ArcQuant): make prefill measurable, then ship the two
+ *       kernels it proves were switched off" — launch counters prove which
+ *       kernel ran; unknown environment values warn and keep the default.
+ *
+ * Data model (the pages leave the decode constants open; this library fixes):
+ *  - Pair p = t * top_k + j is token t's j-th routed expert topk_ids[t][j].
+ *  - Expert e's weight row r (0 <= r < N) is a bitstream of K 2-bit symbols in
+ *    packed[e][r][0 .. K/4): symbol i is bits [2(i%4), 2(i%4)+2) of byte i/4.
+ *  - The trellis state of symbol i is the L-bit window of the stream ending
+ *    with symbol i (bits [2i+2-L, 2i+2), zeros before the row start), i.e.
+ *    s_i = (s_{i-1} >> 2) | (c_i << (L-2)), s_{-1} = 0.  The weight is
+ *    W_e[r][i] = lut[s_i], lut an fp16 table of 2^L entries.
+ *  - Y[t][r] = sum_j topk_w[t][j] * sum_i W_{topk_ids[t][j]}[r][i] * x[t][i].
+ *
+ * Conventions for every call below:
+ *  - Pointers marked (device) are device memory owned by the caller; the
+ *    library allocates no device memory and keeps no pointer after returning.
+ *  - Calls taking a stream enqueue work on it and return without waiting;
+ *    they never synchronize the device.  Status codes report argument and
+ *    launch errors only; device-side faults of the data (an expert id out of
+ *    range, a tile map over capacity, a wait that timed out) are recorded in a
+ *    device error word read by tq_device_error().
+ *  - Return value: TQ_OK (0) or a negative TQ_ERR_* code.  A failed call has
+ *    launched nothing or reports the launch failure; outputs are then
+ *    undefined and must not be read as results.
+ *  - Layouts are row-major and dense.  bf16/fp16 values are passed as their
+ *    16-bit patterns (uint16_t).
+ */
+#ifndef TQMOE_H
+#define TQMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without the CUDA headers; NULL is the legacy default stream. */
+typedef struct CUstream_st* tq_stream_t;
+
+enum tq_status {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = -1,      /* null pointer, bad size or alignment          */
+  TQ_ERR_UNSUPPORTED_ARCH = -2, /* device or binary lacks sm_103a device code    */
+  TQ_ERR_CAPACITY = -3,         /* tile map larger than the caller's capacity    */
+  TQ_ERR_LAUNCH = -4,           /* kernel launch failed (cudaGetLastError)       */
+  TQ_ERR_CAPTURING = -5,        /* arch witness cannot be taken during capture   */
+  TQ_ERR_DEVICE_TIMEOUT = -6,   /* a device-side wait gave up (device error word)*/
+  TQ_ERR_CUDA = -7,             /* another CUDA runtime error                     */
+  TQ_ERR_WORKSPACE = -8         /* workspace too small or misaligned             */
+};
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* tq_status_string(int status);
+
+/* ---------------------------------------------------------------------------
+ * Arch witness  ([P2] "The arch witness", D18 #12)
+ *
+ * Launches a one-thread kernel compiled under the same architecture guard as
+ * the grouped GEMM and reads back the architecture the running binary carries.
+ * Succeeds only if the device is compute capability 10.3 and the binary holds
+ * sm_103a device code.  Only a successful answer is cached (per device); the
+ * witness is not taken while the calling thread's legacy stream or the given
+ * stream is capturing, in which case TQ_ERR_CAPTURING is returned and the
+ * next call retries.  Every launcher below checks the cached witness first and
+ * takes it if missing.  `device` is a CUDA ordinal; it becomes current.
+ * arch_out (host, may be NULL) receives __CUDA_ARCH__ of the device code.
+ * ------------------------------------------------------------------------- */
+int tq_init(int device);
+int tq_arch_witness(int device, int* arch_out);
+
+/* ---------------------------------------------------------------------------
+ * Tile fill and the amortization gate  ([P1] "The cause is a threshold",
+ * "The fix", post-merge note).  Host-only closed forms in three scalars: safe
+ * inside CUDA-graph capture.  All evaluated in fp64.
+ * ------------------------------------------------------------------------- */
+
+/* n*k / (E * (1 - (1 - k/E)^n)); 0 for n == 0; NaN on invalid arguments
+ * (k < 1, k > E, n < 0). */
+double tq_pairs_per_woken_expert(int64_t n, int top_k, int E);
+
+/* 1 if pairs per woken expert >= tile_m (an average m-tile is full), 0 if
+ * not or n == 0, TQ_ERR_INVALID_ARG if k < 1, k > E, tile_m < 1 or n < 0. */
+int tq_tiles_amortize(int64_t n, int top_k, int E, int tile_m);
+
+/* Smallest n with tq_tiles_amortize(n, ...) == 1 (683 for top-6 of 256 at
+ * tile_m 16).  Negative TQ_ERR_INVALID_ARG on invalid arguments. */
+int64_t tq_grouped_min_tokens(int top_k, int E, int tile_m);
+
+/* Upper bound on the number of m-tiles sum_e ceil(count_e / tile_m) for ANY
+ * routing of n*top_k pairs: min(P, floor(P / tile_m) + min(E, P)).  Size the
+ * tile map with it.  Negative on invalid arguments. */
+int64_t tq_tile_map_capacity(int64_t n, int top_k, int E, int tile_m);
+
+/* Arm selection ([P1] post-merge note): TQ_ARM_GEMV when n <= 8 or the tiles
+ * do not amortize, TQ_ARM_GROUPED otherwise; `pin` forces an arm.  Negative
+ * on invalid arguments. */
+enum tq_arm { TQ_ARM_AUTO = 0, TQ_ARM_GEMV = 1, TQ_ARM_GROUPED = 2 };
+#define TQ_DECODE_REGIME_MAX_TOKENS 8
+int tq_select_arm(int64_t n, int top_k, int E, int tile_m, int pin);
+
+/* ---------------------------------------------------------------------------
+ * Routing sort  ([P1] "The cause is a threshold": the grouped GEMM sorts pairs
+ * by expert)
+ *
+ * topk_ids    (device) int32 [n][top_k], expert ids in [0, E).
+ * counts      (device) int32 [E]       out: pairs per expert.
+ * offsets     (device) int32 [E + 1]   out: exclusive prefix sum of counts.
+ * sorted_pairs(device) int32 [n*top_k] out: pair ids p ordered by expert,
+ *             ascending p within an expert (a stable sort).
+ * Limits: 1 <= top_k <= E <= 1024, 0 <= n*top_k < 2^31.  An expert id out of
+ * range is skipped and sets TQ_ERR_INVALID_ARG in the device error word.
+ * One thread block; no scratch memory.
+ * ------------------------------------------------------------------------- */
+int tq_route(const int32_t* topk_ids, int64_t n, int top_k, int E,
+             int32_t* counts, int32_t* offsets, int32_t* sorted_pairs,
+             tq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * m-tile map  ([P1] "The cause is a threshold"; [P2] D18: route and GEMM must
+ * agree on tile_m)
+ *
+ * For experts e ascending with count_e > 0 and i < ceil(count_e / tile_m):
+ *   tiles[t] = { e, offsets[e] + i*tile_m, min(tile_m, count_e - i*tile_m) }.
+ * offsets   (device) int32 [E + 1] from tq_route.
+ * tiles     (device) int32 [cap][3]  out.
+ * num_tiles (device) int32 [1]       out: number of tiles written (<= cap).
+ * cap: capacity of `tiles` in tiles, >= 1; tq_tile_map_capacity() is always
+ * enough.  If the map would exceed cap, only cap tiles are written,
+ * *num_tiles = cap and TQ_ERR_CAPACITY is set in the device error word.
+ * 1 <= tile_m <= 256 (the grouped kernel's largest m-tile).
+ * ------------------------------------------------------------------------- */
+int tq_build_tile_map(const int32_t* offsets, int E, int tile_m,
+                      int32_t* tiles, int32_t* num_tiles, int64_t cap,
+                      tq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Grouped GEMM  ([P1] m-tiles; [P2] contiguous-run decode, decode fused into
+ * the multiply)
+ *
+ * For every m-tile and every 128-row block of N: TMA stages the expert's
+ * packed rows once, warps decode runs of 32 symbols (seeded by the window
+ * identity, then stepped) into a bf16 weight tile in tensor memory, tcgen05
+ * MMAs contract it with the tile's gathered activations (fp32 accumulate),
+ * and the epilogue scales by the router weight and adds into y32.
+ *
+ * x          (device) bf16 [n][K]; 16-byte aligned.
+ * packed     (device) uint8 [E][N][K/4]; 16-byte aligned.
+ * lut        (device) fp16 [2^L] (converted to bf16, nearest-even, on chip).
+ * sorted_pairs, tiles, num_tiles: from tq_route / tq_build_tile_map with the
+ *            same tile_m.  cap = capacity of `tiles`.
+ * topk_w     (device) fp32 [n][top_k] router weights.
+ * y32        (device) fp32 [n][N]: ACCUMULATED into (y32 += ...); zero it
+ *            first for a plain product.  Additions are fp32 atomics, so the
+ *            summation order (and the last bits) vary between runs.
+ * Requires: K % 64 == 0, N % 128 == 0, L even in [2, 16], 1 <= tile_m <= 256,
+ * 1 <= top_k <= E.  Device: compute capability 10.3.
+ * ------------------------------------------------------------------------- */
+int tq_grouped_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
+                    const int32_t* sorted_pairs, const float* topk_w,
+                    const int32_t* tiles, const int32_t* num_tiles, int64_t cap,
+                    int64_t n, int top_k, int E, int K, int N, int tile_m,
+                    float* y32, tq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Per-pair GEMV arm  ([P1] "The regression": the per-pair gather GEMV; no
+ * de-duplication of experts across pairs)
+ *
+ * For every pair p (token t = p / top_k, expert e = topk_ids[p]) and every
+ * row r: y32[t][r] += topk_w[p] * sum_i W_e[r][i] * x[t][i], fp32 accumulate,
+ * fp16 weights widened exactly.  Same layouts as tq_grouped_gemm; needs no
+ * routing sort.  Requires K % 64 == 0, K <= 8192, L even in [2, 16].
+ * ------------------------------------------------------------------------- */
+int tq_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
+            const int32_t* topk_ids, const float* topk_w,
+            int64_t n, int top_k, int E, int K, int N,
+            float* y32, tq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Combine: y[i] = bf16(y32[i]), round to nearest even, for i < count.
+ * y32 (device) fp32 [count]; y (device) bf16 [count].
+ * ------------------------------------------------------------------------- */
+int tq_combine(const float* y32, uint16_t* y, int64_t count, tq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Whole routed-expert product: zero y32, route, tile map, arm selection
+ * (tq_select_arm with `pin`), the selected arm, combine to bf16 y [n][N].
+ *
+ * workspace (device): caller-owned scratch of at least
+ *   tq_moe_workspace_size(n, top_k, E, N, tile_m) bytes, 256-byte aligned.
+ *   It holds counts, offsets, sorted pairs, the tile map and the fp32
+ *   accumulator; its contents are undefined after the call.
+ * arm_used (host, may be NULL): receives TQ_ARM_GEMV or TQ_ARM_GROUPED.
+ * The first grouped engagement in a process logs the tile fill and the
+ * amortization boundary to stderr once (unless TQ_QUIET=1).
+ * ------------------------------------------------------------------------- */
+size_t tq_moe_workspace_size(int64_t n, int top_k, int E, int N, int tile_m);
+int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
+                   const int32_t* topk_ids, const float* topk_w,
+                   int64_t n, int top_k, int E, int K, int N, int tile_m, int pin,
+                   void* workspace, size_t workspace_bytes,
+                   uint16_t* y, int* arm_used, tq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics
+ * ------------------------------------------------------------------------- */
+
+/* Reads and clears the current device's error word (synchronizes the device).
+ * *code (host) receives 0 or the first TQ_ERR_* recorded by a kernel since the
+ * last read; *where (host, may be NULL) a kernel-specific location tag. */
+int tq_device_error(int* code, int* where);
+
+/* Host-side counts of successful launches since process start, per kernel:
+ * out[0] route, out[1] tile map, out[2] grouped GEMM, out[3] GEMV,
+ * out[4] combine ([P3]: counters prove which arm ran). */
+void tq_launch_counts(int64_t out[5]);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQMOE_H */

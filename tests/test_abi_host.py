@@ -1,0 +1,84 @@
+"""C ABI without a GPU: the library loads, exports every function the header
+declares, and its host-only gate arithmetic (tile fill, amortization predicate,
+flip point, tile-map capacity, arm selection) equals the oracle bit for bit."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle.trellis_moe as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tqmoe.h")
+
+
+@pytest.fixture(scope="module")
+def tq():
+    from trellis_quantized_moe_sort_gb300 import build
+    build.build()
+    import trellis_quantized_moe_sort_gb300 as tq
+    return tq
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(tq):
+    declared = _declared_functions()
+    assert len(declared) >= 17
+    h = ctypes.CDLL(tq.lib_path)
+    missing = [name for name in declared if not hasattr(h, name)]
+    assert not missing, missing
+    assert sorted(tq.EXPORTED_SYMBOLS) == declared
+
+
+def test_status_strings(tq):
+    for code in range(0, -9, -1):
+        s = tq.tq_status_string(code)
+        assert s and "unknown" not in s
+    assert "unknown" in tq.tq_status_string(-99)
+
+
+SHAPES = [(k, E) for (k, E) in ((1, 1), (1, 8), (2, 8), (6, 8), (8, 8), (2, 16), (4, 32),
+                                 (6, 64), (8, 128), (6, 256), (8, 256), (2, 256), (7, 1000))]
+
+
+def test_pairs_per_woken_bitexact(tq):
+    for k, E in SHAPES:
+        for n in list(range(0, 50)) + [127, 128, 512, 682, 683, 1024, 1572, 2000, 8192, 10**6]:
+            a = tq.tq_pairs_per_woken_expert(n, k, E)
+            b = O.pairs_per_woken_expert(n, k, E)
+            assert a == b, (n, k, E, a, b)
+
+
+def test_gate_and_flip_bitexact(tq):
+    for k, E in SHAPES:
+        for T in (1, 4, 16, 64, 128, 256):
+            flip = tq.tq_grouped_min_tokens(k, E, T)
+            assert flip == O.grouped_min_tokens(k, E, T), (k, E, T)
+            for n in sorted({0, 1, 8, 9, flip - 1, flip, flip + 1, 2 * flip}):
+                if n < 0:
+                    continue
+                assert tq.tq_tiles_amortize(n, k, E, T) == O.tiles_amortize(n, k, E, T)
+                assert tq.tq_tile_map_capacity(n, k, E, T) == O.tile_map_capacity(n, k, E, T)
+                for pin, name in ((0, "auto"), (1, "gemv"), (2, "grouped")):
+                    arm = tq.tq_select_arm(n, k, E, T, pin)
+                    assert {1: "gemv", 2: "grouped"}[arm] == O.dispatch_arm(n, k, E, T, name)
+    assert tq.tq_grouped_min_tokens(6, 256, 16) == 683
+
+
+def test_host_functions_reject_invalid_arguments(tq):
+    for args in ((5, 0, 8, 16), (5, 9, 8, 16), (5, 2, 8, 0), (-1, 2, 8, 16)):
+        with pytest.raises(tq.TQError):
+            tq.tq_tiles_amortize(*args)
+        with pytest.raises(tq.TQError):
+            tq.tq_tile_map_capacity(*args)
+    with pytest.raises(tq.TQError):
+        tq.tq_select_arm(10, 2, 8, 16, pin=7)
+    assert np.isnan(tq.tq_pairs_per_woken_expert(4, 9, 8))
+    assert tq.tq_moe_workspace_size(16, 2, 8, 128, 16) > 16 * 128 * 4

@@ -1,0 +1,157 @@
+"""Grouped GEMM and per-pair GEMV arms on the GPU against the CPU oracle.
+
+Small problems (several tiles, ragged tails, every L, K of 1..many k-steps,
+several 128-row blocks) are compared on every output; the five workloads at
+full size on sampled rows.  Tolerance: max|y - ref| / max|ref| <= 1e-2 on the
+fp32 accumulator (bf16 weights on the tensor cores; the GEMV widens fp16
+weights exactly and is held to 1e-4)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs
+import oracle.trellis_moe as O
+import trellis_quantized_moe_sort_gb300 as tq
+from gpu_util import to_device, grouped_y32, gemv_y32, normwise, sample_rows, check_no_device_error
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+TOL_GEMV = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from trellis_quantized_moe_sort_gb300 import build
+    build.build()
+    tq.tq_init(0)
+
+
+# (E, top_k, n, K, N, L, tile_m, routing)
+SMALL = {
+    "tiny_e8_k2_n16_T16": (8, 2, 16, 256, 128, 12, 16, "uniform"),
+    "tiny_T64": (8, 2, 16, 256, 128, 12, 64, "uniform"),
+    "tiny_T1": (8, 2, 16, 256, 128, 12, 1, "uniform"),
+    "ragged_n37_K192_N256": (4, 4, 37, 192, 256, 16, 16, "uniform"),
+    "one_kstep_K64": (16, 3, 50, 64, 128, 8, 32, "uniform"),
+    "big_tiles_T256": (8, 2, 300, 128, 384, 16, 256, "uniform"),
+    "T48_L10": (6, 2, 40, 512, 128, 10, 48, "uniform"),
+    "L2": (3, 3, 20, 320, 128, 2, 16, "uniform"),
+    "L4_L6_mix": (5, 2, 24, 128, 128, 6, 16, "uniform"),
+    "zipf_T128": (32, 4, 200, 256, 256, 14, 128, "zipf"),
+}
+
+
+def _small(name):
+    E, k, n, K, N, L, T, routing = SMALL[name]
+    return moe_inputs.make_custom(E, k, n, K, N, L, seed=hash(name) % 1000, routing=routing), T
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_grouped_small_all_outputs(name):
+    prob, T = _small(name)
+    d = to_device(prob)
+    y = grouped_y32(prob, d, T).cpu().numpy()
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, prob.shape.L)
+    err = normwise(y, ref)
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_gemv_small_all_outputs(name):
+    prob, _ = _small(name)
+    d = to_device(prob)
+    y = gemv_y32(prob, d).cpu().numpy()
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, prob.shape.L)
+    assert normwise(y, ref) <= TOL_GEMV
+
+
+def test_grouped_accumulates_into_y32():
+    prob, T = _small("tiny_e8_k2_n16_T16")
+    d = to_device(prob)
+    s = prob.shape
+    _, offsets, sp = tq.tq_route(d["ids"], s.E)
+    cap = tq.tq_tile_map_capacity(s.n, s.top_k, s.E, T)
+    tiles, nt = tq.tq_build_tile_map(offsets, T, cap)
+    y32 = torch.ones((s.n, s.N), dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        tq.tq_grouped_gemm(d["x"], d["packed"], d["lut"], sp, d["w"], tiles, nt, s.top_k, T, y32)
+    check_no_device_error()
+    ref = 1.0 + 2.0 * O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed,
+                                    prob.lut_bits, s.L)
+    assert normwise(y32.cpu().numpy(), ref) <= TOL
+
+
+def test_grouped_onehot_x_reads_single_weight_column():
+    """x[t] = e_i: y[t, r] = sum_j w W_e[r, i] -> checks the k ordering inside
+    the decoded tile (a transposed or shifted A layout fails here)."""
+    prob = moe_inputs.make_custom(4, 2, 8, 256, 128, 16, seed=77)
+    x = np.zeros_like(prob.x_bits)
+    cols = [0, 1, 15, 16, 63, 64, 130, 255]
+    for t, i in enumerate(cols):
+        x[t, i] = 0x3F80
+    prob.x_bits = x
+    d = to_device(prob)
+    y = grouped_y32(prob, d, 16).cpu().numpy()
+    ref = O.moe_forward(x, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, 16)
+    assert normwise(y, ref) <= TOL
+
+
+FULL = ["v4_decode_n32", "v4_n128_up", "v4_n128_down", "v4_fill_n512", "v4_fill_n683",
+        "v4_fill_n1024", "v4_prefill_n8192_up", "v4_prefill_n8192_down"]
+
+
+@pytest.fixture(scope="module")
+def full_problems():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            cache.clear()
+            prob = moe_inputs.make_problem(name)
+            cache[name] = (prob, to_device(prob))
+        return cache[name]
+    return get
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows(name, full_problems):
+    prob, d = full_problems(name)
+    s = prob.shape
+    rows = sample_rows(s.N, 48, seed=len(name))
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L, rows=rows)
+    for T in (16, 128):
+        y = grouped_y32(prob, d, T)[:, torch.from_numpy(rows).cuda()].cpu().numpy()
+        assert normwise(y, ref) <= TOL, (T, normwise(y, ref))
+    if s.n <= 1024:
+        y = gemv_y32(prob, d)[:, torch.from_numpy(rows).cuda()].cpu().numpy()
+        assert normwise(y, ref) <= TOL_GEMV
+
+
+def test_moe_forward_gate_and_arms():
+    """(top-2 of 8, TILE_M=16) flips at n = 64: below it the GEMV runs, at it
+    the grouped GEMM; n <= 8 always GEMV; the pin forces either arm; the
+    launch counters prove which kernel ran; y is bf16 of the product."""
+    assert tq.tq_grouped_min_tokens(2, 8, 16) == 64
+    for n, pin, want_arm in ((63, 0, 1), (64, 0, 2), (8, 0, 1), (5, 2, 2), (200, 1, 1)):
+        prob = moe_inputs.make_custom(8, 2, n, 256, 128, 12, seed=n + 10 * pin)
+        d = to_device(prob)
+        before = tq.tq_launch_counts()
+        y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=16, pin=pin)
+        check_no_device_error()
+        after = tq.tq_launch_counts()
+        assert arm == want_arm
+        ran = "grouped" if arm == 2 else "gemv"
+        other = "gemv" if arm == 2 else "grouped"
+        assert after[ran] == before[ran] + 1 and after[other] == before[other]
+        ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, 12)
+        got = y.float().cpu().numpy()
+        assert normwise(got, ref) <= TOL
+
+
+def test_moe_forward_empty_batch():
+    prob = moe_inputs.make_custom(8, 2, 4, 256, 128, 12, seed=3)
+    d = to_device(prob)
+    x0 = d["x"][:0]
+    y, arm = tq.tq_moe_forward(x0, d["packed"], d["lut"], d["ids"][:0], d["w"][:0])
+    check_no_device_error()
+    assert tuple(y.shape) == (0, 128)

@@ -1,0 +1,111 @@
+"""Routing sort, tile map and bf16 combine on the GPU: bit-exact against the
+oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs
+import oracle.trellis_moe as O
+import trellis_quantized_moe_sort_gb300 as tq
+from gpu_util import check_no_device_error
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from trellis_quantized_moe_sort_gb300 import build
+    build.build()
+    tq.tq_init(0)
+
+
+def test_arch_witness_is_sm103():
+    assert tq.tq_arch_witness(0) == 1030
+
+
+def _ids_cases():
+    rng = np.random.Generator(np.random.PCG64(5))
+    cases = {
+        "tiny": (moe_inputs.draw_routing(rng, 16, 8, 2)[0], 8),
+        "v4_n32": (moe_inputs.draw_routing(rng, 32, 256, 6)[0], 256),
+        "v4_n128": (moe_inputs.draw_routing(rng, 128, 256, 6)[0], 256),
+        "v4_zipf_n8192": (moe_inputs.draw_routing(rng, 8192, 256, 6, "zipf")[0], 256),
+        "one_expert_all": (np.full((1000, 1), 3, np.int32), 8),
+        "E1024": (moe_inputs.draw_routing(rng, 300, 1024, 8)[0], 1024),
+        "E1_k1": (np.zeros((5, 1), np.int32), 1),
+        "ragged_P_37x3": (moe_inputs.draw_routing(rng, 37, 5, 3)[0], 5),
+        "empty": (np.zeros((0, 6), np.int32), 256),
+    }
+    return cases
+
+
+CASES = _ids_cases()
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_route_bitexact(name):
+    ids, E = CASES[name]
+    d_ids = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32)).cuda()
+    counts, offsets, sp = tq.tq_route(d_ids, E)
+    check_no_device_error()
+    c, o, s = O.route(ids, E)
+    assert np.array_equal(counts.cpu().numpy(), c)
+    assert np.array_equal(offsets.cpu().numpy(), o)
+    assert np.array_equal(sp.cpu().numpy(), s)
+
+
+@pytest.mark.parametrize("name", ["tiny", "v4_n32", "v4_zipf_n8192", "one_expert_all", "E1024", "ragged_P_37x3"])
+@pytest.mark.parametrize("tile_m", [1, 7, 16, 64, 256])
+def test_tile_map_bitexact(name, tile_m):
+    ids, E = CASES[name]
+    n, k = ids.shape
+    d_ids = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32)).cuda()
+    _, offsets, _ = tq.tq_route(d_ids, E)
+    cap = tq.tq_tile_map_capacity(n, k, E, tile_m)
+    tiles, nt = tq.tq_build_tile_map(offsets, tile_m, cap)
+    check_no_device_error()
+    want = O.tile_map(O.route(ids, E)[1], tile_m)
+    got_n = int(nt.item())
+    assert got_n == len(want)
+    assert np.array_equal(tiles[:got_n].cpu().numpy(), want)
+
+
+def test_tile_map_over_capacity_is_flagged():
+    ids, E = CASES["v4_n32"]
+    d_ids = torch.from_numpy(ids).cuda()
+    _, offsets, _ = tq.tq_route(d_ids, E)
+    want = O.tile_map(O.route(ids, E)[1], 16)
+    cap = len(want) - 5
+    tiles, nt = tq.tq_build_tile_map(offsets, 16, cap)
+    torch.cuda.synchronize()
+    assert int(nt.item()) == cap
+    assert np.array_equal(tiles.cpu().numpy(), want[:cap])
+    code, where = tq.tq_device_error()
+    assert code == -3 and where == 2          # TQ_ERR_CAPACITY at the tile map
+    check_no_device_error()
+
+
+def test_route_flags_out_of_range_expert():
+    ids = np.array([[0, 1], [2, 8], [3, 1]], np.int32)    # 8 is out of range for E=8
+    counts, offsets, sp = tq.tq_route(torch.from_numpy(ids).cuda(), 8)
+    torch.cuda.synchronize()
+    code, where = tq.tq_device_error()
+    assert code == -1 and where == 1
+    c = counts.cpu().numpy()
+    assert c.sum() == 5 and c[8 - 1] == 0
+    check_no_device_error()
+
+
+def test_combine_bitexact():
+    rng = np.random.Generator(np.random.PCG64(9))
+    u = rng.integers(0, 1 << 16, 4096, dtype=np.uint32)
+    ties = ((u << 16) | 0x8000).astype(np.uint32).view(np.float32)
+    vals = np.concatenate([rng.standard_normal(100003).astype(np.float32),
+                           ties[np.isfinite(ties)],
+                           np.array([3.3895e38, -3.4e38, 0.0, -0.0, 1e-40], np.float32)])
+    for arr in (vals, vals[:-1], vals[: (len(vals) // 4) * 4]):      # ragged and vector paths
+        y32 = torch.from_numpy(arr.copy()).cuda()
+        y = tq.tq_combine(y32)
+        check_no_device_error()
+        got = y.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, O.bf16_rne_bits(arr))

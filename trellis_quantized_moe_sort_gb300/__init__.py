@@ -1,0 +1,283 @@
+"""Python binding of libtqmoe.so (C ABI: include/tqmoe.h).
+
+Argument marshalling only: every step of the MoE path runs in the library's
+CUDA kernels.  PyTorch provides device memory and the current stream.  There
+is no CPU fallback: if the library is missing or no sm_103a device is present,
+calls raise.
+
+Tensor conventions: bf16 activations (torch.bfloat16 or 16-bit integer views),
+packed bitstreams torch.uint8 [E, N, K/4], LUT fp16 (torch.float16 or 16-bit
+integer view) [2^L], router ids torch.int32 [n, top_k], router weights
+torch.float32 [n, top_k].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "TQError", "lib", "lib_path", "tq_init", "tq_arch_witness", "tq_pairs_per_woken_expert",
+    "tq_tiles_amortize", "tq_grouped_min_tokens", "tq_tile_map_capacity", "tq_select_arm",
+    "tq_route", "tq_build_tile_map", "tq_grouped_gemm", "tq_gemv", "tq_combine",
+    "tq_moe_workspace_size", "tq_moe_forward", "tq_device_error", "tq_launch_counts",
+    "tq_status_string", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "EXPORTED_SYMBOLS",
+]
+
+ARM_AUTO, ARM_GEMV, ARM_GROUPED = 0, 1, 2
+_HERE = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_HERE, "libtqmoe.so")
+
+_c_i64, _c_int, _c_dbl, _c_p, _c_sz = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p, ctypes.c_size_t
+
+# name -> (restype, argtypes); the same set include/tqmoe.h declares
+_SIGS = {
+    "tq_status_string": (ctypes.c_char_p, [_c_int]),
+    "tq_init": (_c_int, [_c_int]),
+    "tq_arch_witness": (_c_int, [_c_int, ctypes.POINTER(_c_int)]),
+    "tq_pairs_per_woken_expert": (_c_dbl, [_c_i64, _c_int, _c_int]),
+    "tq_tiles_amortize": (_c_int, [_c_i64, _c_int, _c_int, _c_int]),
+    "tq_grouped_min_tokens": (_c_i64, [_c_int, _c_int, _c_int]),
+    "tq_tile_map_capacity": (_c_i64, [_c_i64, _c_int, _c_int, _c_int]),
+    "tq_select_arm": (_c_int, [_c_i64, _c_int, _c_int, _c_int, _c_int]),
+    "tq_route": (_c_int, [_c_p, _c_i64, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p]),
+    "tq_build_tile_map": (_c_int, [_c_p, _c_int, _c_int, _c_p, _c_p, _c_i64, _c_p]),
+    "tq_grouped_gemm": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64,
+                                 _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p]),
+    "tq_gemv": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int, _c_int,
+                         _c_int, _c_p, _c_p]),
+    "tq_combine": (_c_int, [_c_p, _c_p, _c_i64, _c_p]),
+    "tq_moe_workspace_size": (_c_sz, [_c_i64, _c_int, _c_int, _c_int, _c_int]),
+    "tq_moe_forward": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int,
+                                _c_int, _c_int, _c_int, _c_int, _c_p, _c_sz, _c_p,
+                                ctypes.POINTER(_c_int), _c_p]),
+    "tq_device_error": (_c_int, [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
+    "tq_launch_counts": (None, [ctypes.POINTER(_c_i64)]),
+}
+EXPORTED_SYMBOLS = tuple(_SIGS)
+
+_lib = None
+
+
+class TQError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {tq_status_string(status)} ({status})" if what else
+                         f"{tq_status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libtqmoe.so (built by __graft_entry__.build()); raise if missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(lib_path):
+            raise RuntimeError(f"{lib_path} is not built; run `python -c 'import __graft_entry__ as g; "
+                               f"g.build()'` (nvcc, sm_103a)")
+        h = ctypes.CDLL(lib_path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(h, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = h
+    return _lib
+
+
+def tq_status_string(status: int) -> str:
+    return lib().tq_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise TQError(rc, what)
+
+
+# ------------------------------------------------------------------ torch glue
+
+def _torch():
+    import torch
+    if not torch.cuda.is_available():
+        raise RuntimeError("trellis_quantized_moe_sort_gb300 needs a CUDA device (sm_103a); none found")
+    return torch
+
+
+def _dev_ptr(t, dtypes, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtypes and t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _bits16():
+    torch = _torch()
+    return (torch.bfloat16, torch.float16, torch.int16, torch.uint16)
+
+
+# ------------------------------------------------------------------ API
+
+def tq_init(device: int = 0) -> None:
+    _check(lib().tq_init(device), "tq_init")
+
+
+def tq_arch_witness(device: int = 0) -> int:
+    arch = ctypes.c_int(0)
+    _check(lib().tq_arch_witness(device, ctypes.byref(arch)), "tq_arch_witness")
+    return arch.value
+
+
+def tq_pairs_per_woken_expert(n: int, top_k: int, E: int) -> float:
+    return lib().tq_pairs_per_woken_expert(n, top_k, E)
+
+
+def tq_tiles_amortize(n: int, top_k: int, E: int, tile_m: int) -> bool:
+    rc = lib().tq_tiles_amortize(n, top_k, E, tile_m)
+    if rc < 0:
+        raise TQError(rc, "tq_tiles_amortize")
+    return bool(rc)
+
+
+def tq_grouped_min_tokens(top_k: int, E: int, tile_m: int) -> int:
+    rc = lib().tq_grouped_min_tokens(top_k, E, tile_m)
+    if rc < 0:
+        raise TQError(int(rc), "tq_grouped_min_tokens")
+    return int(rc)
+
+
+def tq_tile_map_capacity(n: int, top_k: int, E: int, tile_m: int) -> int:
+    rc = lib().tq_tile_map_capacity(n, top_k, E, tile_m)
+    if rc < 0:
+        raise TQError(int(rc), "tq_tile_map_capacity")
+    return int(rc)
+
+
+def tq_select_arm(n: int, top_k: int, E: int, tile_m: int, pin: int = ARM_AUTO) -> int:
+    rc = lib().tq_select_arm(n, top_k, E, tile_m, pin)
+    if rc < 0:
+        raise TQError(rc, "tq_select_arm")
+    return rc
+
+
+def tq_route(topk_ids, E: int, counts=None, offsets=None, sorted_pairs=None, stream=None):
+    """Stable sort of pairs by expert -> (counts[E], offsets[E+1], sorted_pairs[P])."""
+    torch = _torch()
+    n, k = topk_ids.shape
+    dev = topk_ids.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev) if counts is None else counts
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
+    if sorted_pairs is None:
+        sorted_pairs = torch.empty(max(n * k, 1), dtype=torch.int32, device=dev)
+    _check(lib().tq_route(_dev_ptr(topk_ids, (torch.int32,), "topk_ids"), n, k, E,
+                          _dev_ptr(counts, (torch.int32,), "counts"),
+                          _dev_ptr(offsets, (torch.int32,), "offsets"),
+                          _dev_ptr(sorted_pairs, (torch.int32,), "sorted_pairs"), _stream(stream)),
+           "tq_route")
+    return counts, offsets, sorted_pairs[: n * k]
+
+
+def tq_build_tile_map(offsets, tile_m: int, cap: int, tiles=None, num_tiles=None, stream=None):
+    """m-tile map -> (tiles[cap, 3], num_tiles[1]) (device)."""
+    torch = _torch()
+    E = offsets.numel() - 1
+    dev = offsets.device
+    tiles = torch.empty((cap, 3), dtype=torch.int32, device=dev) if tiles is None else tiles
+    num_tiles = torch.empty(1, dtype=torch.int32, device=dev) if num_tiles is None else num_tiles
+    _check(lib().tq_build_tile_map(_dev_ptr(offsets, (torch.int32,), "offsets"), E, tile_m,
+                                   _dev_ptr(tiles, (torch.int32,), "tiles"),
+                                   _dev_ptr(num_tiles, (torch.int32,), "num_tiles"), cap, _stream(stream)),
+           "tq_build_tile_map")
+    return tiles, num_tiles
+
+
+def _shapes(x, packed, lut):
+    n, K = x.shape
+    E, N, kb = packed.shape
+    if kb * 4 != K:
+        raise ValueError(f"packed has {kb} bytes per row, expected K/4 = {K // 4}")
+    L = lut.numel().bit_length() - 1
+    if lut.numel() != (1 << L):
+        raise ValueError("lut must have 2^L entries")
+    return n, K, E, N, L
+
+
+def tq_grouped_gemm(x, packed, lut, sorted_pairs, topk_w, tiles, num_tiles, top_k: int, tile_m: int,
+                    y32, stream=None) -> None:
+    """y32 += grouped product (y32 fp32 [n, N], zero it for a plain product)."""
+    torch = _torch()
+    n, K, E, N, L = _shapes(x, packed, lut)
+    cap = tiles.shape[0]
+    _check(lib().tq_grouped_gemm(_dev_ptr(x, _bits16(), "x"), _dev_ptr(packed, (torch.uint8,), "packed"),
+                                 _dev_ptr(lut, _bits16(), "lut"), L,
+                                 _dev_ptr(sorted_pairs, (torch.int32,), "sorted_pairs"),
+                                 _dev_ptr(topk_w, (torch.float32,), "topk_w"),
+                                 _dev_ptr(tiles, (torch.int32,), "tiles"),
+                                 _dev_ptr(num_tiles, (torch.int32,), "num_tiles"), cap, n, top_k, E, K, N,
+                                 tile_m, _dev_ptr(y32, (torch.float32,), "y32"), _stream(stream)),
+           "tq_grouped_gemm")
+
+
+def tq_gemv(x, packed, lut, topk_ids, topk_w, y32, stream=None) -> None:
+    """y32 += per-pair GEMV product."""
+    torch = _torch()
+    n, K, E, N, L = _shapes(x, packed, lut)
+    top_k = topk_ids.shape[1]
+    _check(lib().tq_gemv(_dev_ptr(x, _bits16(), "x"), _dev_ptr(packed, (torch.uint8,), "packed"),
+                         _dev_ptr(lut, _bits16(), "lut"), L, _dev_ptr(topk_ids, (torch.int32,), "topk_ids"),
+                         _dev_ptr(topk_w, (torch.float32,), "topk_w"), n, top_k, E, K, N,
+                         _dev_ptr(y32, (torch.float32,), "y32"), _stream(stream)), "tq_gemv")
+
+
+def tq_combine(y32, y=None, stream=None):
+    """bf16 (round to nearest even) copy of y32."""
+    torch = _torch()
+    y = torch.empty(y32.shape, dtype=torch.bfloat16, device=y32.device) if y is None else y
+    _check(lib().tq_combine(_dev_ptr(y32, (torch.float32,), "y32"), _dev_ptr(y, _bits16(), "y"),
+                            y32.numel(), _stream(stream)), "tq_combine")
+    return y
+
+
+def tq_moe_workspace_size(n: int, top_k: int, E: int, N: int, tile_m: int) -> int:
+    return int(lib().tq_moe_workspace_size(n, top_k, E, N, tile_m))
+
+
+def tq_moe_forward(x, packed, lut, topk_ids, topk_w, tile_m: int = 16, pin: int = ARM_AUTO,
+                   workspace=None, y=None, stream=None):
+    """Whole routed-expert product -> (y bf16 [n, N], arm used)."""
+    torch = _torch()
+    n, K, E, N, L = _shapes(x, packed, lut)
+    top_k = topk_ids.shape[1]
+    need = tq_moe_workspace_size(n, top_k, E, N, tile_m)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    y = torch.empty((n, N), dtype=torch.bfloat16, device=x.device) if y is None else y
+    arm = ctypes.c_int(-1)
+    _check(lib().tq_moe_forward(_dev_ptr(x, _bits16(), "x"), _dev_ptr(packed, (torch.uint8,), "packed"),
+                                _dev_ptr(lut, _bits16(), "lut"), L,
+                                _dev_ptr(topk_ids, (torch.int32,), "topk_ids"),
+                                _dev_ptr(topk_w, (torch.float32,), "topk_w"), n, top_k, E, K, N, tile_m, pin,
+                                _dev_ptr(workspace, (torch.uint8,), "workspace"), workspace.numel(),
+                                _dev_ptr(y, _bits16(), "y"), ctypes.byref(arm), _stream(stream)),
+           "tq_moe_forward")
+    return y, arm.value
+
+
+def tq_device_error() -> tuple[int, int]:
+    """(code, where) of the first device-side error since the last call; clears it."""
+    code, where = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().tq_device_error(ctypes.byref(code), ctypes.byref(where)), "tq_device_error")
+    return code.value, where.value
+
+
+def tq_launch_counts() -> dict:
+    arr = (ctypes.c_int64 * 5)()
+    lib().tq_launch_counts(arr)
+    return dict(zip(("route", "tile_map", "grouped", "gemv", "combine"), list(arr)))

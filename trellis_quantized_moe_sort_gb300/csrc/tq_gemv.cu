@@ -1,0 +1,188 @@
+// Per-pair GEMV arm over 2-bit bitshift-trellis experts.
+//
+// Page "fix(qtip): gate the trellis grouped GEMM on m-tile occupancy, not token
+// count", section "The regression" and the post-merge note: below the
+// amortization boundary (and always for n <= 8) each (token, expert) pair runs
+// its own GEMV, re-reading and re-decoding the expert once per pair (no
+// de-duplication across pairs).
+//
+// GB300 design: one CTA per SM holds the fp16 LUT in shared memory.  A warp
+// takes a work item (pair, group of RG consecutive weight rows).  It keeps the
+// token's activations in registers (lane l holds the 64-element chunks
+// l, l+32, ... of x[t]) and, for each row, loads the row's packed bytes with
+// coalesced 16-byte loads (lane l takes bytes [16c, 16c+16) of chunk c), gets
+// the 4 bytes before its chunk from the neighbour lane by shuffle (lane 0 from
+// lane 31 of the previous pass, zero at the row start), decodes its 64
+// symbols by window identity, multiplies in fp32 (fp16 weights widened
+// exactly) and reduces the row over the warp with xor shuffles.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+constexpr int kChunkSyms = 64;  // symbols per lane per pass (16 packed bytes)
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+template <int L, int CPL, int THREADS>
+__global__ void __launch_bounds__(THREADS, 1)
+gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
+            const uint16_t* __restrict__ lut, const int32_t* __restrict__ topk_ids,
+            const float* __restrict__ topk_w, int P, int top_k, int E, int K, int N, int rg,
+            float* __restrict__ y32, int* err) {
+  extern __shared__ __align__(16) uint16_t lut_s[];
+  constexpr int kEntries = 1 << L;
+  if constexpr (kEntries >= 8) {
+    const uint4* src = reinterpret_cast<const uint4*>(lut);
+    uint4* dst = reinterpret_cast<uint4*>(lut_s);
+    for (int i = threadIdx.x; i < kEntries / 8; i += THREADS) dst[i] = __ldg(src + i);
+  } else {
+    for (int i = threadIdx.x; i < kEntries; i += THREADS) lut_s[i] = lut[i];
+  }
+  __syncthreads();
+  const uint32_t lut_base = smem_u32(lut_s);
+
+  const int lane = threadIdx.x & 31;
+  const int warps_per_block = THREADS / 32;
+  const long long gwarp = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
+  const long long nwarps = static_cast<long long>(gridDim.x) * warps_per_block;
+  const int groups = N / rg;
+  const long long items = static_cast<long long>(P) * groups;
+  const int nchunks = K / kChunkSyms;
+  const size_t row_bytes = static_cast<size_t>(K / 4);
+
+  for (long long it = gwarp; it < items; it += nwarps) {
+    const int pair = static_cast<int>(it / groups);
+    const int g = static_cast<int>(it - static_cast<long long>(pair) * groups);
+    const int tok = pair / top_k;
+    const int e = topk_ids[pair];
+    if (e < 0 || e >= E) {
+      if (lane == 0 && g == 0) record_error(err, TQ_ERR_INVALID_ARG, kWhereRoute);
+      continue;
+    }
+    const float wt = topk_w[pair];
+
+    // activations of this token: chunk c = lane + 32 i, 64 bf16 = 32 words
+    uint32_t xr[CPL][32];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nchunks) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(tok) * K + c * kChunkSyms);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 q = __ldg(src + v);
+          xr[i][4 * v] = q.x;
+          xr[i][4 * v + 1] = q.y;
+          xr[i][4 * v + 2] = q.z;
+          xr[i][4 * v + 3] = q.w;
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < 32; ++v) xr[i][v] = 0u;
+      }
+    }
+
+    const uint8_t* erow = packed + (static_cast<size_t>(e) * N + static_cast<size_t>(g) * rg) * row_bytes;
+    for (int r = 0; r < rg; ++r) {
+      const uint8_t* rowp = erow + static_cast<size_t>(r) * row_bytes;
+      float acc = 0.f;
+      uint32_t carry = 0u;  // last word of chunk (32 i - 1), held by lane 31
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        const int c = lane + 32 * i;
+        uint4 q = make_uint4(0u, 0u, 0u, 0u);
+        if (c < nchunks) q = __ldg(reinterpret_cast<const uint4*>(rowp) + c);
+        uint32_t prev = __shfl_up_sync(0xffffffffu, q.w, 1);
+        if (lane == 0) prev = carry;
+        carry = __shfl_sync(0xffffffffu, q.w, 31);
+        if (c < nchunks) {
+          const uint32_t words[5] = {prev, q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) {
+            const uint64_t lo64 = static_cast<uint64_t>(words[wi]) | (static_cast<uint64_t>(words[wi + 1]) << 32);
+#pragma unroll
+            for (int m = 0; m < 16; m += 2) {
+              const uint32_t o0 = static_cast<uint32_t>(lo64 >> (33 + 2 * m - L)) & ((1u << (L + 1)) - 2u);
+              const uint32_t o1 = static_cast<uint32_t>(lo64 >> (35 + 2 * m - L)) & ((1u << (L + 1)) - 2u);
+              uint32_t h0, h1;
+              asm volatile("ld.shared.u16 %0, [%1];" : "=r"(h0) : "r"(lut_base + o0));
+              asm volatile("ld.shared.u16 %0, [%1];" : "=r"(h1) : "r"(lut_base + o1));
+              const uint32_t xv = xr[i][wi * 8 + m / 2];
+              acc = fmaf(__half2float(__ushort_as_half(static_cast<unsigned short>(h0))), bf16lo(xv), acc);
+              acc = fmaf(__half2float(__ushort_as_half(static_cast<unsigned short>(h1))), bf16hi(xv), acc);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) atomicAdd(y32 + static_cast<size_t>(tok) * N + static_cast<size_t>(g) * rg + r, acc * wt);
+    }
+  }
+}
+
+template <int L, int CPL>
+int launch_one(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, const int32_t* ids,
+               const float* w, int P, int top_k, int E, int K, int N, float* y32, int* err,
+               cudaStream_t s) {
+  constexpr int kThreads = (CPL >= 2) ? 256 : 512;
+  auto kfn = gemv_kernel<L, CPL, kThreads>;
+  const size_t smem = std::max<size_t>(16, sizeof(uint16_t) << L);
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return TQ_ERR_CUDA;
+  }
+  const int sms = sm_count();
+  const long long warps = static_cast<long long>(sms) * (kThreads / 32);
+  // rows per work item: as many as keep >= 4 items per warp (1..16, divides N)
+  int rg = 16;
+  while (rg > 1 && (static_cast<long long>(P) * (N / rg) < 4 * warps || N % rg != 0)) rg >>= 1;
+  const long long items = static_cast<long long>(P) * (N / rg);
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(sms, (items + kThreads / 32 - 1) / (kThreads / 32))));
+  kfn<<<grid, kThreads, smem, s>>>(x, packed, lut, ids, w, P, top_k, E, K, N, rg, y32, err);
+  return launch_status();
+}
+
+template <int L>
+int launch_L(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, const int32_t* ids,
+             const float* w, int P, int top_k, int E, int K, int N, float* y32, int* err,
+             cudaStream_t s) {
+  const int nchunks = K / kChunkSyms;
+  if (nchunks <= 32) return launch_one<L, 1>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s);
+  if (nchunks <= 64) return launch_one<L, 2>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s);
+  return launch_one<L, 4>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s);
+}
+
+}  // namespace
+
+int launch_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
+                const int32_t* topk_ids, const float* topk_w, int64_t n, int top_k, int E, int K,
+                int N, float* y32, int* err, cudaStream_t s) {
+  const int P = static_cast<int>(n * top_k);
+  if (P == 0) return TQ_OK;
+  int st;
+  switch (L) {
+    case 2: st = launch_L<2>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
+    case 4: st = launch_L<4>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
+    case 6: st = launch_L<6>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
+    case 8: st = launch_L<8>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
+    case 10: st = launch_L<10>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
+    case 12: st = launch_L<12>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
+    case 14: st = launch_L<14>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
+    case 16: st = launch_L<16>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
+    default: return TQ_ERR_INVALID_ARG;
+  }
+  if (st == TQ_OK) count_launch(kCntGemv);
+  return st;
+}
+
+}  // namespace tq

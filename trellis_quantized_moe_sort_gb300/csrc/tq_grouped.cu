@@ -1,0 +1,568 @@
+// Grouped GEMM over 2-bit bitshift-trellis experts with the decode fused into
+// the multiply, for sm_103a (tcgen05 tensor cores, tensor memory, TMA).
+//
+// What it computes (page "fix(qtip): gate the trellis grouped GEMM on m-tile
+// occupancy, not token count", section "The cause is a threshold, not a kernel
+// defect"): pairs are sorted by expert and grouped into m-tiles; for each
+// m-tile the expert's packed bytes are staged once and every pair of the tile
+// is multiplied against them.  Page "perf(qtip): arch-specialise the trellis
+// grouped GEMM (D16) + close the silent-failure holes (D18)", item 2 and "The
+// two changes": a thread owns a run of 32 symbols of one weight row, seeds the
+// trellis state once from the window identity and steps the recurrence; only
+// packed 2-bit bytes cross HBM and full-size weights never materialise.
+//
+// GB300 design (one persistent CTA per SM, warp-specialised):
+//   warp 0      TMA producer: per 64-symbol k-step, one 2-D box of the expert's
+//               128 packed rows (16 history bytes + 16 bytes) and one 128-byte
+//               box per pair of the tile's activation rows (128B-swizzled).
+//   warp 1      MMA issuer: tcgen05.mma kind::f16, A = decoded weights in tensor
+//               memory (M = 128 rows), B = activations in shared memory
+//               (N = pairs of the tile padded to 16), fp32 accumulator in
+//               tensor memory.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator, scale by the router
+//               weight, fp32 atomic add into y32[token][row].
+//   warps 6-13  decode: thread (quarter q, half h) owns weight row 32q + lane
+//               and symbols [32h, 32h + 32) of each k-step; the state of each
+//               symbol is a 16-bit window of the staged bytes (shift + mask),
+//               looked up in a bf16 copy of the LUT held in shared memory, and
+//               the 32 bf16 weights go to tensor memory with tcgen05.st.
+// Work unit = (m-tile, 128-row block of N), strided over the CTAs.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+constexpr int kBlockRows = 128;                      // weight rows per unit (MMA M)
+constexpr int kKStep = 64;                           // symbols per pipeline step
+constexpr int kKStepBytes = kKStep / 4;              // 16 packed bytes per row per step
+constexpr int kHistBytes = 16;                       // bytes staged ahead of each step
+constexpr int kPkRowBytes = kHistBytes + kKStepBytes;
+constexpr int kPkStageBytes = kBlockRows * kPkRowBytes;  // 4 KiB
+constexpr int kActRowBytes = kKStep * 2;             // one 128-byte swizzle row per pair
+constexpr int kATmemCols = kKStep / 2;               // bf16x2 columns per A stage
+constexpr int kNumAStages = 4;
+constexpr int kNumDecodeWarps = 8;
+constexpr int kNumEpiWarps = 4;
+constexpr int kWarpProducer = 0;
+constexpr int kWarpMma = 1;
+constexpr int kWarpEpi0 = 2;
+constexpr int kWarpDec0 = kWarpEpi0 + kNumEpiWarps;
+constexpr int kThreads = 32 * (kWarpDec0 + kNumDecodeWarps);  // 448
+constexpr int kMaxStages = 8;
+constexpr int kMaxTileM = 256;
+constexpr int kSmemLimit = 232448;                   // 227 KiB opt-in per block
+static_assert(kNumDecodeWarps == 8, "decode mapping assumes 2 warps per TMEM lane quarter");
+static_assert(kWarpEpi0 % 4 == 2 && kWarpDec0 % 4 == 2, "role warps must cover all four quarters");
+
+struct Params {
+  const int32_t* sorted_pairs;
+  const float* topk_w;
+  const int32_t* tiles;
+  const int32_t* num_tiles;
+  const uint16_t* lut;
+  float* y32;
+  int* err;
+  long long cap;
+  int P, E, tile_m;
+  int top_k, N, K;
+  int row_blocks;
+  int n_mma_max;    // largest MMA N (tile_m rounded up to 16)
+  int num_stages;   // shared-memory pipeline depth
+  int nacc;         // accumulator buffers in tensor memory (1 or 2)
+  int tmem_cols;    // allocated tensor-memory columns
+  uint32_t off_pk, off_lut, off_bar;  // byte offsets from the 1024-aligned base
+};
+
+struct Pipe {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void advance(int n) {
+    if (++stage == n) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// A tile entry is used only if it describes 1..tile_m consecutive sorted slots
+// of an existing expert; anything else (a map built for another tile_m, a
+// stale buffer) is skipped by every role alike and reported.
+struct Tile {
+  int e, slot0, rows;
+  bool ok;
+};
+__device__ __forceinline__ Tile read_tile(const Params& p, int tile) {
+  Tile t;
+  t.e = p.tiles[3 * tile];
+  t.slot0 = p.tiles[3 * tile + 1];
+  t.rows = p.tiles[3 * tile + 2];
+  t.ok = t.e >= 0 && t.e < p.E && t.rows >= 1 && t.rows <= p.tile_m && t.slot0 >= 0 &&
+         t.slot0 <= p.P - t.rows;
+  return t;
+}
+
+template <int L>
+__device__ __forceinline__ uint32_t lut_byte_offset_lo(uint64_t lo64, int m) {
+  // state of run symbol m (< 16): bits [34 + 2m - L, 34 + 2m) of lo64; times 2
+  return static_cast<uint32_t>(lo64 >> (33 + 2 * m - L)) & ((1u << (L + 1)) - 2u);
+}
+template <int L>
+__device__ __forceinline__ uint32_t lut_byte_offset_hi(uint64_t cur, int m) {
+  // state of run symbol m (>= 16): bits [2 + 2m - L, 2 + 2m) of the 8 run bytes
+  return static_cast<uint32_t>(cur >> (1 + 2 * m - L)) & ((1u << (L + 1)) - 2u);
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t lds_u64(uint32_t addr) {
+  uint64_t v;
+  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+template <int L>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_constant__ CUtensorMap tm_x,
+               const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.num_stages;
+
+  const uint32_t act0 = base;                                  // S x n_mma_max x 128 B
+  const uint32_t pk0 = base + p.off_pk;                        // S x 4 KiB
+  const uint32_t lut_s = base + p.off_lut;                     // 2^L bf16
+  const uint32_t bar_full = base + p.off_bar;                  // S
+  const uint32_t bar_empty = bar_full + 8 * kMaxStages;        // S
+  const uint32_t bar_afull = bar_empty + 8 * kMaxStages;       // kNumAStages
+  const uint32_t bar_aempty = bar_afull + 8 * kNumAStages;     // kNumAStages
+  const uint32_t bar_accfull = bar_aempty + 8 * kNumAStages;   // 2
+  const uint32_t bar_accempty = bar_accfull + 16;              // 2
+  const uint32_t bar_drain = bar_accempty + 16;                // 1
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + p.off_bar + 8 * (2 * kMaxStages + 2 * kNumAStages + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kNumDecodeWarps + 1);
+    }
+    for (int a = 0; a < kNumAStages; ++a) {
+      mbar_init(bar_afull + 8 * a, kNumDecodeWarps);
+      mbar_init(bar_aempty + 8 * a, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_accfull + 8 * b, 1);
+      mbar_init(bar_accempty + 8 * b, kNumEpiWarps);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == kWarpProducer) tmem_alloc(smem_u32(tmem_holder), static_cast<uint32_t>(p.tmem_cols));
+
+  // LUT: fp16 (global) -> bf16 (shared), nearest-even.
+  {
+    constexpr int kEntries = 1 << L;
+    uint16_t* lut_dst = reinterpret_cast<uint16_t*>(gbase + p.off_lut);
+    if constexpr (kEntries >= 8) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.lut);
+      uint4* dst = reinterpret_cast<uint4*>(lut_dst);
+      for (int i = threadIdx.x; i < kEntries / 8; i += kThreads) {
+        uint4 v = __ldg(src + i);
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __half2 h = *reinterpret_cast<const __half2*>(&w[j]);
+          const float2 f = __half22float2(h);
+          const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+          w[j] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else {
+      for (int i = threadIdx.x; i < kEntries; i += kThreads) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(__half2float(__ushort_as_half(p.lut[i])));
+        lut_dst[i] = *reinterpret_cast<const uint16_t*>(&b);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+
+  const int num_tiles = static_cast<int>(min(static_cast<long long>(*p.num_tiles), p.cap));
+  const int total_units = num_tiles * p.row_blocks;
+  const int ksteps = p.K / kKStep;
+  const uint32_t acol0 = static_cast<uint32_t>(p.nacc * p.n_mma_max);
+
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_packed);
+      tma_prefetch_desc(&tm_x);
+    }
+    Pipe pipe;
+    long long issued = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      const int tile = u / p.row_blocks, rb = u - tile * p.row_blocks;
+      const Tile tl = read_tile(p, tile);
+      if (!tl.ok) {
+        if (lane == 0 && rb == 0) record_error(p.err, TQ_ERR_INVALID_ARG, kWhereGroupedProducer);
+        continue;
+      }
+      const int e = tl.e, slot0 = tl.slot0, rows = tl.rows;
+      int tok[kMaxTileM / 32];
+#pragma unroll
+      for (int j = 0; j < kMaxTileM / 32; ++j) {
+        const int i = lane + 32 * j;
+        const int pair = (i < rows) ? p.sorted_pairs[slot0 + i] : 0;
+        // an out-of-range pair id reads a zero-filled row (TMA bounds) and is
+        // skipped by the epilogue
+        tok[j] = (pair >= 0 && pair < p.P) ? pair / p.top_k : p.P;
+      }
+      const int row_g = e * p.N + rb * kBlockRows;
+      const uint32_t tx = kPkStageBytes + static_cast<uint32_t>(rows) * kActRowBytes;
+      for (int ks = 0; ks < ksteps; ++ks) {
+        if (!mbar_wait(bar_empty + 8 * pipe.stage, pipe.phase ^ 1u, abort_flag, p.err,
+                       kWhereGroupedProducer)) {
+          ok = false;
+          break;
+        }
+        __syncwarp();
+        const uint32_t full = bar_full + 8 * pipe.stage;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, tx);
+          tma_load_2d(pk0 + pipe.stage * kPkStageBytes, &tm_packed, ks * kKStepBytes - kHistBytes,
+                      row_g, full);
+        }
+        const uint32_t act = act0 + static_cast<uint32_t>(pipe.stage * p.n_mma_max * kActRowBytes);
+#pragma unroll
+        for (int j = 0; j < kMaxTileM / 32; ++j) {
+          const int i = lane + 32 * j;
+          if (i < rows) tma_load_2d(act + i * kActRowBytes, &tm_x, ks * kKStep, tok[j], full);
+        }
+        ++issued;
+        pipe.advance(S);
+      }
+    }
+    // Teardown: every copy issued must have landed before the CTA exits.
+    __syncwarp();
+    const long long pending = min(issued, static_cast<long long>(S));
+    for (long long k = 1; k <= pending; ++k) {
+      int st = pipe.stage - static_cast<int>(k);
+      uint32_t ph = pipe.phase;
+      if (st < 0) {
+        st += S;
+        ph ^= 1u;
+      }
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(bar_full + 8 * st, ph)) {
+        if (globaltimer() - t0 > kWaitTimeoutNs) {
+          record_error(p.err, TQ_ERR_DEVICE_TIMEOUT, kWhereGroupedTeardown);
+          break;
+        }
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    Pipe pipe, apipe, accp;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      const int tile = u / p.row_blocks;
+      const Tile tl = read_tile(p, tile);
+      if (!tl.ok) continue;
+      const int rows = tl.rows;
+      const uint32_t n_mma = static_cast<uint32_t>((rows + 15) & ~15);
+      const uint32_t idesc = idesc_bf16_f32(kBlockRows, n_mma);
+      if (!mbar_wait(bar_accempty + 8 * accp.stage, accp.phase ^ 1u, abort_flag, p.err, kWhereGroupedMma)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(accp.stage * p.n_mma_max);
+      for (int ks = 0; ks < ksteps; ++ks) {
+        if (!mbar_wait(bar_full + 8 * pipe.stage, pipe.phase, abort_flag, p.err, kWhereGroupedMma) ||
+            !mbar_wait(bar_afull + 8 * apipe.stage, apipe.phase, abort_flag, p.err, kWhereGroupedMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_tmem = tmem_base + acol0 + static_cast<uint32_t>(apipe.stage * kATmemCols);
+          const uint32_t act = act0 + static_cast<uint32_t>(pipe.stage * p.n_mma_max * kActRowBytes);
+#pragma unroll
+          for (int kk = 0; kk < kKStep / 16; ++kk) {
+            mma_bf16_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(act + kk * 32), idesc,
+                        (ks | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(bar_empty + 8 * pipe.stage);
+          mma_commit(bar_aempty + 8 * apipe.stage);
+        }
+        __syncwarp();
+        pipe.advance(S);
+        apipe.advance(kNumAStages);
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(bar_accfull + 8 * accp.stage);
+      __syncwarp();
+      accp.advance(p.nacc);
+    }
+    // Drain: every MMA issued by this warp has completed before teardown.
+    if (lane == 0) {
+      mma_commit(bar_drain);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(bar_drain, 0)) {
+        if (globaltimer() - t0 > kWaitTimeoutNs) {
+          record_error(p.err, TQ_ERR_DEVICE_TIMEOUT, kWhereGroupedTeardown);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < kWarpDec0) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    Pipe accp;
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+      const int tile = u / p.row_blocks, rb = u - tile * p.row_blocks;
+      const Tile tl = read_tile(p, tile);
+      if (!tl.ok) continue;
+      const int slot0 = tl.slot0, rows = tl.rows;
+      if (!mbar_wait(bar_accfull + 8 * accp.stage, accp.phase, abort_flag, p.err, kWhereGroupedEpilogue)) break;
+      tc_fence_after();
+      const int row = rb * kBlockRows + 32 * q + lane;
+      const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                             static_cast<uint32_t>(accp.stage * p.n_mma_max);
+      for (int c0 = 0; c0 < rows; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(t_acc + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (c0 + i < rows) {
+            const int pair = p.sorted_pairs[slot0 + c0 + i];
+            if (pair < 0 || pair >= p.P) {
+              if (lane == 0) record_error(p.err, TQ_ERR_INVALID_ARG, kWhereGroupedEpilogue);
+              continue;
+            }
+            const int tok = pair / p.top_k;
+            atomicAdd(p.y32 + static_cast<size_t>(tok) * p.N + row, __uint_as_float(v[i]) * p.topk_w[pair]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_accempty + 8 * accp.stage);
+      accp.advance(p.nacc);
+    }
+  } else {
+    // ------------------------------------------------------------ decode
+    const int dw = warp - kWarpDec0;
+    const int q = warp & 3;
+    const int h = dw >> 2;
+    const int row = 32 * q + lane;
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acol0 +
+                            static_cast<uint32_t>(16 * h);
+    Pipe pipe, apipe;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      if (!read_tile(p, u / p.row_blocks).ok) continue;
+      for (int ks = 0; ks < ksteps; ++ks) {
+        if (!mbar_wait(bar_full + 8 * pipe.stage, pipe.phase, abort_flag, p.err, kWhereGroupedDecode)) {
+          ok = false;
+          break;
+        }
+        const uint32_t src = pk0 + pipe.stage * kPkStageBytes + row * kPkRowBytes + kHistBytes + 8 * h;
+        const uint32_t prev = lds_u32(src - 4);
+        const uint64_t cur = lds_u64(src);
+        const uint64_t lo64 = static_cast<uint64_t>(prev) | (cur << 32);
+        uint32_t off[32];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) off[m] = lut_byte_offset_lo<L>(lo64, m);
+#pragma unroll
+        for (int m = 16; m < 32; ++m) off[m] = lut_byte_offset_hi<L>(cur, m);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * pipe.stage);
+        pipe.advance(S);
+
+        uint32_t w[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const uint32_t a = lds_u16(lut_s + off[2 * m]);
+          const uint32_t b = lds_u16(lut_s + off[2 * m + 1]);
+          w[m] = a | (b << 16);
+        }
+        if (!mbar_wait(bar_aempty + 8 * apipe.stage, apipe.phase ^ 1u, abort_flag, p.err, kWhereGroupedDecode)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st16(t_lane + static_cast<uint32_t>(apipe.stage * kATmemCols), w);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_afull + 8 * apipe.stage);
+        apipe.advance(kNumAStages);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpProducer) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+  }
+}
+
+using GroupedFn = void (*)(CUtensorMap, CUtensorMap, Params);
+
+template <int L>
+void* kernel_ptr() {
+  return reinterpret_cast<void*>(&grouped_kernel<L>);
+}
+
+void* grouped_kernel_for(int L) {
+  switch (L) {
+    case 2: return kernel_ptr<2>();
+    case 4: return kernel_ptr<4>();
+    case 6: return kernel_ptr<6>();
+    case 8: return kernel_ptr<8>();
+    case 10: return kernel_ptr<10>();
+    case 12: return kernel_ptr<12>();
+    case 14: return kernel_ptr<14>();
+    case 16: return kernel_ptr<16>();
+    default: return nullptr;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+}  // namespace
+
+int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
+                   const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
+                   const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
+                   int tile_m, float* y32, int* err, cudaStream_t s) {
+  auto encode = encode_fn();
+  if (!encode) return TQ_ERR_CUDA;
+  void* kfn = grouped_kernel_for(L);
+  if (!kfn) return TQ_ERR_INVALID_ARG;
+
+  Params p{};
+  p.sorted_pairs = sorted_pairs;
+  p.topk_w = topk_w;
+  p.tiles = tiles;
+  p.num_tiles = num_tiles;
+  p.lut = lut;
+  p.y32 = y32;
+  p.err = err;
+  p.cap = cap;
+  p.P = static_cast<int>(n * top_k);
+  p.E = E;
+  p.tile_m = tile_m;
+  p.top_k = top_k;
+  p.N = N;
+  p.K = K;
+  p.row_blocks = N / kBlockRows;
+  p.n_mma_max = (tile_m + 15) & ~15;
+  p.nacc = (2 * p.n_mma_max + kNumAStages * kATmemCols <= 512) ? 2 : 1;
+  const int cols_needed = p.nacc * p.n_mma_max + kNumAStages * kATmemCols;
+  int cols = 32;
+  while (cols < cols_needed) cols <<= 1;
+  p.tmem_cols = cols;
+
+  const uint32_t act_stage = static_cast<uint32_t>(p.n_mma_max * kActRowBytes);
+  const uint32_t lut_bytes = std::max<uint32_t>(16u, 2u << L);
+  const uint32_t bar_bytes = 8 * (2 * kMaxStages + 2 * kNumAStages + 5) + 16;
+  int S = kMaxStages;
+  auto total_for = [&](int st) {
+    return 1024u + st * (act_stage + kPkStageBytes) + lut_bytes + bar_bytes;
+  };
+  while (S > 2 && total_for(S) > static_cast<uint32_t>(kSmemLimit)) --S;
+  if (total_for(S) > static_cast<uint32_t>(kSmemLimit)) return TQ_ERR_INVALID_ARG;
+  p.num_stages = S;
+  p.off_pk = S * act_stage;
+  p.off_lut = p.off_pk + S * kPkStageBytes;
+  p.off_bar = (p.off_lut + lut_bytes + 15u) & ~15u;
+  // Ask for more than half of the SM's shared memory so that exactly one CTA
+  // (and one tensor-memory allocation) sits on each SM.
+  const uint32_t smem = std::max<uint32_t>(total_for(S), 120u * 1024u);
+
+  CUtensorMap tm_packed, tm_x;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 4), static_cast<cuuint64_t>(E) * N};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 4)};
+    const cuuint32_t box[2] = {kPkRowBytes, kBlockRows};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tm_packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(packed), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return TQ_ERR_INVALID_ARG;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(n)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {kKStep, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return TQ_ERR_INVALID_ARG;
+  }
+
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return TQ_ERR_CUDA;
+  }
+  const long long units = cap * static_cast<long long>(p.row_blocks);
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(units, sm_count())));
+  void* args[] = {&tm_packed, &tm_x, &p};
+  if (cudaLaunchKernel(kfn, dim3(grid), dim3(kThreads), args, smem, s) != cudaSuccess) {
+    cudaGetLastError();
+    return TQ_ERR_LAUNCH;
+  }
+  const int st = launch_status();
+  if (st == TQ_OK) count_launch(kCntGrouped);
+  return st;
+}
+
+}  // namespace tq

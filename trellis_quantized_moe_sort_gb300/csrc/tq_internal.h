@@ -1,0 +1,42 @@
+// Host-side internals shared by the library's translation units.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "tqmoe.h"
+
+namespace tq {
+
+// Device address of the current device's error word (int[2]: code, where),
+// or nullptr with *status set on failure.
+int* error_word(int* status);
+
+// Checks (and on first use takes) the arch witness for the current device.
+// Refuses during capture of `stream` if the witness has not been cached yet.
+int require_sm103(cudaStream_t stream);
+
+// Converts the last launch error into a status and clears it.
+int launch_status();
+
+enum Counter { kCntRoute = 0, kCntTileMap, kCntGrouped, kCntGemv, kCntCombine, kCntNum };
+void count_launch(Counter c);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Kernel launchers (defined in their own translation units).  Arguments are
+// validated by the caller; these only configure and launch.
+int launch_route(const int32_t* topk_ids, int P, int E, int32_t* counts, int32_t* offsets,
+                 int32_t* sorted_pairs, int* err, cudaStream_t s);
+int launch_tile_map(const int32_t* offsets, int E, int tile_m, int32_t* tiles, int32_t* num_tiles,
+                    int64_t cap, int* err, cudaStream_t s);
+int launch_combine(const float* y32, uint16_t* y, int64_t count, cudaStream_t s);
+int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
+                   const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
+                   const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
+                   int tile_m, float* y32, int* err, cudaStream_t s);
+int launch_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
+                const int32_t* topk_ids, const float* topk_w, int64_t n, int top_k, int E, int K,
+                int N, float* y32, int* err, cudaStream_t s);
+
+}  // namespace tq

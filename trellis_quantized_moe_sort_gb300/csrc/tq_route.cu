@@ -1,0 +1,226 @@
+// Routing sort, m-tile map and the bf16 combine.
+//
+// Routing: the grouped GEMM "sorts pairs by expert and walks
+// sum_e ceil(count_e / GROUPED_TILE_M) m-tiles" (page "fix(qtip): gate the
+// trellis grouped GEMM on m-tile occupancy, not token count", section "The
+// cause is a threshold, not a kernel defect").  The sort here is a stable
+// counting sort done by one thread block: each warp owns a contiguous slice of
+// the pair list, so ranking lanes with equal experts (match.any) inside a warp
+// and offsetting by the counts of lower warps keeps ascending pair order.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+constexpr int kBlock = 1024;
+constexpr int kWarps = kBlock / 32;
+
+// Exclusive scan of one int per thread over the whole 1024-thread block.
+// Returns the exclusive prefix; *total receives the block sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total) {
+  __shared__ int warp_sums[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sums[lane];
+    int si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, si, o);
+      if (lane >= o) si += t;
+    }
+    warp_sums[lane] = si - s;  // exclusive prefix of warp sums
+    __syncwarp();
+  }
+  __syncthreads();
+  const int excl = warp_sums[warp] + incl - v;
+  // block total: last thread's inclusive value
+  __shared__ int blk_total;
+  if (threadIdx.x == kBlock - 1) blk_total = excl + v;
+  __syncthreads();
+  *total = blk_total;
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(kBlock, 1)
+route_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ counts,
+             int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pairs, int* err) {
+  extern __shared__ int32_t wcnt[];  // [kWarps][E]: per-warp count, then per-warp base
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kWarps * E; i += kBlock) wcnt[i] = 0;
+  __syncthreads();
+
+  const int per_warp = (((P + kWarps - 1) / kWarps) + 31) & ~31;
+  const int beg = min(P, warp * per_warp);
+  const int end = min(P, beg + per_warp);
+  int32_t* mine = wcnt + warp * E;
+
+  // 1. per-warp histogram of its slice
+  for (int base = beg; base < end; base += 32) {
+    const int p = base + lane;
+    int e = -1;
+    if (p < end) {
+      e = ids[p];
+      if (e < 0 || e >= E) {
+        record_error(err, TQ_ERR_INVALID_ARG, kWhereRoute);
+        e = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // 2. totals per expert, exclusive scan over experts, per-warp bases
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < E) {
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = total;
+      total += c;
+    }
+  }
+  int all = 0;
+  const int excl = block_exclusive_scan(total, &all);
+  if (e < E) {
+    counts[e] = total;
+    offsets[e] = excl;
+    for (int w = 0; w < kWarps; ++w) wcnt[w * E + e] += excl;
+  }
+  if (threadIdx.x == 0) offsets[E] = all;
+  __syncthreads();
+
+  // 3. stable scatter: rank among equal experts of lower lanes, then advance
+  const unsigned lower = (1u << lane) - 1u;
+  for (int base = beg; base < end; base += 32) {
+    const int p = base + lane;
+    int ex = -1;
+    if (p < end) {
+      ex = ids[p];
+      if (ex < 0 || ex >= E) ex = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, ex);
+    int slot = 0;
+    if (ex >= 0) slot = mine[ex] + __popc(peers & lower);
+    __syncwarp();
+    if (ex >= 0) {
+      sorted_pairs[slot] = p;
+      if (lane == __ffs(peers) - 1) mine[ex] += __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(kBlock, 1)
+tile_map_kernel(const int32_t* __restrict__ offsets, int E, int tile_m, int32_t* __restrict__ tiles,
+                int32_t* __restrict__ num_tiles, long long cap, int* err) {
+  const int e = threadIdx.x;
+  int cnt = 0, nt = 0, off = 0;
+  if (e < E) {
+    off = offsets[e];
+    cnt = offsets[e + 1] - off;
+    nt = (cnt + tile_m - 1) / tile_m;
+  }
+  int total = 0;
+  const int start = block_exclusive_scan(nt, &total);
+  for (int i = 0; i < nt; ++i) {
+    const long long idx = static_cast<long long>(start) + i;
+    if (idx >= cap) break;
+    int32_t* t = tiles + 3 * idx;
+    t[0] = e;
+    t[1] = off + i * tile_m;
+    t[2] = min(tile_m, cnt - i * tile_m);
+  }
+  if (threadIdx.x == 0) {
+    if (total > cap) {
+      record_error(err, TQ_ERR_CAPACITY, kWhereTileMap);
+      *num_tiles = static_cast<int32_t>(cap);
+    } else {
+      *num_tiles = total;
+    }
+  }
+}
+
+__global__ void combine_kernel_v4(const float4* __restrict__ y32, uint2* __restrict__ y, long long n4) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float4 v = y32[i];
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&a);
+    o.y = *reinterpret_cast<const uint32_t*>(&b);
+    y[i] = o;
+  }
+}
+
+__global__ void combine_kernel_scalar(const float* __restrict__ y32, uint16_t* __restrict__ y,
+                                      long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(y32[i]);
+    y[i] = *reinterpret_cast<const uint16_t*>(&b);
+  }
+}
+
+}  // namespace
+
+int launch_route(const int32_t* topk_ids, int P, int E, int32_t* counts, int32_t* offsets,
+                 int32_t* sorted_pairs, int* err, cudaStream_t s) {
+  const size_t smem = sizeof(int32_t) * kWarps * E;
+  if (cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(sizeof(int32_t) * kWarps * 1024)) != cudaSuccess) {
+    cudaGetLastError();
+    return TQ_ERR_CUDA;
+  }
+  route_kernel<<<1, kBlock, smem, s>>>(topk_ids, P, E, counts, offsets, sorted_pairs, err);
+  const int st = launch_status();
+  if (st == TQ_OK) count_launch(kCntRoute);
+  return st;
+}
+
+int launch_tile_map(const int32_t* offsets, int E, int tile_m, int32_t* tiles, int32_t* num_tiles,
+                    int64_t cap, int* err, cudaStream_t s) {
+  tile_map_kernel<<<1, kBlock, 0, s>>>(offsets, E, tile_m, tiles, num_tiles, (long long)cap, err);
+  const int st = launch_status();
+  if (st == TQ_OK) count_launch(kCntTileMap);
+  return st;
+}
+
+int launch_combine(const float* y32, uint16_t* y, int64_t count, cudaStream_t s) {
+  if (count == 0) return TQ_OK;
+  const int threads = 256;
+  const int max_blocks = sm_count() * 8;
+  const bool vec = (count % 4 == 0) && (reinterpret_cast<uintptr_t>(y32) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(y) % 8 == 0);
+  if (vec) {
+    const long long n4 = count / 4;
+    const int blocks = static_cast<int>(std::min<long long>((n4 + threads - 1) / threads, max_blocks));
+    combine_kernel_v4<<<blocks, threads, 0, s>>>(reinterpret_cast<const float4*>(y32),
+                                                 reinterpret_cast<uint2*>(y), n4);
+  } else {
+    const int blocks = static_cast<int>(std::min<long long>((count + threads - 1) / threads, max_blocks));
+    combine_kernel_scalar<<<blocks, threads, 0, s>>>(y32, y, count);
+  }
+  const int st = launch_status();
+  if (st == TQ_OK) count_launch(kCntCombine);
+  return st;
+}
+
+}  // namespace tq
