@@ -1,0 +1,423 @@
+"""Benchmark of the trellis-quantized MoE grouped GEMM on GB300.
+
+One step = one pass of the routed-expert hot path over one batch: zero the
+fp32 accumulator, routing sort, m-tile map, grouped GEMM (trellis decode fused
+into the tcgen05 multiply, router-weighted combine), bf16 combine.  Default
+workload: DeepSeek-V4-shaped decode, 32 tokens x top-6 of 256 experts,
+K=4096 -> N=2048, 2-bit trellis L=16, TILE_M=16 (192 pairs, ~136 woken experts).
+
+Steps cycle over 4 independent weight sets (as successive layers would), so the
+~285 MB of woken packed bytes a step streams never sits warm in the 129 MB L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import os
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the CPU baseline runs on one core
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import argparse
+import json
+import math
+import platform
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import moe_inputs  # noqa: E402
+
+METRIC = "trellis-MoE grouped GEMM us/call, pairs/s, packed-weight GB/s vs roofline"
+DEFAULT_WORKLOAD = "v4_decode_n32"
+NUM_WEIGHT_SETS = 4
+
+
+# --------------------------------------------------------------- traffic model
+
+def grouped_algorithmic_bytes(num_tiles: int, n: int, top_k: int, K: int, N: int, L: int) -> int:
+    """Bytes the grouped GEMM must move per launch: each m-tile stages its
+    expert's packed rows once (N*K/4 bytes; the pages' bandwidth bound), each
+    pair's activation row is read once (K bf16), the fp32 accumulator is read
+    and written once (n*N*4 each way), plus the fp16 LUT."""
+    return num_tiles * N * K // 4 + n * top_k * K * 2 + n * N * 8 + (2 << L)
+
+
+def grouped_flops(n: int, top_k: int, K: int, N: int) -> int:
+    return 2 * n * top_k * K * N
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# --------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        self.f.close()
+        os.unlink(self.f.name)
+        sm, smax, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = max(smax, float(r[2]))
+                for name, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(name)
+            except Exception:
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- our arm
+
+def _cuda(torch, a):
+    import warnings
+    with warnings.catch_warnings():
+        warnings.simplefilter("ignore")     # read-only numpy buffers: copied to the device anyway
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    import trellis_quantized_moe_sort_gb300 as tq
+    from trellis_quantized_moe_sort_gb300 import build as b
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(tq.lib_path):
+        b.build()
+    if dist is not None:
+        dist.barrier()
+    tq.tq_init(local)
+    shp = moe_inputs.shape(args.workload)
+    n, k, E, K, N, L, T = shp.n, shp.top_k, shp.E, shp.K, shp.N, shp.L, args.tile_m
+    P = n * k
+
+    # ---- resident inputs: args.weight_sets independent layers
+    sets = []
+    for layer in range(args.weight_sets):
+        prob = moe_inputs.make_problem(args.workload, layer=layer)
+        sets.append({"x": _cuda(torch, prob.x_bits.view(np.int16)), "ids": _cuda(torch, prob.topk_ids),
+                     "w": _cuda(torch, prob.topk_w), "packed": _cuda(torch, prob.packed),
+                     "lut": _cuda(torch, prob.lut_bits.view(np.int16)), "prob": prob})
+    cap = tq.tq_tile_map_capacity(n, k, E, T)
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    sorted_pairs = torch.empty(P, dtype=torch.int32, device="cuda")
+    tiles = torch.empty((cap, 3), dtype=torch.int32, device="cuda")
+    num_tiles = torch.empty(1, dtype=torch.int32, device="cuda")
+    y32 = torch.empty((n, N), dtype=torch.float32, device="cuda")
+    y = torch.empty((n, N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+
+    def step(i, timed_slot=None):
+        s = sets[i % args.weight_sets]
+        y32.zero_()
+        tq.tq_route(s["ids"], E, counts, offsets, sorted_pairs)
+        tq.tq_build_tile_map(offsets, T, cap, tiles, num_tiles)
+        if timed_slot is not None:
+            gev[timed_slot][0].record(stream)
+        tq.tq_grouped_gemm(s["x"], s["packed"], s["lut"], sorted_pairs, s["w"], tiles, num_tiles, k, T, y32)
+        if timed_slot is not None:
+            gev[timed_slot][1].record(stream)
+        tq.tq_combine(y32, y)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    code, where = tq.tq_device_error()
+    if code:
+        raise RuntimeError(f"device error {code} at {where} during warm-up")
+
+    counts_before = tq.tq_launch_counts()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i, timed_slot=i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    counts_after = tq.tq_launch_counts()
+    code, where = tq.tq_device_error()
+    if code:
+        raise RuntimeError(f"device error {code} at {where} during the timed steps")
+    ms_step = t0.elapsed_time(t1) / args.steps
+    grouped_ms = float(np.mean([a.elapsed_time(b_) for a, b_ in gev]))
+    launches = sum(counts_after[key] - counts_before[key] for key in counts_after)
+    if dist is not None:
+        tt = torch.tensor([ms_step, grouped_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step, grouped_ms = float(tt[0]), float(tt[1])
+
+    # tiles per set (device) for the traffic model; correctness spot check vs nothing on the hot path
+    tiles_per_set = []
+    for i in range(args.weight_sets):
+        step(i)
+        torch.cuda.synchronize()
+        tiles_per_set.append(int(num_tiles.item()))
+    mean_tiles = float(np.mean(tiles_per_set))
+
+    # ---- end to end through the public call with host buffers
+    e2e = run_e2e(args, tq, torch, sets, n, k, E, K, N, T)
+
+    if rank != 0:
+        return None
+    hbm, bf16, bf16_sus, peak_src = measured_peaks()
+    alg_bytes = grouped_algorithmic_bytes(int(round(mean_tiles)), n, k, K, N, L)
+    achieved = alg_bytes / (grouped_ms * 1e-3) / 1e9
+    flops = grouped_flops(n, k, K, N)
+    t_hbm_us = alg_bytes / (hbm * 1e9) * 1e6
+    t_tc_us = flops / (bf16_sus * 1e12) * 1e6
+    bound = "hbm" if t_hbm_us >= t_tc_us else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4)}
+    else:
+        tf = flops / (grouped_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(tf, 2), "peak": bf16_sus, "unit": "TFLOP/s",
+                "frac": round(tf / bf16_sus, 4)}
+    roof.update({"traffic": args.traffic, "peak_source": peak_src, "kernel": "grouped_kernel",
+                 "algorithmic_bytes": alg_bytes, "kernel_us": round(grouped_ms * 1e3, 2)})
+
+    us_call = ms_step * 1e3
+    line = {
+        "metric": METRIC,
+        "value": round(us_call, 2),
+        "unit": "us/call",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; uniform random bitstreams, N(0,1/K) fp16 LUT, N(0,1) bf16 activations)",
+        "config": {
+            "workload": f"{args.workload}: E={E} top-{k}, n={n} tokens ({P} pairs), K={K} -> N={N}, "
+                        f"2-bit trellis L={L}, TILE_M={T}",
+            "global_batch": n, "pairs": P, "tile_m": T, "mean_m_tiles": mean_tiles,
+            "l2": f"inputs larger than L2: {args.weight_sets} weight sets cycled, "
+                  f"~{mean_tiles * N * K / 4 / 1e6:.0f} MB of woken packed bytes per step vs 129 MB L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "pairs_per_s": round(world * P / (ms_step * 1e-3), 1),
+        "packed_GBps": round(mean_tiles * N * K / 4 / (grouped_ms * 1e-3) / 1e9, 1),
+        "grouped_kernel_us": round(grouped_ms * 1e3, 2),
+        "roofline": roof,
+        "decode_ceiling": decode_ceiling(mean_tiles, N, K, clk),
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, sets[0]["prob"], budget_s=args.cpu_seconds)
+    return line
+
+
+def decode_ceiling(mean_tiles, N, K, clk):
+    """Every weight of every staged (m-tile, expert) is one random lookup in
+    the 2^16-entry LUT held in shared memory: 32 banks, so at most 32 lookups
+    per SM clock, and about 32/3.5 with the bank conflicts of random
+    addresses.  Reported beside the roofline."""
+    lookups = mean_tiles * N * K
+    mhz = (clk or {}).get("sm_mhz") or 1900.0
+    sms = 152
+    ideal_us = lookups / (sms * mhz * 1e6 * 32) * 1e6
+    random_us = lookups / (sms * mhz * 1e6 * (32 / 3.5)) * 1e6
+    return {"lookups": int(lookups), "conflict_free_us": round(ideal_us, 1),
+            "random_bank_us": round(random_us, 1), "sm_mhz": mhz}
+
+
+def run_e2e(args, tq, torch, sets, n, k, E, K, N, T):
+    """Same step through tq_moe_forward with host buffers: H2D of the batch's
+    activations and routing from pinned memory, the call, D2H of y."""
+    hosts = []
+    for s in sets:
+        prob = s["prob"]
+        hosts.append({
+            "x": torch.from_numpy(prob.x_bits.view(np.int16).copy()).pin_memory(),
+            "ids": torch.from_numpy(np.ascontiguousarray(prob.topk_ids)).pin_memory(),
+            "w": torch.from_numpy(np.ascontiguousarray(prob.topk_w)).pin_memory(),
+        })
+    dx = torch.empty((n, K), dtype=torch.int16, device="cuda")
+    dids = torch.empty((n, k), dtype=torch.int32, device="cuda")
+    dw = torch.empty((n, k), dtype=torch.float32, device="cuda")
+    y = torch.empty((n, N), dtype=torch.bfloat16, device="cuda")
+    yh = torch.empty((n, N), dtype=torch.bfloat16).pin_memory()
+    ws = torch.empty(tq.tq_moe_workspace_size(n, k, E, N, T), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def one(i):
+        h = hosts[i % args.weight_sets]
+        dx.copy_(h["x"], non_blocking=True)
+        dids.copy_(h["ids"], non_blocking=True)
+        dw.copy_(h["w"], non_blocking=True)
+        tq.tq_moe_forward(dx, sets[i % args.weight_sets]["packed"], sets[i % args.weight_sets]["lut"], dids, dw,
+                          tile_m=T, pin=tq.ARM_GROUPED, workspace=ws, y=y)
+        yh.copy_(y, non_blocking=True)
+
+    for i in range(args.warmup):
+        one(i)
+    torch.cuda.synchronize()
+    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(args.steps):
+        one(i)
+    b_.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b_) / args.steps
+    h2d = n * K * 2 + n * k * 4 + n * k * 4
+    return {"value": round(ms * 1e3, 2), "unit": "us/call", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": n * N * 2, "api": "tq_moe_forward (pin=grouped)"}
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def cpu_baseline(workload, prob, budget_s=15.0, rows_per_call=None):
+    """The CPU oracle on the host, one core, on a bounded sample: all pairs of
+    the batch against a subset of output rows; the time scales linearly in the
+    rows, so us/call = time x N / rows."""
+    import oracle.trellis_moe as O
+    s = prob.shape
+    rows_per_call = rows_per_call or 16
+    rng = np.random.Generator(np.random.PCG64(1))
+    done_rows, t_total = 0, 0.0
+    while t_total < budget_s and done_rows < s.N:
+        rows = np.sort(rng.choice(s.N, size=rows_per_call, replace=False))
+        t0 = time.perf_counter()
+        O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L, rows=rows)
+        t_total += time.perf_counter() - t0
+        done_rows += rows_per_call
+    us_call = t_total / done_rows * s.N * 1e6
+    return {"value": round(us_call, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
+            "sample": f"{workload}: all {s.pairs} pairs x {done_rows} of {s.N} output rows "
+                      f"({t_total:.1f} s), scaled by N/rows",
+            "cpu": platform.processor() or platform.machine()}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    prob = moe_inputs.make_problem(args.workload)
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(args.workload, prob, budget_s=max(1.0, args.cpu_seconds / max(args.steps, 1)))
+        if i >= args.warmup:
+            per_step.append(r)
+    value = float(np.mean([r["value"] for r in per_step]))
+    s = prob.shape
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "us/call",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(value / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": f"{args.workload}: E={s.E} top-{s.top_k}, n={s.n}, K={s.K} -> N={s.N}, "
+                               f"L={s.L}, TILE_M={args.tile_m}"},
+        "cpu_baseline": {"value": round(value, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
+                         "sample": per_step[0]["sample"]},
+        "e2e": {"value": round(value, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(moe_inputs.WORKLOADS))
+    ap.add_argument("--tile-m", type=int, default=16)
+    ap.add_argument("--weight-sets", type=int, default=NUM_WEIGHT_SETS,
+                    help="independent weight sets cycled over the steps (defeats L2 reuse)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes (read+write) per grouped launch, if captured for this build")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+        dist = tdist
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, dist)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
