@@ -33,8 +33,9 @@
  *  - Y[t][r] = sum_j topk_w[t][j] * sum_i W_{topk_ids[t][j]}[r][i] * x[t][i].
  *
  * Conventions for every call below:
- *  - Pointers marked (device) are device memory owned by the caller; the
- *    library allocates no device memory and keeps no pointer after returning.
+ *  - Pointers marked (device) are device memory owned by the caller; no call
+ *    allocates device memory or keeps a pointer after returning (the one fixed
+ *    device array the library holds is described at tq_moe_forward_static).
  *  - Calls taking a stream enqueue work on it and return without waiting;
  *    they never synchronize the device.  Status codes report argument and
  *    launch errors only; device-side faults of the data (an expert id out of
@@ -221,6 +222,35 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
                    int64_t n, int top_k, int E, int K, int N, int tile_m, int pin,
                    void* workspace, size_t workspace_bytes,
                    uint16_t* y, int* arm_used, tq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Whole routed-expert product without allocating: tq_moe_forward with its
+ * scratch in a fixed device array inside the library instead of a caller
+ * workspace.  The pages have no counterpart; this exists for callers that
+ * cannot allocate device memory — e.g. a plugin to which a host framework
+ * passes only input and output buffers, or a serving loop that forbids
+ * allocation after start-up because cudaMalloc can block and synchronize.
+ *
+ * Arguments, layouts and results are those of tq_moe_forward minus the
+ * workspace.  The scratch is a file-scope device array of
+ * TQ_STATIC_SCRATCH_BYTES (16 MiB) that every GPU loading this library holds
+ * until the process exits; a shape whose tq_moe_workspace_size() exceeds it
+ * is rejected with TQ_ERR_WORKSPACE before anything is launched (at N = 2048
+ * that is about n > 2000 tokens).  The call allocates nothing (no cudaMalloc,
+ * no cudaFree, no allocating library routine).
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress) and caches it; make that first call
+ * before any stream capture.  Every call on a device shares the one array and
+ * it keeps the last call's contents (each call zeroes what must start at
+ * zero): calls that overlap on the GPU — on different streams or threads —
+ * race and corrupt each other's results; serialize them.
+ * ------------------------------------------------------------------------- */
+#define TQ_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int tq_moe_forward_static(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
+                          const int32_t* topk_ids, const float* topk_w,
+                          int64_t n, int top_k, int E, int K, int N, int tile_m, int pin,
+                          uint16_t* y, int* arm_used, tq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Diagnostics

@@ -19,7 +19,7 @@ __all__ = [
     "TQError", "lib", "lib_path", "tq_init", "tq_arch_witness", "tq_pairs_per_woken_expert",
     "tq_tiles_amortize", "tq_grouped_min_tokens", "tq_tile_map_capacity", "tq_select_arm",
     "tq_route", "tq_build_tile_map", "tq_grouped_gemm", "tq_gemv", "tq_combine",
-    "tq_moe_workspace_size", "tq_moe_forward", "tq_device_error", "tq_launch_counts",
+    "tq_moe_workspace_size", "tq_moe_forward", "tq_moe_forward_static", "tq_device_error", "tq_launch_counts",
     "tq_status_string", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "EXPORTED_SYMBOLS",
 ]
 
@@ -50,6 +50,8 @@ _SIGS = {
     "tq_moe_forward": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int,
                                 _c_int, _c_int, _c_int, _c_int, _c_p, _c_sz, _c_p,
                                 ctypes.POINTER(_c_int), _c_p]),
+    "tq_moe_forward_static": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int,
+                                       _c_int, _c_int, _c_int, _c_int, _c_p, ctypes.POINTER(_c_int), _c_p]),
     "tq_device_error": (_c_int, [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
     "tq_launch_counts": (None, [ctypes.POINTER(_c_i64)]),
 }
@@ -267,6 +269,29 @@ def tq_moe_forward(x, packed, lut, topk_ids, topk_w, tile_m: int = 16, pin: int 
                                 _dev_ptr(workspace, (torch.uint8,), "workspace"), workspace.numel(),
                                 _dev_ptr(y, _bits16(), "y"), ctypes.byref(arm), _stream(stream)),
            "tq_moe_forward")
+    return y, arm.value
+
+
+STATIC_SCRATCH_BYTES = 16 * 1024 * 1024   # TQ_STATIC_SCRATCH_BYTES in include/tqmoe.h
+
+
+def tq_moe_forward_static(x, packed, lut, topk_ids, topk_w, tile_m: int = 16, pin: int = ARM_AUTO,
+                          y=None, stream=None):
+    """Whole routed-expert product with the library's fixed scratch array
+    instead of a workspace (for callers that cannot allocate device memory;
+    here only `y` is allocated, and only when not given) -> (y, arm used).
+    Calls sharing a device must not overlap on the GPU."""
+    torch = _torch()
+    n, K, E, N, L = _shapes(x, packed, lut)
+    top_k = topk_ids.shape[1]
+    y = torch.empty((n, N), dtype=torch.bfloat16, device=x.device) if y is None else y
+    arm = ctypes.c_int(-1)
+    _check(lib().tq_moe_forward_static(_dev_ptr(x, _bits16(), "x"), _dev_ptr(packed, (torch.uint8,), "packed"),
+                                       _dev_ptr(lut, _bits16(), "lut"), L,
+                                       _dev_ptr(topk_ids, (torch.int32,), "topk_ids"),
+                                       _dev_ptr(topk_w, (torch.float32,), "topk_w"), n, top_k, E, K, N, tile_m,
+                                       pin, _dev_ptr(y, _bits16(), "y"), ctypes.byref(arm), _stream(stream)),
+           "tq_moe_forward_static")
     return y, arm.value
 
 
