@@ -8,13 +8,15 @@
 // is multiplied against them.  Page "perf(qtip): arch-specialise the trellis
 // grouped GEMM (D16) + close the silent-failure holes (D18)", item 2 and "The
 // two changes": a thread owns a run of 32 symbols of one weight row, seeds the
-// trellis state once from the window identity and steps the recurrence; only
-// packed 2-bit bytes cross HBM and full-size weights never materialise.
+// trellis state from the window identity; only packed 2-bit bytes cross HBM
+// and full-size weights never materialise.
 //
 // GB300 design (one persistent CTA per SM, warp-specialised):
-//   warp 0      TMA producer: per 64-symbol k-step, one 2-D box of the expert's
-//               128 packed rows (16 history bytes + 16 bytes) and one 128-byte
-//               box per pair of the tile's activation rows (128B-swizzled).
+//   warp 0      TMA producer.  Packed bytes: one 2-D box of the expert's 128
+//               rows x 128 bytes (512 symbols = 8 k-steps of 64) per
+//               "super-stage", 128B-swizzled; wide rows keep the TMA unit's
+//               per-row cost low.  Activations: one 128-byte box per pair of
+//               the tile per k-step, 128B-swizzled into the MMA's B layout.
 //   warp 1      MMA issuer: tcgen05.mma kind::f16, A = decoded weights in tensor
 //               memory (M = 128 rows), B = activations in shared memory
 //               (N = pairs of the tile padded to 16), fp32 accumulator in
@@ -23,10 +25,13 @@
 //               weight, fp32 atomic add into y32[token][row].
 //   warps 6-13  decode: thread (quarter q, half h) owns weight row 32q + lane
 //               and symbols [32h, 32h + 32) of each k-step; the state of each
-//               symbol is a 16-bit window of the staged bytes (shift + mask),
-//               looked up in a bf16 copy of the LUT held in shared memory, and
-//               the 32 bf16 weights go to tensor memory with tcgen05.st.
-// Work unit = (m-tile, 128-row block of N), strided over the CTAs.
+//               symbol is a shift + mask of a 64-bit window of the staged
+//               bytes (window identity), looked up in a bf16 copy of the LUT
+//               held in shared memory, and the 32 bf16 weights go to tensor
+//               memory with tcgen05.st.
+// Work: units = (m-tile, 128-row block of N) x super-stages, split into equal
+// contiguous ranges per CTA (a unit may be shared by two CTAs; the epilogue
+// adds partial sums atomically).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -43,24 +48,27 @@ namespace tq {
 namespace {
 
 constexpr int kBlockRows = 128;                      // weight rows per unit (MMA M)
-constexpr int kKStep = 64;                           // symbols per pipeline step
-constexpr int kKStepBytes = kKStep / 4;              // 16 packed bytes per row per step
-constexpr int kHistBytes = 16;                       // bytes staged ahead of each step
-constexpr int kPkRowBytes = kHistBytes + kKStepBytes;
-constexpr int kPkStageBytes = kBlockRows * kPkRowBytes;  // 4 KiB
+constexpr int kKStep = 64;                           // symbols per MMA step (4 x K16)
+constexpr int kKStepBytes = kKStep / 4;              // 16 packed bytes per row per k-step
+constexpr int kSSBytes = 128;                        // packed bytes per row per super-stage
+constexpr int kSSSteps = kSSBytes / kKStepBytes;     // 8 k-steps per super-stage
+constexpr int kPkStageBytes = kBlockRows * kSSBytes; // 16 KiB
 constexpr int kActRowBytes = kKStep * 2;             // one 128-byte swizzle row per pair
 constexpr int kATmemCols = kKStep / 2;               // bf16x2 columns per A stage
-constexpr int kNumAStages = 4;
+constexpr int kNumAStages = 8;
 constexpr int kNumDecodeWarps = 8;
 constexpr int kNumEpiWarps = 4;
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpEpi0 = 2;
 constexpr int kWarpDec0 = kWarpEpi0 + kNumEpiWarps;
-constexpr int kThreads = 32 * (kWarpDec0 + kNumDecodeWarps);  // 448
-constexpr int kMaxStages = 8;
+constexpr int kWarpActProducer = kWarpDec0 + kNumDecodeWarps;
+constexpr int kThreads = 32 * (kWarpActProducer + 1);  // 480
+constexpr int kMaxPkStages = 6;
+constexpr int kMaxActStages = 8;
 constexpr int kMaxTileM = 256;
 constexpr int kSmemLimit = 232448;                   // 227 KiB opt-in per block
+constexpr int kNumBars = 2 * kMaxPkStages + 2 * kMaxActStages + 2 * kNumAStages + 2 + 2 + 1;
 static_assert(kNumDecodeWarps == 8, "decode mapping assumes 2 warps per TMEM lane quarter");
 static_assert(kWarpEpi0 % 4 == 2 && kWarpDec0 % 4 == 2, "role warps must cover all four quarters");
 
@@ -70,6 +78,7 @@ struct Params {
   const int32_t* tiles;
   const int32_t* num_tiles;
   const uint16_t* lut;
+  const uint8_t* packed;
   float* y32;
   int* err;
   long long cap;
@@ -77,7 +86,8 @@ struct Params {
   int top_k, N, K;
   int row_blocks;
   int n_mma_max;    // largest MMA N (tile_m rounded up to 16)
-  int num_stages;   // shared-memory pipeline depth
+  int pk_stages;    // packed super-stage buffers
+  int act_stages;   // activation k-step buffers
   int nacc;         // accumulator buffers in tensor memory (1 or 2)
   int tmem_cols;    // allocated tensor-memory columns
   uint32_t off_pk, off_lut, off_bar;  // byte offsets from the 1024-aligned base
@@ -111,6 +121,27 @@ __device__ __forceinline__ Tile read_tile(const Params& p, int tile) {
   return t;
 }
 
+// A run of super-stages [ss0, ss1) of one work unit (m-tile `tile`, row block
+// `rb`) starting at flattened position g and ending no later than g_end.
+struct Segment {
+  int tile, rb, ss0, ss1;
+};
+__device__ __forceinline__ Segment segment_at(long long g, long long g_end, int n_ss, int row_blocks) {
+  Segment sg;
+  const long long u = g / n_ss;
+  sg.ss0 = static_cast<int>(g - u * n_ss);
+  sg.ss1 = static_cast<int>(min(static_cast<long long>(n_ss), sg.ss0 + (g_end - g)));
+  sg.tile = static_cast<int>(u / row_blocks);
+  sg.rb = static_cast<int>(u - static_cast<long long>(sg.tile) * row_blocks);
+  return sg;
+}
+
+// Byte offset of logical byte b of staged row r (128-byte pitch) in the
+// 128B-swizzled super-stage: the 16-byte chunk index is XORed with r mod 8.
+__device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t b) {
+  return r * kSSBytes + (b ^ ((r & 7u) << 4));
+}
+
 template <int L>
 __device__ __forceinline__ uint32_t lut_byte_offset_lo(uint64_t lo64, int m) {
   // state of run symbol m (< 16): bits [34 + 2m - L, 34 + 2m) of lo64; times 2
@@ -138,6 +169,47 @@ __device__ __forceinline__ uint64_t lds_u64(uint32_t addr) {
   return v;
 }
 
+// The 32 bf16 weights of one run: window states of the 4 bytes before the run
+// (prev) and the run's 8 bytes (cur), looked up in the shared-memory LUT and
+// packed two per 32-bit word (even symbol in the low half).
+template <int L>
+__device__ __forceinline__ void lookup_run(uint32_t lut_s, uint32_t prev, uint64_t cur, uint32_t (&w)[16]) {
+  const uint64_t lo64 = static_cast<uint64_t>(prev) | (cur << 32);
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const uint32_t a = lds_u16(lut_s + lut_byte_offset_lo<L>(lo64, 2 * m));
+    const uint32_t b = lds_u16(lut_s + lut_byte_offset_lo<L>(lo64, 2 * m + 1));
+    w[m] = a | (b << 16);
+  }
+#pragma unroll
+  for (int m = 8; m < 16; ++m) {
+    const uint32_t a = lds_u16(lut_s + lut_byte_offset_hi<L>(cur, 2 * m));
+    const uint32_t b = lds_u16(lut_s + lut_byte_offset_hi<L>(cur, 2 * m + 1));
+    w[m] = a | (b << 16);
+  }
+}
+
+// Waits (bounded, ignoring the abort flag) for the last `pending` phases of a
+// ring of full barriers to complete: copies in flight must land before exit.
+__device__ __forceinline__ void drain_ring(uint32_t bar0, Pipe pipe, int nstages, long long issued, int* err) {
+  const long long pending = min(issued, static_cast<long long>(nstages));
+  for (long long k = 1; k <= pending; ++k) {
+    int st = pipe.stage - static_cast<int>(k);
+    uint32_t ph = pipe.phase;
+    if (st < 0) {
+      st += nstages;
+      ph ^= 1u;
+    }
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar0 + 8 * st, ph)) {
+      if (globaltimer() - t0 > kWaitTimeoutNs) {
+        record_error(err, TQ_ERR_DEVICE_TIMEOUT, kWhereGroupedTeardown);
+        break;
+      }
+    }
+  }
+}
+
 template <int L>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_constant__ CUtensorMap tm_x,
@@ -149,25 +221,32 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int S = p.num_stages;
+  const int SP = p.pk_stages;
+  const int SA = p.act_stages;
 
-  const uint32_t act0 = base;                                  // S x n_mma_max x 128 B
-  const uint32_t pk0 = base + p.off_pk;                        // S x 4 KiB
+  const uint32_t act0 = base;                                  // SA x n_mma_max x 128 B
+  const uint32_t pk0 = base + p.off_pk;                        // SP x 16 KiB
   const uint32_t lut_s = base + p.off_lut;                     // 2^L bf16
-  const uint32_t bar_full = base + p.off_bar;                  // S
-  const uint32_t bar_empty = bar_full + 8 * kMaxStages;        // S
-  const uint32_t bar_afull = bar_empty + 8 * kMaxStages;       // kNumAStages
-  const uint32_t bar_aempty = bar_afull + 8 * kNumAStages;     // kNumAStages
-  const uint32_t bar_accfull = bar_aempty + 8 * kNumAStages;   // 2
-  const uint32_t bar_accempty = bar_accfull + 16;              // 2
-  const uint32_t bar_drain = bar_accempty + 16;                // 1
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + p.off_bar + 8 * (2 * kMaxStages + 2 * kNumAStages + 5));
+  const uint32_t bar_pkfull = base + p.off_bar;
+  const uint32_t bar_pkempty = bar_pkfull + 8 * kMaxPkStages;
+  const uint32_t bar_actfull = bar_pkempty + 8 * kMaxPkStages;
+  const uint32_t bar_actempty = bar_actfull + 8 * kMaxActStages;
+  const uint32_t bar_afull = bar_actempty + 8 * kMaxActStages;
+  const uint32_t bar_aempty = bar_afull + 8 * kNumAStages;
+  const uint32_t bar_accfull = bar_aempty + 8 * kNumAStages;
+  const uint32_t bar_accempty = bar_accfull + 16;
+  const uint32_t bar_drain = bar_accempty + 16;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + p.off_bar + 8 * kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, kNumDecodeWarps + 1);
+    for (int s = 0; s < SP; ++s) {
+      mbar_init(bar_pkfull + 8 * s, 1);
+      mbar_init(bar_pkempty + 8 * s, kNumDecodeWarps);
+    }
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(bar_actfull + 8 * s, 1);
+      mbar_init(bar_actempty + 8 * s, 1);
     }
     for (int a = 0; a < kNumAStages; ++a) {
       mbar_init(bar_afull + 8 * a, kNumDecodeWarps);
@@ -215,89 +294,101 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
 
   const int num_tiles = static_cast<int>(min(static_cast<long long>(*p.num_tiles), p.cap));
-  const int total_units = num_tiles * p.row_blocks;
   const int ksteps = p.K / kKStep;
+  const int n_ss = (ksteps + kSSSteps - 1) / kSSSteps;
   const uint32_t acol0 = static_cast<uint32_t>(p.nacc * p.n_mma_max);
+  // This CTA's equal share of the flattened (unit, super-stage) work; every
+  // role walks it in the same order, one segment at a time.
+  const long long total = static_cast<long long>(num_tiles) * p.row_blocks * n_ss;
+  const long long g_beg = total * blockIdx.x / gridDim.x;
+  const long long g_end = total * (blockIdx.x + 1) / gridDim.x;
 
   if (warp == kWarpProducer) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_packed);
-      tma_prefetch_desc(&tm_x);
-    }
-    Pipe pipe;
-    long long issued = 0;
+    // ------------------------------------------------------------ packed-byte producer
+    if (lane == 0) tma_prefetch_desc(&tm_packed);
+    Pipe pk;
+    long long pk_issued = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-      const int tile = u / p.row_blocks, rb = u - tile * p.row_blocks;
-      const Tile tl = read_tile(p, tile);
+    for (long long g = g_beg; g < g_end && ok;) {
+      const Segment sg = segment_at(g, g_end, n_ss, p.row_blocks);
+      g += sg.ss1 - sg.ss0;
+      const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) {
-        if (lane == 0 && rb == 0) record_error(p.err, TQ_ERR_INVALID_ARG, kWhereGroupedProducer);
+        if (lane == 0) record_error(p.err, TQ_ERR_INVALID_ARG, kWhereGroupedProducer);
         continue;
       }
-      const int e = tl.e, slot0 = tl.slot0, rows = tl.rows;
+      const int row_g = tl.e * p.N + sg.rb * kBlockRows;
+      for (int ss = sg.ss0; ss < sg.ss1; ++ss) {
+        if (!mbar_wait(bar_pkempty + 8 * pk.stage, pk.phase ^ 1u, abort_flag, p.err, kWhereGroupedProducer)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t full = bar_pkfull + 8 * pk.stage;
+          mbar_arrive_expect_tx(full, kPkStageBytes);
+          tma_load_2d(pk0 + pk.stage * kPkStageBytes, &tm_packed, ss * kSSBytes, row_g, full);
+        }
+        ++pk_issued;
+        pk.advance(SP);
+      }
+    }
+    // Teardown: every copy issued must have landed before the CTA exits.
+    __syncwarp();
+    drain_ring(bar_pkfull, pk, SP, pk_issued, p.err);
+  } else if (warp == kWarpActProducer) {
+    // ------------------------------------------------------------ activation producer
+    if (lane == 0) tma_prefetch_desc(&tm_x);
+    Pipe act;
+    long long act_issued = 0;
+    bool ok = true;
+    for (long long g = g_beg; g < g_end && ok;) {
+      const Segment sg = segment_at(g, g_end, n_ss, p.row_blocks);
+      g += sg.ss1 - sg.ss0;
+      const Tile tl = read_tile(p, sg.tile);
+      if (!tl.ok) continue;
+      const int rows = tl.rows;
       int tok[kMaxTileM / 32];
 #pragma unroll
       for (int j = 0; j < kMaxTileM / 32; ++j) {
         const int i = lane + 32 * j;
-        const int pair = (i < rows) ? p.sorted_pairs[slot0 + i] : 0;
+        const int pair = (i < rows) ? p.sorted_pairs[tl.slot0 + i] : 0;
         // an out-of-range pair id reads a zero-filled row (TMA bounds) and is
         // skipped by the epilogue
         tok[j] = (pair >= 0 && pair < p.P) ? pair / p.top_k : p.P;
       }
-      const int row_g = e * p.N + rb * kBlockRows;
-      const uint32_t tx = kPkStageBytes + static_cast<uint32_t>(rows) * kActRowBytes;
-      for (int ks = 0; ks < ksteps; ++ks) {
-        if (!mbar_wait(bar_empty + 8 * pipe.stage, pipe.phase ^ 1u, abort_flag, p.err,
+      const uint32_t act_tx = static_cast<uint32_t>(rows) * kActRowBytes;
+      const int ks0 = sg.ss0 * kSSSteps, ks1 = min(ksteps, sg.ss1 * kSSSteps);
+      for (int ks = ks0; ks < ks1; ++ks) {
+        if (!mbar_wait(bar_actempty + 8 * act.stage, act.phase ^ 1u, abort_flag, p.err,
                        kWhereGroupedProducer)) {
           ok = false;
           break;
         }
         __syncwarp();
-        const uint32_t full = bar_full + 8 * pipe.stage;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(full, tx);
-          tma_load_2d(pk0 + pipe.stage * kPkStageBytes, &tm_packed, ks * kKStepBytes - kHistBytes,
-                      row_g, full);
-        }
-        const uint32_t act = act0 + static_cast<uint32_t>(pipe.stage * p.n_mma_max * kActRowBytes);
+        const uint32_t full = bar_actfull + 8 * act.stage;
+        if (lane == 0) mbar_arrive_expect_tx(full, act_tx);
+        const uint32_t dst = act0 + static_cast<uint32_t>(act.stage * p.n_mma_max * kActRowBytes);
 #pragma unroll
         for (int j = 0; j < kMaxTileM / 32; ++j) {
           const int i = lane + 32 * j;
-          if (i < rows) tma_load_2d(act + i * kActRowBytes, &tm_x, ks * kKStep, tok[j], full);
+          if (i < rows) tma_load_2d(dst + i * kActRowBytes, &tm_x, ks * kKStep, tok[j], full);
         }
-        ++issued;
-        pipe.advance(S);
+        ++act_issued;
+        act.advance(SA);
       }
     }
-    // Teardown: every copy issued must have landed before the CTA exits.
     __syncwarp();
-    const long long pending = min(issued, static_cast<long long>(S));
-    for (long long k = 1; k <= pending; ++k) {
-      int st = pipe.stage - static_cast<int>(k);
-      uint32_t ph = pipe.phase;
-      if (st < 0) {
-        st += S;
-        ph ^= 1u;
-      }
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(bar_full + 8 * st, ph)) {
-        if (globaltimer() - t0 > kWaitTimeoutNs) {
-          record_error(p.err, TQ_ERR_DEVICE_TIMEOUT, kWhereGroupedTeardown);
-          break;
-        }
-      }
-    }
+    drain_ring(bar_actfull, act, SA, act_issued, p.err);
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    Pipe pipe, apipe, accp;
+    Pipe act, apipe, accp;
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-      const int tile = u / p.row_blocks;
-      const Tile tl = read_tile(p, tile);
+    for (long long g = g_beg; g < g_end && ok;) {
+      const Segment sg = segment_at(g, g_end, n_ss, p.row_blocks);
+      g += sg.ss1 - sg.ss0;
+      const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
-      const int rows = tl.rows;
-      const uint32_t n_mma = static_cast<uint32_t>((rows + 15) & ~15);
+      const uint32_t n_mma = static_cast<uint32_t>((tl.rows + 15) & ~15);
       const uint32_t idesc = idesc_bf16_f32(kBlockRows, n_mma);
       if (!mbar_wait(bar_accempty + 8 * accp.stage, accp.phase ^ 1u, abort_flag, p.err, kWhereGroupedMma)) {
         ok = false;
@@ -305,8 +396,9 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(accp.stage * p.n_mma_max);
-      for (int ks = 0; ks < ksteps; ++ks) {
-        if (!mbar_wait(bar_full + 8 * pipe.stage, pipe.phase, abort_flag, p.err, kWhereGroupedMma) ||
+      const int ks0 = sg.ss0 * kSSSteps, ks1 = min(ksteps, sg.ss1 * kSSSteps);
+      for (int ks = ks0; ks < ks1; ++ks) {
+        if (!mbar_wait(bar_actfull + 8 * act.stage, act.phase, abort_flag, p.err, kWhereGroupedMma) ||
             !mbar_wait(bar_afull + 8 * apipe.stage, apipe.phase, abort_flag, p.err, kWhereGroupedMma)) {
           ok = false;
           break;
@@ -314,17 +406,17 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
         tc_fence_after();
         if (lane == 0) {
           const uint32_t a_tmem = tmem_base + acol0 + static_cast<uint32_t>(apipe.stage * kATmemCols);
-          const uint32_t act = act0 + static_cast<uint32_t>(pipe.stage * p.n_mma_max * kActRowBytes);
+          const uint32_t b_smem = act0 + static_cast<uint32_t>(act.stage * p.n_mma_max * kActRowBytes);
 #pragma unroll
           for (int kk = 0; kk < kKStep / 16; ++kk) {
-            mma_bf16_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(act + kk * 32), idesc,
-                        (ks | kk) != 0 ? 1u : 0u);
+            mma_bf16_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b_smem + kk * 32), idesc,
+                        (ks != ks0 || kk != 0) ? 1u : 0u);
           }
-          mma_commit(bar_empty + 8 * pipe.stage);
+          mma_commit(bar_actempty + 8 * act.stage);
           mma_commit(bar_aempty + 8 * apipe.stage);
         }
         __syncwarp();
-        pipe.advance(S);
+        act.advance(SA);
         apipe.advance(kNumAStages);
       }
       if (!ok) break;
@@ -348,14 +440,15 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     Pipe accp;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-      const int tile = u / p.row_blocks, rb = u - tile * p.row_blocks;
-      const Tile tl = read_tile(p, tile);
+    for (long long g = g_beg; g < g_end;) {
+      const Segment sg = segment_at(g, g_end, n_ss, p.row_blocks);
+      g += sg.ss1 - sg.ss0;
+      const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
       const int slot0 = tl.slot0, rows = tl.rows;
       if (!mbar_wait(bar_accfull + 8 * accp.stage, accp.phase, abort_flag, p.err, kWhereGroupedEpilogue)) break;
       tc_fence_after();
-      const int row = rb * kBlockRows + 32 * q + lane;
+      const int row = sg.rb * kBlockRows + 32 * q + lane;
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(accp.stage * p.n_mma_max);
       for (int c0 = 0; c0 < rows; c0 += 16) {
@@ -385,50 +478,79 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     const int dw = warp - kWarpDec0;
     const int q = warp & 3;
     const int h = dw >> 2;
-    const int row = 32 * q + lane;
+    const uint32_t row = static_cast<uint32_t>(32 * q + lane);
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acol0 +
                             static_cast<uint32_t>(16 * h);
-    Pipe pipe, apipe;
+    const size_t row_bytes = static_cast<size_t>(p.K / 4);
+    Pipe pk, apipe;
+    int pending_afull = -1;   // A stage stored but not yet handed to the MMA
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-      if (!read_tile(p, u / p.row_blocks).ok) continue;
-      for (int ks = 0; ks < ksteps; ++ks) {
-        if (!mbar_wait(bar_full + 8 * pipe.stage, pipe.phase, abort_flag, p.err, kWhereGroupedDecode)) {
-          ok = false;
-          break;
-        }
-        const uint32_t src = pk0 + pipe.stage * kPkStageBytes + row * kPkRowBytes + kHistBytes + 8 * h;
-        const uint32_t prev = lds_u32(src - 4);
-        const uint64_t cur = lds_u64(src);
-        const uint64_t lo64 = static_cast<uint64_t>(prev) | (cur << 32);
-        uint32_t off[32];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) off[m] = lut_byte_offset_lo<L>(lo64, m);
-#pragma unroll
-        for (int m = 16; m < 32; ++m) off[m] = lut_byte_offset_hi<L>(cur, m);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * pipe.stage);
-        pipe.advance(S);
-
-        uint32_t w[16];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const uint32_t a = lds_u16(lut_s + off[2 * m]);
-          const uint32_t b = lds_u16(lut_s + off[2 * m + 1]);
-          w[m] = a | (b << 16);
-        }
-        if (!mbar_wait(bar_aempty + 8 * apipe.stage, apipe.phase ^ 1u, abort_flag, p.err, kWhereGroupedDecode)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        tmem_st16(t_lane + static_cast<uint32_t>(apipe.stage * kATmemCols), w);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_afull + 8 * apipe.stage);
-        apipe.advance(kNumAStages);
+    for (long long g = g_beg; g < g_end && ok;) {
+      const Segment sg = segment_at(g, g_end, n_ss, p.row_blocks);
+      g += sg.ss1 - sg.ss0;
+      const Tile tl = read_tile(p, sg.tile);
+      if (!tl.ok) continue;
+      // 4 stream bytes before the first symbol of the segment (zero at the
+      // row start): symbols of the window that lie in an earlier super-stage.
+      uint32_t carry = 0;
+      if (h == 0 && sg.ss0 > 0) {
+        const uint8_t* rp = p.packed + (static_cast<size_t>(tl.e) * p.N + sg.rb * kBlockRows + row) * row_bytes;
+        carry = __ldg(reinterpret_cast<const uint32_t*>(rp + sg.ss0 * kSSBytes - 4));
       }
+      for (int ss = sg.ss0; ss < sg.ss1 && ok; ++ss) {
+        if (!mbar_wait(bar_pkfull + 8 * pk.stage, pk.phase, abort_flag, p.err, kWhereGroupedDecode)) {
+          ok = false;
+          break;
+        }
+        const uint32_t buf = pk0 + pk.stage * kPkStageBytes;
+        const int nks = min(kSSSteps, ksteps - ss * kSSSteps);
+        // packed words of k-step i: run bytes [16i + 8h, +8) and the 4 bytes
+        // before them; loaded one k-step ahead so their latency overlaps
+        auto load_cur = [&](int i) { return lds_u64(buf + sw128(row, 16 * i + 8 * h)); };
+        auto load_prev = [&](int i) {
+          return h == 1 ? lds_u32(buf + sw128(row, 16 * i + 4))
+                        : (i == 0 ? carry : lds_u32(buf + sw128(row, 16 * i - 4)));
+        };
+        uint64_t cur_n = load_cur(0);
+        uint32_t prev_n = load_prev(0);
+        if (h == 0 && nks == kSSSteps) carry = lds_u32(buf + sw128(row, kSSBytes - 4));
+        for (int i = 0; i < nks && ok; ++i) {
+          const uint64_t cur = cur_n;
+          const uint32_t prev = prev_n;
+          // issue this k-step's LUT loads first, then the next k-step's packed words
+          uint32_t w[16];
+          lookup_run<L>(lut_s, prev, cur, w);
+          if (i + 1 < nks) {
+            cur_n = load_cur(i + 1);
+            prev_n = load_prev(i + 1);
+          }
+          // while the loads are in flight: hand the previous k-step's weights to the MMA
+          if (pending_afull >= 0) {
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_afull + 8 * pending_afull);
+            pending_afull = -1;
+          }
+          if (!mbar_wait(bar_aempty + 8 * apipe.stage, apipe.phase ^ 1u, abort_flag, p.err, kWhereGroupedDecode)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          tmem_st16(t_lane + static_cast<uint32_t>(apipe.stage * kATmemCols), w);
+          pending_afull = apipe.stage;
+          apipe.advance(kNumAStages);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_pkempty + 8 * pk.stage);
+        pk.advance(SP);
+      }
+    }
+    if (pending_afull >= 0) {
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_afull + 8 * pending_afull);
     }
   }
 
@@ -439,8 +561,6 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
   }
 }
-
-using GroupedFn = void (*)(CUtensorMap, CUtensorMap, Params);
 
 template <int L>
 void* kernel_ptr() {
@@ -492,6 +612,7 @@ int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
   p.tiles = tiles;
   p.num_tiles = num_tiles;
   p.lut = lut;
+  p.packed = packed;
   p.y32 = y32;
   p.err = err;
   p.cap = cap;
@@ -509,31 +630,43 @@ int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
   while (cols < cols_needed) cols <<= 1;
   p.tmem_cols = cols;
 
+  // Shared memory: activation stages, packed super-stages, LUT, barriers.
+  // Prefer 3 packed buffers and up to 8 activation stages; shrink to fit.
   const uint32_t act_stage = static_cast<uint32_t>(p.n_mma_max * kActRowBytes);
   const uint32_t lut_bytes = std::max<uint32_t>(16u, 2u << L);
-  const uint32_t bar_bytes = 8 * (2 * kMaxStages + 2 * kNumAStages + 5) + 16;
-  int S = kMaxStages;
-  auto total_for = [&](int st) {
-    return 1024u + st * (act_stage + kPkStageBytes) + lut_bytes + bar_bytes;
+  const uint32_t bar_bytes = 8 * kNumBars + 16;
+  auto total_for = [&](int sp, int sa) {
+    return 1024u + sa * act_stage + sp * kPkStageBytes + lut_bytes + bar_bytes;
   };
-  while (S > 2 && total_for(S) > static_cast<uint32_t>(kSmemLimit)) --S;
-  if (total_for(S) > static_cast<uint32_t>(kSmemLimit)) return TQ_ERR_INVALID_ARG;
-  p.num_stages = S;
-  p.off_pk = S * act_stage;
-  p.off_lut = p.off_pk + S * kPkStageBytes;
+  int SP = 0, SA = 0;
+  for (int sp = kMaxPkStages; sp >= 2 && SP == 0; --sp) {
+    for (int sa = kMaxActStages; sa >= 2; --sa) {
+      if (total_for(sp, sa) <= static_cast<uint32_t>(kSmemLimit)) {
+        SP = sp;
+        SA = sa;
+        break;
+      }
+    }
+  }
+  if (SP == 0) return TQ_ERR_INVALID_ARG;
+  p.pk_stages = SP;
+  p.act_stages = SA;
+  p.off_pk = SA * act_stage;
+  p.off_lut = p.off_pk + SP * kPkStageBytes;
   p.off_bar = (p.off_lut + lut_bytes + 15u) & ~15u;
   // Ask for more than half of the SM's shared memory so that exactly one CTA
   // (and one tensor-memory allocation) sits on each SM.
-  const uint32_t smem = std::max<uint32_t>(total_for(S), 120u * 1024u);
+  const uint32_t smem = std::max<uint32_t>(total_for(SP, SA), 120u * 1024u);
 
   CUtensorMap tm_packed, tm_x;
   {
+    // Box wider than a short row (K/4 < 128) reads zeros past the row end.
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 4), static_cast<cuuint64_t>(E) * N};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 4)};
-    const cuuint32_t box[2] = {kPkRowBytes, kBlockRows};
+    const cuuint32_t box[2] = {kSSBytes, kBlockRows};
     const cuuint32_t estr[2] = {1, 1};
     if (encode(&tm_packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(packed), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return TQ_ERR_INVALID_ARG;
   }
@@ -553,8 +686,9 @@ int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
     cudaGetLastError();
     return TQ_ERR_CUDA;
   }
-  const long long units = cap * static_cast<long long>(p.row_blocks);
-  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(units, sm_count())));
+  const int n_ss = (K / kKStep + kSSSteps - 1) / kSSSteps;
+  const long long work = cap * static_cast<long long>(p.row_blocks) * n_ss;
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(work, sm_count())));
   void* args[] = {&tm_packed, &tm_x, &p};
   if (cudaLaunchKernel(kfn, dim3(grid), dim3(kThreads), args, smem, s) != cudaSuccess) {
     cudaGetLastError();
