@@ -175,6 +175,7 @@ def run_ours(args, rank, world, dist):
     num_tiles = torch.empty(1, dtype=torch.int32, device="cuda")
     y32 = torch.empty((n, N), dtype=torch.float32, device="cuda")
     y = torch.empty((n, N), dtype=torch.bfloat16, device="cuda")
+    x_sorted = torch.empty((P, K), dtype=torch.int16, device="cuda")
     stream = torch.cuda.current_stream()
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
@@ -184,9 +185,10 @@ def run_ours(args, rank, world, dist):
         y32.zero_()
         tq.tq_route(s["ids"], E, counts, offsets, sorted_pairs)
         tq.tq_build_tile_map(offsets, T, cap, tiles, num_tiles)
+        tq.tq_gather_rows(s["x"], sorted_pairs, k, x_sorted)
         if timed_slot is not None:
             gev[timed_slot][0].record(stream)
-        tq.tq_grouped_gemm(s["x"], s["packed"], s["lut"], sorted_pairs, s["w"], tiles, num_tiles, k, T, y32)
+        tq.tq_grouped_gemm(x_sorted, s["packed"], s["lut"], sorted_pairs, s["w"], tiles, num_tiles, k, T, y32)
         if timed_slot is not None:
             gev[timed_slot][1].record(stream)
         tq.tq_combine(y32, y)
@@ -324,7 +326,7 @@ def run_e2e(args, tq, torch, sets, n, k, E, K, N, T):
     dw = torch.empty((n, k), dtype=torch.float32, device="cuda")
     y = torch.empty((n, N), dtype=torch.bfloat16, device="cuda")
     yh = torch.empty((n, N), dtype=torch.bfloat16).pin_memory()
-    ws = torch.empty(tq.tq_moe_workspace_size(n, k, E, N, T), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(tq.tq_moe_workspace_size(n, k, E, K, N, T), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
     def one(i):
@@ -399,6 +401,83 @@ def run_reference(args, rank, world):
     }
 
 
+def run_sweep(args):
+    """Every workload, both arms, each launch timed alone after an L2 flush
+    (median of args.steps); one JSON line per (workload, arm, TILE_M).  This
+    is the per-configuration table and the GB300 gate study."""
+    import torch
+    import trellis_quantized_moe_sort_gb300 as tq
+    from trellis_quantized_moe_sort_gb300 import build as b
+    b.build()
+    torch.cuda.set_device(0)
+    tq.tq_init(0)
+    hbm, bf16, bf16_sus, peak_src = measured_peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    names = args.sweep_workloads.split(",") if args.sweep_workloads else list(moe_inputs.WORKLOADS)
+    for name in names:
+        prob = moe_inputs.make_problem(name)
+        s = prob.shape
+        d = {"x": _cuda(torch, prob.x_bits.view(np.int16)), "ids": _cuda(torch, prob.topk_ids),
+             "w": _cuda(torch, prob.topk_w), "packed": _cuda(torch, prob.packed),
+             "lut": _cuda(torch, prob.lut_bits.view(np.int16))}
+        y32 = torch.zeros((s.n, s.N), dtype=torch.float32, device="cuda")
+
+        def timed(fn):
+            fn()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(args.steps):
+                flush.zero_()
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b_.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b_) * 1e3)
+            return float(np.median(ts))
+
+        arms = [("grouped", T) for T in (16, 128)]
+        if s.n <= 1024:
+            arms.append(("gemv", None))
+        for arm, T in arms:
+            if arm == "grouped":
+                _, offsets, sp = tq.tq_route(d["ids"], s.E)
+                cap = tq.tq_tile_map_capacity(s.n, s.top_k, s.E, T)
+                tiles, nt = tq.tq_build_tile_map(offsets, T, cap)
+                xs = tq.tq_gather_rows(d["x"], sp, s.top_k)
+                torch.cuda.synchronize()
+                ntiles = int(nt.item())
+                gather_us = timed(lambda: tq.tq_gather_rows(d["x"], sp, s.top_k, xs))
+                us = timed(lambda: tq.tq_grouped_gemm(xs, d["packed"], d["lut"], sp, d["w"], tiles, nt,
+                                                       s.top_k, T, y32))
+                staged = ntiles * s.N * s.K // 4
+            else:
+                us = timed(lambda: tq.tq_gemv(d["x"], d["packed"], d["lut"], d["ids"], d["w"], y32))
+                ntiles = None
+                gather_us = None
+                staged = s.pairs * s.N * s.K // 4
+            code, where = tq.tq_device_error()
+            if code:
+                raise RuntimeError(f"device error {code} at {where} ({name}, {arm})")
+            woken = len(np.unique(prob.topk_ids))
+            m_tiles = ntiles if ntiles is not None else woken
+            alg = grouped_algorithmic_bytes(m_tiles, s.n, s.top_k, s.K, s.N, s.L)
+            flops = grouped_flops(s.n, s.top_k, s.K, s.N)
+            t_hbm = alg / (hbm * 1e9) * 1e6
+            t_tc = flops / (bf16_sus * 1e12) * 1e6
+            lookups = (ntiles if ntiles is not None else s.pairs) * s.N * s.K
+            print(json.dumps({
+                "workload": name, "arm": arm, "tile_m": T, "n": s.n, "pairs": s.pairs, "woken": woken,
+                "m_tiles": ntiles, "us": round(us, 1), "gather_us": gather_us, "pairs_per_s": round(s.pairs / (us * 1e-6), 1),
+                "staged_packed_GBps": round(staged / (us * 1e-6) / 1e9, 1),
+                "roofline_us": round(max(t_hbm, t_tc), 1), "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                "frac": round(max(t_hbm, t_tc) / us, 4),
+                "decode_lookups_per_clk_per_sm": round(lookups / (us * 1e-6) / 152 / 2.07e9, 2),
+                "peak_source": peak_src}), flush=True)
+        del d, y32
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -411,6 +490,9 @@ def main(argv=None):
                     help="independent weight sets cycled over the steps (defeats L2 reuse)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--sweep", action="store_true",
+                    help="per-workload table of both arms instead of the single bench line")
+    ap.add_argument("--sweep-workloads", default="", help="comma-separated subset for --sweep")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes (read+write) per grouped launch, if captured for this build")
     args = ap.parse_args(argv)
@@ -426,6 +508,9 @@ def main(argv=None):
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         tdist.init_process_group("nccl" if args.impl == "ours" else "gloo")
         dist = tdist
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
     else:

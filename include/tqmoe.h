@@ -157,6 +157,16 @@ int tq_build_tile_map(const int32_t* offsets, int E, int tile_m,
                       tq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Activation gather: x_sorted[s][:] = x[sorted_pairs[s] / top_k][:] for every
+ * sorted slot s < n*top_k, so that the rows of an m-tile are consecutive.
+ * x (device) bf16 [n][K]; x_sorted (device) bf16 [n*top_k][K]; both 16-byte
+ * aligned; K % 8 == 0.  A pair id out of range gives a zero row and sets
+ * TQ_ERR_INVALID_ARG in the device error word.
+ * ------------------------------------------------------------------------- */
+int tq_gather_rows(const uint16_t* x, const int32_t* sorted_pairs, int64_t n, int top_k, int K,
+                   uint16_t* x_sorted, tq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Grouped GEMM  ([P1] m-tiles; [P2] contiguous-run decode, decode fused into
  * the multiply)
  *
@@ -166,7 +176,8 @@ int tq_build_tile_map(const int32_t* offsets, int E, int tile_m,
  * MMAs contract it with the tile's gathered activations (fp32 accumulate),
  * and the epilogue scales by the router weight and adds into y32.
  *
- * x          (device) bf16 [n][K]; 16-byte aligned.
+ * x_sorted   (device) bf16 [n*top_k][K], the pair-sorted activations from
+ *            tq_gather_rows with the same sorted_pairs; 16-byte aligned.
  * packed     (device) uint8 [E][N][K/4]; 16-byte aligned.
  * lut        (device) fp16 [2^L] (converted to bf16, nearest-even, on chip).
  * sorted_pairs, tiles, num_tiles: from tq_route / tq_build_tile_map with the
@@ -209,14 +220,15 @@ int tq_combine(const float* y32, uint16_t* y, int64_t count, tq_stream_t stream)
  * (tq_select_arm with `pin`), the selected arm, combine to bf16 y [n][N].
  *
  * workspace (device): caller-owned scratch of at least
- *   tq_moe_workspace_size(n, top_k, E, N, tile_m) bytes, 256-byte aligned.
- *   It holds counts, offsets, sorted pairs, the tile map and the fp32
- *   accumulator; its contents are undefined after the call.
+ *   tq_moe_workspace_size(n, top_k, E, K, N, tile_m) bytes, 256-byte aligned.
+ *   It holds counts, offsets, sorted pairs, the tile map, the fp32
+ *   accumulator and the pair-sorted activations; its contents are undefined
+ *   after the call.
  * arm_used (host, may be NULL): receives TQ_ARM_GEMV or TQ_ARM_GROUPED.
  * The first grouped engagement in a process logs the tile fill and the
  * amortization boundary to stderr once (unless TQ_QUIET=1).
  * ------------------------------------------------------------------------- */
-size_t tq_moe_workspace_size(int64_t n, int top_k, int E, int N, int tile_m);
+size_t tq_moe_workspace_size(int64_t n, int top_k, int E, int K, int N, int tile_m);
 int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
                    const int32_t* topk_ids, const float* topk_w,
                    int64_t n, int top_k, int E, int K, int N, int tile_m, int pin,
@@ -235,8 +247,8 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
  * workspace.  The scratch is a file-scope device array of
  * TQ_STATIC_SCRATCH_BYTES (16 MiB) that every GPU loading this library holds
  * until the process exits; a shape whose tq_moe_workspace_size() exceeds it
- * is rejected with TQ_ERR_WORKSPACE before anything is launched (at N = 2048
- * that is about n > 2000 tokens).  The call allocates nothing (no cudaMalloc,
+ * is rejected with TQ_ERR_WORKSPACE before anything is launched (at
+ * K = 4096, N = 2048, top-6 that is about n > 290 tokens).  The call allocates nothing (no cudaMalloc,
  * no cudaFree, no allocating library routine).
  *
  * The first call on a device looks up the array's device address with that
@@ -263,8 +275,9 @@ int tq_device_error(int* code, int* where);
 
 /* Host-side counts of successful launches since process start, per kernel:
  * out[0] route, out[1] tile map, out[2] grouped GEMM, out[3] GEMV,
- * out[4] combine ([P3]: counters prove which arm ran). */
-void tq_launch_counts(int64_t out[5]);
+ * out[4] combine, out[5] activation gather ([P3]: counters prove which arm
+ * ran). */
+void tq_launch_counts(int64_t out[6]);
 
 #ifdef __cplusplus
 }

@@ -31,8 +31,9 @@ def grouped_y32(prob, d, tile_m):
     counts, offsets, sp = tq.tq_route(d["ids"], s.E)
     cap = tq.tq_tile_map_capacity(s.n, s.top_k, s.E, tile_m)
     tiles, nt = tq.tq_build_tile_map(offsets, tile_m, cap)
+    xs = tq.tq_gather_rows(d["x"], sp, s.top_k)
     y32 = torch.zeros((s.n, s.N), dtype=torch.float32, device="cuda")
-    tq.tq_grouped_gemm(d["x"], d["packed"], d["lut"], sp, d["w"], tiles, nt, s.top_k, tile_m, y32)
+    tq.tq_grouped_gemm(xs, d["packed"], d["lut"], sp, d["w"], tiles, nt, s.top_k, tile_m, y32)
     check_no_device_error()
     return y32
 

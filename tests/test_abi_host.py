@@ -81,4 +81,4 @@ def test_host_functions_reject_invalid_arguments(tq):
     with pytest.raises(tq.TQError):
         tq.tq_select_arm(10, 2, 8, 16, pin=7)
     assert np.isnan(tq.tq_pairs_per_woken_expert(4, 9, 8))
-    assert tq.tq_moe_workspace_size(16, 2, 8, 128, 16) > 16 * 128 * 4
+    assert tq.tq_moe_workspace_size(16, 2, 8, 256, 128, 16) > 16 * 128 * 4 + 32 * 256 * 2

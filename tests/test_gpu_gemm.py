@@ -72,9 +72,10 @@ def test_grouped_accumulates_into_y32():
     _, offsets, sp = tq.tq_route(d["ids"], s.E)
     cap = tq.tq_tile_map_capacity(s.n, s.top_k, s.E, T)
     tiles, nt = tq.tq_build_tile_map(offsets, T, cap)
+    xs = tq.tq_gather_rows(d["x"], sp, s.top_k)
     y32 = torch.ones((s.n, s.N), dtype=torch.float32, device="cuda")
     for _ in range(2):
-        tq.tq_grouped_gemm(d["x"], d["packed"], d["lut"], sp, d["w"], tiles, nt, s.top_k, T, y32)
+        tq.tq_grouped_gemm(xs, d["packed"], d["lut"], sp, d["w"], tiles, nt, s.top_k, T, y32)
     check_no_device_error()
     ref = 1.0 + 2.0 * O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed,
                                     prob.lut_bits, s.L)

@@ -73,7 +73,7 @@ def test_static_matches_workspace_entry_point_two_calls(name, tile_m, pin):
 
 def test_static_rejects_shapes_beyond_its_array():
     # 8192 tokens x 2048 outputs need a 64 MiB fp32 accumulator: over the 16 MiB array
-    assert tq.tq_moe_workspace_size(8192, 6, 256, 2048, 16) > tq.STATIC_SCRATCH_BYTES
+    assert tq.tq_moe_workspace_size(8192, 6, 256, 256, 2048, 16) > tq.STATIC_SCRATCH_BYTES
     prob = moe_inputs.make_custom(8, 2, 4, 256, 128, 12, seed=1)
     x, packed, lut, ids, w = _dev(prob)
     y = torch.empty((4, 128), dtype=torch.bfloat16, device="cuda")

@@ -18,7 +18,7 @@ import os
 __all__ = [
     "TQError", "lib", "lib_path", "tq_init", "tq_arch_witness", "tq_pairs_per_woken_expert",
     "tq_tiles_amortize", "tq_grouped_min_tokens", "tq_tile_map_capacity", "tq_select_arm",
-    "tq_route", "tq_build_tile_map", "tq_grouped_gemm", "tq_gemv", "tq_combine",
+    "tq_route", "tq_build_tile_map", "tq_gather_rows", "tq_grouped_gemm", "tq_gemv", "tq_combine",
     "tq_moe_workspace_size", "tq_moe_forward", "tq_moe_forward_static", "tq_device_error", "tq_launch_counts",
     "tq_status_string", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "EXPORTED_SYMBOLS",
 ]
@@ -46,7 +46,8 @@ _SIGS = {
     "tq_gemv": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int, _c_int,
                          _c_int, _c_p, _c_p]),
     "tq_combine": (_c_int, [_c_p, _c_p, _c_i64, _c_p]),
-    "tq_moe_workspace_size": (_c_sz, [_c_i64, _c_int, _c_int, _c_int, _c_int]),
+    "tq_gather_rows": (_c_int, [_c_p, _c_p, _c_i64, _c_int, _c_int, _c_p, _c_p]),
+    "tq_moe_workspace_size": (_c_sz, [_c_i64, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "tq_moe_forward": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int,
                                 _c_int, _c_int, _c_int, _c_int, _c_p, _c_sz, _c_p,
                                 ctypes.POINTER(_c_int), _c_p]),
@@ -211,13 +212,33 @@ def _shapes(x, packed, lut):
     return n, K, E, N, L
 
 
-def tq_grouped_gemm(x, packed, lut, sorted_pairs, topk_w, tiles, num_tiles, top_k: int, tile_m: int,
-                    y32, stream=None) -> None:
-    """y32 += grouped product (y32 fp32 [n, N], zero it for a plain product)."""
+def tq_gather_rows(x, sorted_pairs, top_k: int, x_sorted=None, stream=None):
+    """Pair-sorted copy of the activations: x_sorted[s] = x[sorted_pairs[s] // top_k]."""
     torch = _torch()
-    n, K, E, N, L = _shapes(x, packed, lut)
+    n, K = x.shape
+    P = n * top_k
+    x_sorted = torch.empty((max(P, 1), K), dtype=x.dtype, device=x.device) if x_sorted is None else x_sorted
+    _check(lib().tq_gather_rows(_dev_ptr(x, _bits16(), "x"), _dev_ptr(sorted_pairs, (torch.int32,), "sorted_pairs"),
+                                n, top_k, K, _dev_ptr(x_sorted, _bits16(), "x_sorted"), _stream(stream)),
+           "tq_gather_rows")
+    return x_sorted[:P]
+
+
+def tq_grouped_gemm(x_sorted, packed, lut, sorted_pairs, topk_w, tiles, num_tiles, top_k: int, tile_m: int,
+                    y32, stream=None) -> None:
+    """y32 += grouped product (y32 fp32 [n, N], zero it for a plain product).
+    x_sorted: pair-sorted activations [n*top_k, K] from tq_gather_rows."""
+    torch = _torch()
+    P, K = x_sorted.shape
+    E, N, kb = packed.shape
+    if kb * 4 != K:
+        raise ValueError(f"packed has {kb} bytes per row, expected K/4 = {K // 4}")
+    if P % top_k:
+        raise ValueError("x_sorted must have n*top_k rows")
+    n = P // top_k
+    L = lut.numel().bit_length() - 1
     cap = tiles.shape[0]
-    _check(lib().tq_grouped_gemm(_dev_ptr(x, _bits16(), "x"), _dev_ptr(packed, (torch.uint8,), "packed"),
+    _check(lib().tq_grouped_gemm(_dev_ptr(x_sorted, _bits16(), "x_sorted"), _dev_ptr(packed, (torch.uint8,), "packed"),
                                  _dev_ptr(lut, _bits16(), "lut"), L,
                                  _dev_ptr(sorted_pairs, (torch.int32,), "sorted_pairs"),
                                  _dev_ptr(topk_w, (torch.float32,), "topk_w"),
@@ -247,8 +268,8 @@ def tq_combine(y32, y=None, stream=None):
     return y
 
 
-def tq_moe_workspace_size(n: int, top_k: int, E: int, N: int, tile_m: int) -> int:
-    return int(lib().tq_moe_workspace_size(n, top_k, E, N, tile_m))
+def tq_moe_workspace_size(n: int, top_k: int, E: int, K: int, N: int, tile_m: int) -> int:
+    return int(lib().tq_moe_workspace_size(n, top_k, E, K, N, tile_m))
 
 
 def tq_moe_forward(x, packed, lut, topk_ids, topk_w, tile_m: int = 16, pin: int = ARM_AUTO,
@@ -257,7 +278,7 @@ def tq_moe_forward(x, packed, lut, topk_ids, topk_w, tile_m: int = 16, pin: int 
     torch = _torch()
     n, K, E, N, L = _shapes(x, packed, lut)
     top_k = topk_ids.shape[1]
-    need = tq_moe_workspace_size(n, top_k, E, N, tile_m)
+    need = tq_moe_workspace_size(n, top_k, E, K, N, tile_m)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
     y = torch.empty((n, N), dtype=torch.bfloat16, device=x.device) if y is None else y
@@ -303,6 +324,6 @@ def tq_device_error() -> tuple[int, int]:
 
 
 def tq_launch_counts() -> dict:
-    arr = (ctypes.c_int64 * 5)()
+    arr = (ctypes.c_int64 * 6)()
     lib().tq_launch_counts(arr)
-    return dict(zip(("route", "tile_map", "grouped", "gemv", "combine"), list(arr)))
+    return dict(zip(("route", "tile_map", "grouped", "gemv", "combine", "gather"), list(arr)))

@@ -15,8 +15,11 @@
 //   warp 0      TMA producer.  Packed bytes: one 2-D box of the expert's 128
 //               rows x 128 bytes (512 symbols = 8 k-steps of 64) per
 //               "super-stage", 128B-swizzled; wide rows keep the TMA unit's
-//               per-row cost low.  Activations: one 128-byte box per pair of
-//               the tile per k-step, 128B-swizzled into the MMA's B layout.
+//               per-row cost low.
+//   warp 14     TMA producer for activations: the pair-sorted copy of x puts a
+//               tile's rows next to each other, so one 128B-swizzled box of
+//               64 columns x (tile_m rounded up to 16) rows per k-step lands
+//               directly in the MMA's B layout.
 //   warp 1      MMA issuer: tcgen05.mma kind::f16, A = decoded weights in tensor
 //               memory (M = 128 rows), B = activations in shared memory
 //               (N = pairs of the tile padded to 16), fp32 accumulator in
@@ -66,7 +69,6 @@ constexpr int kWarpActProducer = kWarpDec0 + kNumDecodeWarps;
 constexpr int kThreads = 32 * (kWarpActProducer + 1);  // 480
 constexpr int kMaxPkStages = 6;
 constexpr int kMaxActStages = 8;
-constexpr int kMaxTileM = 256;
 constexpr int kSmemLimit = 232448;                   // 227 KiB opt-in per block
 constexpr int kNumBars = 2 * kMaxPkStages + 2 * kMaxActStages + 2 * kNumAStages + 2 + 2 + 1;
 static_assert(kNumDecodeWarps == 8, "decode mapping assumes 2 warps per TMEM lane quarter");
@@ -212,7 +214,7 @@ __device__ __forceinline__ void drain_ring(uint32_t bar0, Pipe pipe, int nstages
 
 template <int L>
 __global__ void __launch_bounds__(kThreads, 1)
-grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_constant__ CUtensorMap tm_x,
+grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_constant__ CUtensorMap tm_xs,
                const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -337,26 +339,19 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     drain_ring(bar_pkfull, pk, SP, pk_issued, p.err);
   } else if (warp == kWarpActProducer) {
     // ------------------------------------------------------------ activation producer
-    if (lane == 0) tma_prefetch_desc(&tm_x);
+    // The tile's activation rows are consecutive in the pair-sorted copy of x:
+    // one box of n_mma_max rows per k-step (rows past the tile are never read
+    // back by the epilogue).
+    if (lane == 0) tma_prefetch_desc(&tm_xs);
     Pipe act;
     long long act_issued = 0;
     bool ok = true;
+    const uint32_t act_tx = static_cast<uint32_t>(p.n_mma_max) * kActRowBytes;
     for (long long g = g_beg; g < g_end && ok;) {
       const Segment sg = segment_at(g, g_end, n_ss, p.row_blocks);
       g += sg.ss1 - sg.ss0;
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
-      const int rows = tl.rows;
-      int tok[kMaxTileM / 32];
-#pragma unroll
-      for (int j = 0; j < kMaxTileM / 32; ++j) {
-        const int i = lane + 32 * j;
-        const int pair = (i < rows) ? p.sorted_pairs[tl.slot0 + i] : 0;
-        // an out-of-range pair id reads a zero-filled row (TMA bounds) and is
-        // skipped by the epilogue
-        tok[j] = (pair >= 0 && pair < p.P) ? pair / p.top_k : p.P;
-      }
-      const uint32_t act_tx = static_cast<uint32_t>(rows) * kActRowBytes;
       const int ks0 = sg.ss0 * kSSSteps, ks1 = min(ksteps, sg.ss1 * kSSSteps);
       for (int ks = ks0; ks < ks1; ++ks) {
         if (!mbar_wait(bar_actempty + 8 * act.stage, act.phase ^ 1u, abort_flag, p.err,
@@ -364,14 +359,11 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
           ok = false;
           break;
         }
-        __syncwarp();
-        const uint32_t full = bar_actfull + 8 * act.stage;
-        if (lane == 0) mbar_arrive_expect_tx(full, act_tx);
-        const uint32_t dst = act0 + static_cast<uint32_t>(act.stage * p.n_mma_max * kActRowBytes);
-#pragma unroll
-        for (int j = 0; j < kMaxTileM / 32; ++j) {
-          const int i = lane + 32 * j;
-          if (i < rows) tma_load_2d(dst + i * kActRowBytes, &tm_x, ks * kKStep, tok[j], full);
+        if (lane == 0) {
+          const uint32_t full = bar_actfull + 8 * act.stage;
+          mbar_arrive_expect_tx(full, act_tx);
+          tma_load_2d(act0 + static_cast<uint32_t>(act.stage * p.n_mma_max * kActRowBytes), &tm_xs,
+                      ks * kKStep, tl.slot0, full);
         }
         ++act_issued;
         act.advance(SA);
@@ -597,7 +589,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
+int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
                    const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                    const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
                    int tile_m, float* y32, int* err, cudaStream_t s) {
@@ -658,7 +650,7 @@ int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
   // (and one tensor-memory allocation) sits on each SM.
   const uint32_t smem = std::max<uint32_t>(total_for(SP, SA), 120u * 1024u);
 
-  CUtensorMap tm_packed, tm_x;
+  CUtensorMap tm_packed, tm_xs;
   {
     // Box wider than a short row (K/4 < 128) reads zeros past the row end.
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 4), static_cast<cuuint64_t>(E) * N};
@@ -671,11 +663,11 @@ int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
       return TQ_ERR_INVALID_ARG;
   }
   {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(n)};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(p.P)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {kKStep, 1};
+    const cuuint32_t box[2] = {kKStep, static_cast<cuuint32_t>(p.n_mma_max)};
     const cuuint32_t estr[2] = {1, 1};
-    if (encode(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box,
+    if (encode(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x_sorted), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return TQ_ERR_INVALID_ARG;
@@ -689,7 +681,7 @@ int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
   const int n_ss = (K / kKStep + kSSSteps - 1) / kSSSteps;
   const long long work = cap * static_cast<long long>(p.row_blocks) * n_ss;
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(work, sm_count())));
-  void* args[] = {&tm_packed, &tm_x, &p};
+  void* args[] = {&tm_packed, &tm_xs, &p};
   if (cudaLaunchKernel(kfn, dim3(grid), dim3(kThreads), args, smem, s) != cudaSuccess) {
     cudaGetLastError();
     return TQ_ERR_LAUNCH;

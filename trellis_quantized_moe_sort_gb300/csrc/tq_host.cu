@@ -287,11 +287,26 @@ static int check_gemm_common(const uint16_t* x, const uint8_t* packed, const uin
   return TQ_OK;
 }
 
-int tq_grouped_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
+int tq_gather_rows(const uint16_t* x, const int32_t* sorted_pairs, int64_t n, int top_k, int K,
+                   uint16_t* x_sorted, tq_stream_t stream) {
+  if (n < 0 || top_k < 1 || K < 8 || K % 8 != 0) return TQ_ERR_INVALID_ARG;
+  const int64_t P = n * top_k;
+  if (P >= (static_cast<int64_t>(1) << 31)) return TQ_ERR_INVALID_ARG;
+  if (P > 0 && (!x || !sorted_pairs || !x_sorted || !aligned16(x) || !aligned16(x_sorted)))
+    return TQ_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int rc = require_sm103(s);
+  if (rc != TQ_OK) return rc;
+  int* err = error_word(&rc);
+  if (!err) return rc;
+  return launch_gather(x, sorted_pairs, static_cast<int>(P), top_k, K, x_sorted, err, s);
+}
+
+int tq_grouped_gemm(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
                     const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                     const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
                     int tile_m, float* y32, tq_stream_t stream) {
-  int rc = check_gemm_common(x, packed, lut, L, topk_w, n, top_k, E, K, N, y32);
+  int rc = check_gemm_common(x_sorted, packed, lut, L, topk_w, n, top_k, E, K, N, y32);
   if (rc != TQ_OK) return rc;
   if (N % 128 != 0 || tile_m < 1 || tile_m > 256 || cap < 1 || cap >= (static_cast<int64_t>(1) << 31))
     return TQ_ERR_INVALID_ARG;
@@ -302,8 +317,8 @@ int tq_grouped_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* lu
   if (n == 0) return TQ_OK;
   int* err = error_word(&rc);
   if (!err) return rc;
-  return launch_grouped(x, packed, lut, L, sorted_pairs, topk_w, tiles, num_tiles, cap, n, top_k, E, K, N,
-                        tile_m, y32, err, s);
+  return launch_grouped(x_sorted, packed, lut, L, sorted_pairs, topk_w, tiles, num_tiles, cap, n, top_k, E, K,
+                        N, tile_m, y32, err, s);
 }
 
 int tq_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L, const int32_t* topk_ids,
@@ -329,9 +344,9 @@ int tq_combine(const float* y32, uint16_t* y, int64_t count, tq_stream_t stream)
   return launch_combine(y32, y, count, s);
 }
 
-size_t tq_moe_workspace_size(int64_t n, int top_k, int E, int N, int tile_m) {
+size_t tq_moe_workspace_size(int64_t n, int top_k, int E, int K, int N, int tile_m) {
   const int64_t cap = tq_tile_map_capacity(n, top_k, E, tile_m);
-  if (cap < 0 || N < 1) return 0;
+  if (cap < 0 || N < 1 || K < 1) return 0;
   const size_t P = static_cast<size_t>(n) * top_k;
   size_t b = 0;
   b += align256(sizeof(int32_t) * E);                               // counts
@@ -340,6 +355,7 @@ size_t tq_moe_workspace_size(int64_t n, int top_k, int E, int N, int tile_m) {
   b += align256(sizeof(int32_t) * 3 * std::max<int64_t>(cap, 1));   // tiles
   b += align256(sizeof(int32_t));                                   // num_tiles
   b += align256(sizeof(float) * static_cast<size_t>(n) * N);        // y32
+  b += align256(sizeof(uint16_t) * P * K);                          // pair-sorted activations
   return b;
 }
 
@@ -367,7 +383,7 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
   if (arm < 0) return arm;
   if (arm == TQ_ARM_GROUPED && N % 128 != 0) return TQ_ERR_INVALID_ARG;
   if (arm == TQ_ARM_GEMV && K > 8192) return TQ_ERR_INVALID_ARG;
-  const size_t need = tq_moe_workspace_size(n, top_k, E, N, tile_m);
+  const size_t need = tq_moe_workspace_size(n, top_k, E, K, N, tile_m);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return TQ_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -386,7 +402,8 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
   int32_t* sorted_pairs = reinterpret_cast<int32_t*>(w);      w += align256(sizeof(int32_t) * P);
   int32_t* tiles = reinterpret_cast<int32_t*>(w);             w += align256(sizeof(int32_t) * 3 * cap);
   int32_t* num_tiles = reinterpret_cast<int32_t*>(w);         w += align256(sizeof(int32_t));
-  float* y32 = reinterpret_cast<float*>(w);
+  float* y32 = reinterpret_cast<float*>(w);                   w += align256(sizeof(float) * static_cast<size_t>(n) * N);
+  uint16_t* x_sorted = reinterpret_cast<uint16_t*>(w);
 
   if (cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(n) * N, s) != cudaSuccess) {
     cudaGetLastError();
@@ -397,8 +414,10 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
     if (rc != TQ_OK) return rc;
     rc = launch_tile_map(offsets, E, tile_m, tiles, num_tiles, cap, err, s);
     if (rc != TQ_OK) return rc;
-    rc = launch_grouped(x, packed, lut, L, sorted_pairs, topk_w, tiles, num_tiles, cap, n, top_k, E, K, N,
-                        tile_m, y32, err, s);
+    rc = launch_gather(x, sorted_pairs, static_cast<int>(P), top_k, K, x_sorted, err, s);
+    if (rc != TQ_OK) return rc;
+    rc = launch_grouped(x_sorted, packed, lut, L, sorted_pairs, topk_w, tiles, num_tiles, cap, n, top_k, E, K,
+                        N, tile_m, y32, err, s);
     if (rc != TQ_OK) return rc;
     std::call_once(g_log_once, [&] {
       const char* q = std::getenv("TQ_QUIET");
@@ -435,7 +454,7 @@ int tq_device_error(int* code, int* where) {
   return TQ_OK;
 }
 
-void tq_launch_counts(int64_t out[5]) {
+void tq_launch_counts(int64_t out[6]) {
   if (!out) return;
   for (int i = 0; i < kCntNum; ++i) out[i] = g_counts[i].load();
 }

@@ -6,9 +6,9 @@
 // (that framework owns every allocation), or a serving loop that forbids
 // allocation after start-up because cudaMalloc can block and synchronize the
 // device.  They still pass inputs and outputs; the scratch this call needs
-// (counts, offsets, sorted pairs, tile map, fp32 accumulator) lives in one
-// file-scope device array of fixed size, which every GPU that loads this
-// library holds until the process exits.
+// (counts, offsets, sorted pairs, tile map, fp32 accumulator, pair-sorted
+// activations) lives in one file-scope device array of fixed size, which
+// every GPU that loads this library holds until the process exits.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -57,7 +57,7 @@ extern "C" int tq_moe_forward_static(const uint16_t* x, const uint8_t* packed, c
                                      int K, int N, int tile_m, int pin, uint16_t* y, int* arm_used,
                                      tq_stream_t stream) {
   if (n < 0 || N < 1) return TQ_ERR_INVALID_ARG;
-  const size_t need = tq_moe_workspace_size(n, top_k, E, N, tile_m);
+  const size_t need = tq_moe_workspace_size(n, top_k, E, K, N, tile_m);
   if (need == 0) return TQ_ERR_INVALID_ARG;
   if (need > static_cast<size_t>(TQ_STATIC_SCRATCH_BYTES)) return TQ_ERR_WORKSPACE;
   void* scratch = nullptr;

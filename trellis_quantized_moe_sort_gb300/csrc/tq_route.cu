@@ -179,7 +179,41 @@ __global__ void combine_kernel_scalar(const float* __restrict__ y32, uint16_t* _
   }
 }
 
+// x_sorted[slot] = x[sorted_pairs[slot] / top_k]: the activations in pair-sorted
+// order, 16 bytes per thread step; an out-of-range pair id yields a zero row.
+__global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_pairs,
+                                   int P, int top_k, int row_vecs, uint4* __restrict__ x_sorted, int* err) {
+  const long long total = static_cast<long long>(P) * row_vecs;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int slot = static_cast<int>(i / row_vecs);
+    const int v = static_cast<int>(i - static_cast<long long>(slot) * row_vecs);
+    const int pair = sorted_pairs[slot];
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (pair >= 0 && pair < P) {
+      val = __ldg(x + static_cast<size_t>(pair / top_k) * row_vecs + v);
+    } else if (v == 0) {
+      record_error(err, TQ_ERR_INVALID_ARG, kWhereRoute);
+    }
+    x_sorted[i] = val;
+  }
+}
+
 }  // namespace
+
+int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top_k, int K, uint16_t* x_sorted,
+                  int* err, cudaStream_t s) {
+  if (P == 0) return TQ_OK;
+  const int row_vecs = K / 8;
+  const long long total = static_cast<long long>(P) * row_vecs;
+  const int threads = 256;
+  const int blocks = static_cast<int>(std::min<long long>((total + threads - 1) / threads, sm_count() * 8));
+  gather_rows_kernel<<<blocks, threads, 0, s>>>(reinterpret_cast<const uint4*>(x), sorted_pairs, P, top_k,
+                                                row_vecs, reinterpret_cast<uint4*>(x_sorted), err);
+  const int st = launch_status();
+  if (st == TQ_OK) count_launch(kCntGather);
+  return st;
+}
 
 int launch_route(const int32_t* topk_ids, int P, int E, int32_t* counts, int32_t* offsets,
                  int32_t* sorted_pairs, int* err, cudaStream_t s) {
