@@ -436,8 +436,9 @@ def run_sweep(args):
                 ts.append(a.elapsed_time(b_) * 1e3)
             return float(np.median(ts))
 
-        arms = [("grouped", T) for T in (16, 128)]
-        if s.n <= 1024:
+        tiles_list = [int(t) for t in args.sweep_tiles.split(",")]
+        arms = [("grouped", T) for T in tiles_list]
+        if s.n <= 1024 and not args.sweep_no_gemv:
             arms.append(("gemv", None))
         for arm, T in arms:
             if arm == "grouped":
@@ -493,6 +494,8 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true",
                     help="per-workload table of both arms instead of the single bench line")
     ap.add_argument("--sweep-workloads", default="", help="comma-separated subset for --sweep")
+    ap.add_argument("--sweep-tiles", default="16,128", help="TILE_M values for --sweep")
+    ap.add_argument("--sweep-no-gemv", action="store_true", help="skip the GEMV arm in --sweep")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes (read+write) per grouped launch, if captured for this build")
     args = ap.parse_args(argv)

@@ -183,7 +183,7 @@ int tq_gather_rows(const uint16_t* x, const int32_t* sorted_pairs, int64_t n, in
  * sorted_pairs, tiles, num_tiles: from tq_route / tq_build_tile_map with the
  *            same tile_m.  cap = capacity of `tiles`.
  * topk_w     (device) fp32 [n][top_k] router weights.
- * y32        (device) fp32 [n][N]: ACCUMULATED into (y32 += ...); zero it
+ * y32        (device) fp32 [n][N], 16-byte aligned: ACCUMULATED into (y32 += ...); zero it
  *            first for a plain product.  Additions are fp32 atomics, so the
  *            summation order (and the last bits) vary between runs.
  * Requires: K % 64 == 0, N % 128 == 0, L even in [2, 16], 1 <= tile_m <= 256,

@@ -25,7 +25,7 @@
 //               (N = pairs of the tile padded to 16), fp32 accumulator in
 //               tensor memory.
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator, scale by the router
-//               weight, fp32 atomic add into y32[token][row].
+//               weight, 16-byte fp32 vector reductions into y32[token][rows].
 //   warps 6-13  decode: thread (quarter q, half h) owns weight row 32q + lane
 //               and symbols [32h, 32h + 32) of each k-step; the state of each
 //               symbol is a shift + mask of a 64-bit window of the staged
@@ -87,6 +87,7 @@ struct Params {
   int P, E, tile_m;
   int top_k, N, K;
   int row_blocks;
+  int rb_group;     // row blocks per ordering group (row_blocks = plain tile-major order)
   int n_mma_max;    // largest MMA N (tile_m rounded up to 16)
   int pk_stages;    // packed super-stage buffers
   int act_stages;   // activation k-step buffers
@@ -125,16 +126,24 @@ __device__ __forceinline__ Tile read_tile(const Params& p, int tile) {
 
 // A run of super-stages [ss0, ss1) of one work unit (m-tile `tile`, row block
 // `rb`) starting at flattened position g and ending no later than g_end.
+// Units are ordered by groups of `rb_group` row blocks, then m-tile, then row
+// block: CTAs running at the same time touch one slice of the output (which
+// stays in L2 for the atomic adds) while each tile's activations are reused
+// across the group's row blocks.
 struct Segment {
   int tile, rb, ss0, ss1;
 };
-__device__ __forceinline__ Segment segment_at(long long g, long long g_end, int n_ss, int row_blocks) {
+__device__ __forceinline__ Segment segment_at(long long g, long long g_end, int n_ss, int num_tiles,
+                                              int rb_group) {
   Segment sg;
   const long long u = g / n_ss;
   sg.ss0 = static_cast<int>(g - u * n_ss);
   sg.ss1 = static_cast<int>(min(static_cast<long long>(n_ss), sg.ss0 + (g_end - g)));
-  sg.tile = static_cast<int>(u / row_blocks);
-  sg.rb = static_cast<int>(u - static_cast<long long>(sg.tile) * row_blocks);
+  const long long per_group = static_cast<long long>(num_tiles) * rb_group;
+  const long long grp = u / per_group;
+  const long long r = u - grp * per_group;
+  sg.tile = static_cast<int>(r / rb_group);
+  sg.rb = static_cast<int>(grp * rb_group + (r - static_cast<long long>(sg.tile) * rb_group));
   return sg;
 }
 
@@ -299,6 +308,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   const int ksteps = p.K / kKStep;
   const int n_ss = (ksteps + kSSSteps - 1) / kSSSteps;
   const uint32_t acol0 = static_cast<uint32_t>(p.nacc * p.n_mma_max);
+  const int rb_group = p.rb_group;
   // This CTA's equal share of the flattened (unit, super-stage) work; every
   // role walks it in the same order, one segment at a time.
   const long long total = static_cast<long long>(num_tiles) * p.row_blocks * n_ss;
@@ -312,7 +322,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     long long pk_issued = 0;
     bool ok = true;
     for (long long g = g_beg; g < g_end && ok;) {
-      const Segment sg = segment_at(g, g_end, n_ss, p.row_blocks);
+      const Segment sg = segment_at(g, g_end, n_ss, num_tiles, rb_group);
       g += sg.ss1 - sg.ss0;
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) {
@@ -348,7 +358,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     bool ok = true;
     const uint32_t act_tx = static_cast<uint32_t>(p.n_mma_max) * kActRowBytes;
     for (long long g = g_beg; g < g_end && ok;) {
-      const Segment sg = segment_at(g, g_end, n_ss, p.row_blocks);
+      const Segment sg = segment_at(g, g_end, n_ss, num_tiles, rb_group);
       g += sg.ss1 - sg.ss0;
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
@@ -376,7 +386,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     Pipe act, apipe, accp;
     bool ok = true;
     for (long long g = g_beg; g < g_end && ok;) {
-      const Segment sg = segment_at(g, g_end, n_ss, p.row_blocks);
+      const Segment sg = segment_at(g, g_end, n_ss, num_tiles, rb_group);
       g += sg.ss1 - sg.ss0;
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
@@ -433,30 +443,49 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     const int q = warp & 3;
     Pipe accp;
     for (long long g = g_beg; g < g_end;) {
-      const Segment sg = segment_at(g, g_end, n_ss, p.row_blocks);
+      const Segment sg = segment_at(g, g_end, n_ss, num_tiles, rb_group);
       g += sg.ss1 - sg.ss0;
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
       const int slot0 = tl.slot0, rows = tl.rows;
       if (!mbar_wait(bar_accfull + 8 * accp.stage, accp.phase, abort_flag, p.err, kWhereGroupedEpilogue)) break;
       tc_fence_after();
-      const int row = sg.rb * kBlockRows + 32 * q + lane;
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(accp.stage * p.n_mma_max);
+      // Each 4x4 block (4 lanes = 4 consecutive rows, 4 pair columns) is
+      // transposed by shuffles so that a lane holds 4 consecutive rows of one
+      // pair and adds them with one 16-byte vector reduction.
+      const int qa = lane >> 2, qb = lane & 3;
+      float* const yrow = p.y32 + static_cast<size_t>(sg.rb) * kBlockRows + 32 * q + 4 * qa;
       for (int c0 = 0; c0 < rows; c0 += 16) {
         uint32_t v[16];
         tmem_ld16(t_acc + c0, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (c0 + i < rows) {
-            const int pair = p.sorted_pairs[slot0 + c0 + i];
+        for (int k = 0; k < 4; ++k) {
+          if (c0 + 4 * k >= rows) break;
+          float x0 = __uint_as_float(v[4 * k]), x1 = __uint_as_float(v[4 * k + 1]);
+          float x2 = __uint_as_float(v[4 * k + 2]), x3 = __uint_as_float(v[4 * k + 3]);
+          float t = __shfl_xor_sync(0xffffffffu, (qb & 1) ? x0 : x1, 1);
+          if (qb & 1) x0 = t; else x1 = t;
+          t = __shfl_xor_sync(0xffffffffu, (qb & 1) ? x2 : x3, 1);
+          if (qb & 1) x2 = t; else x3 = t;
+          t = __shfl_xor_sync(0xffffffffu, (qb & 2) ? x0 : x2, 2);
+          if (qb & 2) x0 = t; else x2 = t;
+          t = __shfl_xor_sync(0xffffffffu, (qb & 2) ? x1 : x3, 2);
+          if (qb & 2) x1 = t; else x3 = t;
+          const int col = c0 + 4 * k + qb;
+          if (col < rows) {
+            const int pair = p.sorted_pairs[slot0 + col];
             if (pair < 0 || pair >= p.P) {
-              if (lane == 0) record_error(p.err, TQ_ERR_INVALID_ARG, kWhereGroupedEpilogue);
-              continue;
+              record_error(p.err, TQ_ERR_INVALID_ARG, kWhereGroupedEpilogue);
+            } else {
+              const float wt = p.topk_w[pair];
+              float* dst = yrow + static_cast<size_t>(pair / p.top_k) * p.N;
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x0 * wt),
+                           "f"(x1 * wt), "f"(x2 * wt), "f"(x3 * wt)
+                           : "memory");
             }
-            const int tok = pair / p.top_k;
-            atomicAdd(p.y32 + static_cast<size_t>(tok) * p.N + row, __uint_as_float(v[i]) * p.topk_w[pair]);
           }
         }
       }
@@ -478,7 +507,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     int pending_afull = -1;   // A stage stored but not yet handed to the MMA
     bool ok = true;
     for (long long g = g_beg; g < g_end && ok;) {
-      const Segment sg = segment_at(g, g_end, n_ss, p.row_blocks);
+      const Segment sg = segment_at(g, g_end, n_ss, num_tiles, rb_group);
       g += sg.ss1 - sg.ss0;
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
@@ -615,6 +644,17 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
   p.N = N;
   p.K = K;
   p.row_blocks = N / kBlockRows;
+  // Order by row-block groups only when the fp32 output is too large to stay
+  // in L2 while six scattered partial sums per element arrive.
+  p.rb_group = p.row_blocks;
+  if (static_cast<long long>(n) * N * 4 > (24ll << 20)) {
+    for (int g = 8; g >= 1; g >>= 1) {
+      if (p.row_blocks % g == 0) {
+        p.rb_group = g;
+        break;
+      }
+    }
+  }
   p.n_mma_max = (tile_m + 15) & ~15;
   p.nacc = (2 * p.n_mma_max + kNumAStages * kATmemCols <= 512) ? 2 : 1;
   const int cols_needed = p.nacc * p.n_mma_max + kNumAStages * kATmemCols;

@@ -310,6 +310,7 @@ int tq_grouped_gemm(const uint16_t* x_sorted, const uint8_t* packed, const uint1
   if (rc != TQ_OK) return rc;
   if (N % 128 != 0 || tile_m < 1 || tile_m > 256 || cap < 1 || cap >= (static_cast<int64_t>(1) << 31))
     return TQ_ERR_INVALID_ARG;
+  if (n > 0 && !aligned16(y32)) return TQ_ERR_INVALID_ARG;
   if (n > 0 && (!sorted_pairs || !tiles || !num_tiles)) return TQ_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   rc = require_sm103(s);
