@@ -193,6 +193,7 @@ def run_ours(args, rank, world, dist):
             gev[timed_slot][1].record(stream)
         tq.tq_combine(y32, y)
 
+    lut_rate = tq.tq_probe_lut_rate(8)
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
@@ -286,7 +287,8 @@ def run_ours(args, rank, world, dist):
         "packed_GBps": round(mean_tiles * N * K / 4 / (grouped_ms * 1e-3) / 1e9, 1),
         "grouped_kernel_us": round(grouped_ms * 1e3, 2),
         "roofline": roof,
-        "decode_ceiling": decode_ceiling(mean_tiles, N, K, clk),
+        "decode_ceiling": decode_ceiling(mean_tiles, N, K, clk, lut_rate, grouped_ms * 1e3,
+                                         torch.cuda.get_device_properties(local).multi_processor_count),
         "gpu_launches": int(launches),
         "clocks": clk,
         "e2e": e2e,
@@ -296,18 +298,17 @@ def run_ours(args, rank, world, dist):
     return line
 
 
-def decode_ceiling(mean_tiles, N, K, clk):
+def decode_ceiling(mean_tiles, N, K, clk, rate, kernel_us, sms):
     """Every weight of every staged (m-tile, expert) is one random lookup in
-    the 2^16-entry LUT held in shared memory: 32 banks, so at most 32 lookups
-    per SM clock, and about 32/3.5 with the bank conflicts of random
-    addresses.  Reported beside the roofline."""
+    the 2^16-entry LUT held in shared memory; `rate` is that lookup rate as
+    measured on this GPU by tq_probe_lut_rate (lookups per clock per SM).
+    The decode cannot beat lookups / (SMs x rate x clock)."""
     lookups = mean_tiles * N * K
-    mhz = (clk or {}).get("sm_mhz") or 1900.0
-    sms = 152
-    ideal_us = lookups / (sms * mhz * 1e6 * 32) * 1e6
-    random_us = lookups / (sms * mhz * 1e6 * (32 / 3.5)) * 1e6
-    return {"lookups": int(lookups), "conflict_free_us": round(ideal_us, 1),
-            "random_bank_us": round(random_us, 1), "sm_mhz": mhz}
+    mhz = (clk or {}).get("sm_mhz") or 2070.0
+    ceiling_us = lookups / (sms * mhz * 1e6 * rate) * 1e6
+    return {"lookups": int(lookups), "lookups_per_clk_per_sm_measured": round(rate, 3),
+            "ceiling_us": round(ceiling_us, 1), "sm_mhz": mhz, "frac": round(ceiling_us / kernel_us, 4),
+            "kernel_lookups_per_clk_per_sm": round(lookups / (kernel_us * 1e-6) / sms / (mhz * 1e6), 3)}
 
 
 def run_e2e(args, tq, torch, sets, n, k, E, K, N, T):
@@ -479,6 +480,84 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_gate_study(args):
+    """GB300 gate study: both arms of the routed-expert product (grouped GEMM
+    at TILE_M 16 and 128, per-pair GEMV) across token counts at the
+    DeepSeek-V4 up shape, each kernel launch timed alone after an L2 flush.
+    The tile-fill predicate's choice (TILE_M 16) is printed beside."""
+    import torch
+    import trellis_quantized_moe_sort_gb300 as tq
+    from trellis_quantized_moe_sort_gb300 import build as b
+    b.build()
+    torch.cuda.set_device(0)
+    tq.tq_init(0)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    base = moe_inputs.make_problem("v4_decode_n32")
+    packed = _cuda(torch, base.packed)
+    lut = _cuda(torch, base.lut_bits.view(np.int16))
+    ns = [int(v) for v in args.gate_ns.split(",")]
+    for n in ns:
+        prob = moe_inputs.make_problem("v4_decode_n32", n=n, with_packed=False)
+        s = prob.shape
+        x, ids, w = _cuda(torch, prob.x_bits.view(np.int16)), _cuda(torch, prob.topk_ids), _cuda(torch, prob.topk_w)
+        y32 = torch.zeros((n, s.N), dtype=torch.float32, device="cuda")
+
+        graphed = []
+
+        def timed(fn):
+            """Median device time of fn, replayed from a CUDA graph (so host
+            launch gaps do not count) when capture works, else launched."""
+            fn()
+            torch.cuda.synchronize()
+            run = fn
+            try:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    fn()
+                run = g.replay
+                graphed.append(True)
+            except Exception:
+                torch.cuda.synchronize()
+                graphed.append(False)
+            ts = []
+            for _ in range(args.steps):
+                flush.zero_()
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                run()
+                b_.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b_) * 1e3)
+            return float(np.median(ts))
+
+        row = {"n": n, "pairs": n * s.top_k, "woken": int(len(np.unique(prob.topk_ids))),
+               "pairs_per_woken_expert": round(tq.tq_pairs_per_woken_expert(n, s.top_k, s.E), 3),
+               "predicate_arm_T16": {1: "gemv", 2: "grouped"}[tq.tq_select_arm(n, s.top_k, s.E, 16)]}
+        row["gemv_us"] = round(timed(lambda: tq.tq_gemv(x, packed, lut, ids, w, y32)), 1)
+        for T in (16, 128):
+            _, offsets, sp = tq.tq_route(ids, s.E)
+            cap = tq.tq_tile_map_capacity(n, s.top_k, s.E, T)
+            tiles, nt = tq.tq_build_tile_map(offsets, T, cap)
+            xs = tq.tq_gather_rows(x, sp, s.top_k)
+
+            counts = torch.empty(s.E, dtype=torch.int32, device="cuda")
+
+            def whole():  # route + tile map + gather + grouped GEMM (the arm's full device work)
+                tq.tq_route(ids, s.E, counts, offsets, sp)
+                tq.tq_build_tile_map(offsets, T, cap, tiles, nt)
+                tq.tq_gather_rows(x, sp, s.top_k, xs)
+                tq.tq_grouped_gemm(xs, packed, lut, sp, w, tiles, nt, s.top_k, T, y32)
+            row[f"grouped_T{T}_us"] = round(timed(whole), 1)
+        code, where = tq.tq_device_error()
+        if code:
+            raise RuntimeError(f"device error {code} at {where} (n={n})")
+        best = min(("gemv", row["gemv_us"]), ("grouped", row["grouped_T16_us"]), key=lambda kv: kv[1])
+        row["faster_arm"] = best[0]
+        row["grouped_over_gemv"] = round(row["gemv_us"] / row["grouped_T16_us"], 3)
+        row["cuda_graphs"] = all(graphed)
+        print(json.dumps(row), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -496,6 +575,8 @@ def main(argv=None):
     ap.add_argument("--sweep-workloads", default="", help="comma-separated subset for --sweep")
     ap.add_argument("--sweep-tiles", default="16,128", help="TILE_M values for --sweep")
     ap.add_argument("--sweep-no-gemv", action="store_true", help="skip the GEMV arm in --sweep")
+    ap.add_argument("--gate-study", action="store_true", help="both arms across token counts (V4 up shape)")
+    ap.add_argument("--gate-ns", default="1,2,4,8,9,16,32,64,128,256,512,682,683,1024")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes (read+write) per grouped launch, if captured for this build")
     args = ap.parse_args(argv)
@@ -513,6 +594,9 @@ def main(argv=None):
         dist = tdist
     if args.sweep:
         run_sweep(args)
+        return
+    if args.gate_study:
+        run_gate_study(args)
         return
     if args.impl == "reference":
         line = run_reference(args, rank, world)

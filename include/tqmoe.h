@@ -273,6 +273,16 @@ int tq_moe_forward_static(const uint16_t* x, const uint8_t* packed, const uint16
  * last read; *where (host, may be NULL) a kernel-specific location tag. */
 int tq_device_error(int* code, int* where);
 
+/* Rate of the resource that bounds the trellis decode: every SM loads the
+ * 65536-entry fp16/bf16 `table` (device, 16-byte aligned) into shared memory
+ * and its `warps_per_sm` (1..32) warps each perform iters x 16 random 16-bit
+ * lookups in it.  cycles (device) [SM count] receives each SM's clock cycles
+ * for the lookups; sink (device) [SM count x warps_per_sm x 32] receives one
+ * word per thread so no load is dead.  Lookups per clock per SM =
+ * warps_per_sm * 32 * iters * 16 / cycles. */
+int tq_probe_lut_rate(const uint16_t* table, int warps_per_sm, int iters, uint32_t* sink,
+                      unsigned long long* cycles, tq_stream_t stream);
+
 /* Host-side counts of successful launches since process start, per kernel:
  * out[0] route, out[1] tile map, out[2] grouped GEMM, out[3] GEMV,
  * out[4] combine, out[5] activation gather ([P3]: counters prove which arm

@@ -1,0 +1,44 @@
+"""The whole routed-expert product through tq_moe_forward at full size
+(sampled output rows against the oracle), and the decode-ceiling probe."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs
+import oracle.trellis_moe as O
+import trellis_quantized_moe_sort_gb300 as tq
+from gpu_util import to_device, normwise, sample_rows, check_no_device_error
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from trellis_quantized_moe_sort_gb300 import build
+    build.build()
+    tq.tq_init(0)
+
+
+@pytest.mark.parametrize("name,tile_m,pin", [("v4_decode_n32", 16, tq.ARM_GROUPED),
+                                              ("v4_decode_n32", 16, tq.ARM_GEMV),
+                                              ("v4_n128_down", 128, tq.ARM_AUTO),
+                                              ("v4_fill_n683", 16, tq.ARM_AUTO)])
+def test_moe_forward_full_size(name, tile_m, pin):
+    prob = moe_inputs.make_problem(name)
+    d = to_device(prob)
+    s = prob.shape
+    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=tile_m, pin=pin)
+    check_no_device_error()
+    want_arm = pin if pin else tq.tq_select_arm(s.n, s.top_k, s.E, tile_m)
+    assert arm == want_arm
+    rows = sample_rows(s.N, 32, seed=7)
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L, rows=rows)
+    got = y[:, torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    assert normwise(got, ref) <= TOL
+
+
+def test_lut_probe_rate_is_sane():
+    rate = tq.tq_probe_lut_rate(8, 128)
+    # between random-address bank conflicts at their worst and 32 banks per clock
+    assert 2.0 < rate <= 32.0, rate

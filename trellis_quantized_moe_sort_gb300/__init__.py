@@ -20,7 +20,7 @@ __all__ = [
     "tq_tiles_amortize", "tq_grouped_min_tokens", "tq_tile_map_capacity", "tq_select_arm",
     "tq_route", "tq_build_tile_map", "tq_gather_rows", "tq_grouped_gemm", "tq_gemv", "tq_combine",
     "tq_moe_workspace_size", "tq_moe_forward", "tq_moe_forward_static", "tq_device_error", "tq_launch_counts",
-    "tq_status_string", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "EXPORTED_SYMBOLS",
+    "tq_status_string", "tq_probe_lut_rate", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "EXPORTED_SYMBOLS",
 ]
 
 ARM_AUTO, ARM_GEMV, ARM_GROUPED = 0, 1, 2
@@ -53,6 +53,7 @@ _SIGS = {
                                 ctypes.POINTER(_c_int), _c_p]),
     "tq_moe_forward_static": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int,
                                        _c_int, _c_int, _c_int, _c_int, _c_p, ctypes.POINTER(_c_int), _c_p]),
+    "tq_probe_lut_rate": (_c_int, [_c_p, _c_int, _c_int, _c_p, _c_p, _c_p]),
     "tq_device_error": (_c_int, [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
     "tq_launch_counts": (None, [ctypes.POINTER(_c_i64)]),
 }
@@ -314,6 +315,22 @@ def tq_moe_forward_static(x, packed, lut, topk_ids, topk_w, tile_m: int = 16, pi
                                        pin, _dev_ptr(y, _bits16(), "y"), ctypes.byref(arm), _stream(stream)),
            "tq_moe_forward_static")
     return y, arm.value
+
+
+def tq_probe_lut_rate(warps_per_sm: int = 8, iters: int = 512, stream=None) -> float:
+    """Measured random 16-bit shared-memory lookups per clock per SM (the
+    resource that bounds the trellis decode)."""
+    torch = _torch()
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    table = torch.zeros(65536, dtype=torch.int16, device="cuda")
+    sink = torch.empty(sms * warps_per_sm * 32, dtype=torch.int32, device="cuda")
+    cycles = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    _check(lib().tq_probe_lut_rate(_dev_ptr(table, _bits16(), "table"), warps_per_sm, iters,
+                                   _dev_ptr(sink, (torch.int32,), "sink"), _dev_ptr(cycles, (torch.int64,), "cycles"),
+                                   _stream(stream)), "tq_probe_lut_rate")
+    torch.cuda.synchronize()
+    c = float(cycles.double().mean())
+    return warps_per_sm * 32 * iters * 16 / c
 
 
 def tq_device_error() -> tuple[int, int]:
