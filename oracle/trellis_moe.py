@@ -10,7 +10,8 @@ states the passage it follows.  Page titles used in the citations:
   "Tests" (flip-point tests), and the post-merge note (the n <= 8 floor).
 * [P2] "perf(qtip): arch-specialise the trellis grouped GEMM (D16) + close the
   silent-failure holes (D18)" — commit message items 1 (m-tile) and 2
-  (contiguous-run decode, window identity, "runs stay independent"), and
+  (contiguous-run decode seeded by the window identity, runs independent of
+  each other), and
   "The two changes" (packed 2-bit bytes cross HBM; decode fused into the
   multiply).
 
@@ -31,7 +32,7 @@ R4  Pairs.  Pair p = t * top_k + j for token t and its j-th routed expert.
     Routing sorts pairs by expert, stably (equal experts keep ascending p).
 R5  Tile map.  For experts in ascending order with count_e > 0, tiles
     (e, offsets[e] + i*T, min(T, count_e - i*T)) for i < ceil(count_e / T)
-    ([P1]: "walks sum_e ceil(count_e / GROUPED_TILE_M) m-tiles").
+    ([P1]: the kernel visits sum_e ceil(count_e / TILE_M) m-tiles).
 R6  Output.  Y[t, r] = sum_j w[t,j] * sum_i W_{e(t,j)}[r, i] * x[t, i], x read
     exactly from bf16, w as fp32; the library then rounds to bf16.
 R7  Gate.  tiles_amortize(n,k,E,T) := n > 0 and

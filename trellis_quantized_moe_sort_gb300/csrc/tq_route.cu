@@ -1,12 +1,12 @@
 // Routing sort, m-tile map and the bf16 combine.
 //
-// Routing: the grouped GEMM "sorts pairs by expert and walks
-// sum_e ceil(count_e / GROUPED_TILE_M) m-tiles" (page "fix(qtip): gate the
-// trellis grouped GEMM on m-tile occupancy, not token count", section "The
-// cause is a threshold, not a kernel defect").  The sort here is a stable
-// counting sort done by one thread block: each warp owns a contiguous slice of
-// the pair list, so ranking lanes with equal experts (match.any) inside a warp
-// and offsetting by the counts of lower warps keeps ascending pair order.
+// Routing: the grouped GEMM works on pairs sorted by expert and visits
+// sum_e ceil(count_e / TILE_M) m-tiles (page "fix(qtip): gate the trellis
+// grouped GEMM on m-tile occupancy, not token count", section "The cause is a
+// threshold, not a kernel defect").  The sort here is a stable counting sort
+// done by one thread block: each warp owns a contiguous slice of the pair
+// list, so ranking lanes with equal experts (match.any) inside a warp and
+// offsetting by the counts of lower warps keeps ascending pair order.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
