@@ -82,6 +82,15 @@ def measured_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest
+    replica sets the job's time)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 # --------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -226,9 +235,7 @@ def run_ours(args, rank, world, dist):
     grouped_ms = float(np.mean([a.elapsed_time(b_) for a, b_ in gev]))
     launches = sum(counts_after[key] - counts_before[key] for key in counts_after)
     if dist is not None:
-        tt = torch.tensor([ms_step, grouped_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step, grouped_ms = float(tt[0]), float(tt[1])
+        ms_step, grouped_ms = max_over_ranks([ms_step, grouped_ms], dist, "cuda")
 
     # tiles per set (device) for the traffic model; correctness spot check vs nothing on the hot path
     tiles_per_set = []
@@ -589,7 +596,8 @@ def main(argv=None):
     if world > 1:
         import torch
         import torch.distributed as tdist
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        if args.impl == "ours":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         tdist.init_process_group("nccl" if args.impl == "ours" else "gloo")
         dist = tdist
     if args.sweep:
