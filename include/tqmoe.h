@@ -139,6 +139,26 @@ int tq_route(const int32_t* topk_ids, int64_t n, int top_k, int E,
              tq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Device router: per token the top_k experts by fp32 logit (descending;
+ * equal logits go to the lower expert id) and their weights, a softmax over
+ * the picked logits computed in fp32.  The router GEMM that produces the
+ * logits is not part of this library.  Page "The 794 ms decode step,
+ * itemised", list of un-owned items: the router runs in fp32.
+ *
+ * logits   (device) fp32 [n][E]; non-finite values count as -infinity (a row
+ *          with no finite logit gets equal weights).
+ * topk_ids (device) int32 [n][top_k] out; topk_w (device) fp32 [n][top_k] out.
+ * Limits: 1 <= top_k <= min(E, 32), E <= 1024.
+ * tq_route_logits = tq_router_topk then tq_route on the ids it wrote.
+ * ------------------------------------------------------------------------- */
+int tq_router_topk(const float* logits, int64_t n, int E, int top_k,
+                   int32_t* topk_ids, float* topk_w, tq_stream_t stream);
+int tq_route_logits(const float* logits, int64_t n, int E, int top_k,
+                    int32_t* topk_ids, float* topk_w,
+                    int32_t* counts, int32_t* offsets, int32_t* sorted_pairs,
+                    tq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * m-tile map  ([P1] "The cause is a threshold"; [P2] D18: route and GEMM must
  * agree on tile_m)
  *
@@ -285,9 +305,9 @@ int tq_probe_lut_rate(const uint16_t* table, int warps_per_sm, int iters, uint32
 
 /* Host-side counts of successful launches since process start, per kernel:
  * out[0] route, out[1] tile map, out[2] grouped GEMM, out[3] GEMV,
- * out[4] combine, out[5] activation gather ([P3]: counters prove which arm
- * ran). */
-void tq_launch_counts(int64_t out[6]);
+ * out[4] combine, out[5] activation gather, out[6] router top-k ([P3]:
+ * counters prove which arm ran). */
+void tq_launch_counts(int64_t out[7]);
 
 #ifdef __cplusplus
 }

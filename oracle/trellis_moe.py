@@ -48,7 +48,7 @@ __all__ = [
     "symbols", "states_window", "run_states", "lut_values", "decode_rows",
     "bf16_bits_to_f64", "route", "tile_map", "expected_woken_experts",
     "pairs_per_woken_expert", "tile_fill", "tiles_amortize", "grouped_min_tokens",
-    "tile_map_capacity", "dispatch_arm", "moe_forward", "bf16_rne_bits",
+    "tile_map_capacity", "dispatch_arm", "moe_forward", "bf16_rne_bits", "router_topk",
     "DECODE_REGIME_MAX_TOKENS",
 ]
 
@@ -213,6 +213,30 @@ def dispatch_arm(n: int, top_k: int, E: int, tile_m: int, pin: str = "auto") -> 
     if n <= DECODE_REGIME_MAX_TOKENS or not tiles_amortize(n, top_k, E, tile_m):
         return "gemv"
     return "grouped"
+
+
+# ---------------------------------------------------------------------------
+# Router top-k  (reading R13: each token's top_k experts by logit, weighted by
+# a softmax over the picked logits; page "The 794 ms decode step, itemised",
+# list of un-owned items, notes that the router runs in fp32)
+# ---------------------------------------------------------------------------
+
+def router_topk(logits: np.ndarray, top_k: int):
+    """Per token: the top_k experts by logit, descending, ties to the lower
+    expert id; weights = softmax over those top_k logits (fp64).  Non-finite
+    logits count as -infinity; a row with no finite logit gets equal weights.
+    logits float32 [n, E] -> (ids int32 [n, k], weights float64 [n, k])."""
+    lg = np.asarray(logits, dtype=np.float32).astype(np.float64)
+    lg = np.where(np.isnan(lg) | (lg == np.inf), -np.inf, lg)
+    n, E = lg.shape
+    if not 1 <= top_k <= E:
+        raise ValueError("need 1 <= top_k <= E")
+    order = np.lexsort((np.broadcast_to(np.arange(E), (n, E)), -lg), axis=1)[:, :top_k]
+    sel = np.take_along_axis(lg, order, axis=1)
+    top = sel[:, :1]
+    with np.errstate(invalid="ignore"):
+        z = np.where(np.isfinite(top), np.exp(sel - np.where(np.isfinite(top), top, 0.0)), 1.0)
+    return order.astype(np.int32), z / z.sum(axis=1, keepdims=True)
 
 
 # ---------------------------------------------------------------------------

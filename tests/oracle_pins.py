@@ -66,7 +66,7 @@ def pin_gate_points():
             assert T.dispatch_arm(n, k, E, tm) == val
         else:
             raise AssertionError(f"unknown fact {fact}")
-    # "no selection at n = 9...512, selection at 683+"
+    # the pages' test: the grouped arm is not selected for 9 <= n <= 682, and is from 683 on
     assert not any(T.tiles_amortize(n, 6, 256, 16) for n in range(9, 683))
     assert all(T.tiles_amortize(n, 6, 256, 16) for n in range(683, 4000))
     assert all(T.dispatch_arm(n, 6, 256, 16) == "gemv" for n in range(0, 683))
@@ -381,7 +381,32 @@ def pin_bf16_rne():
     assert np.array_equal(got, want)
 
 
+def pin_router_topk():
+    """Top-k by a Python sort on (-logit, expert) and softmax by math.exp and
+    fsum; ties to the lower expert id; weights sum to one; k = E keeps every
+    expert; a constant row picks experts 0..k-1 with equal weights."""
+    rng = np.random.Generator(np.random.PCG64(44))
+    for (n, E, k) in ((5, 8, 2), (7, 256, 6), (3, 16, 16), (4, 33, 5)):
+        lg = rng.standard_normal((n, E)).astype(np.float32)
+        lg[0, 3] = lg[0, 5] = lg[0].max() + 1.0           # an exact tie at the top
+        ids, w = T.router_topk(lg, k)
+        for t in range(n):
+            want = sorted(range(E), key=lambda e: (-float(lg[t, e]), e))[:k]
+            assert ids[t].tolist() == want, (n, E, k, t)
+            ex = [math.exp(float(lg[t, e]) - float(lg[t, want[0]])) for e in want]
+            tot = math.fsum(ex)
+            assert np.allclose(w[t], [v / tot for v in ex], rtol=1e-12, atol=0)
+            assert abs(w[t].sum() - 1) < 1e-12
+        assert ids[0, 0] == 3 and ids[0, 1] == 5
+    ids, w = T.router_topk(np.zeros((2, 8), np.float32), 3)
+    assert ids.tolist() == [[0, 1, 2]] * 2 and np.allclose(w, 1 / 3)
+    bad = np.array([[np.nan, 1.0, -np.inf, np.inf, 0.5], [np.nan] * 5], np.float32)
+    ids, w = T.router_topk(bad, 3)
+    assert ids[0].tolist() == [1, 4, 0] and abs(w[0, 2]) == 0.0
+    assert ids[1].tolist() == [0, 1, 2] and np.allclose(w[1], 1 / 3)
+
+
 ALL_PINS = [pin_fill_table, pin_gate_points, pin_gate_closed_forms, pin_min_tokens_flip,
             pin_capacity_bound, pin_decode_bitfield, pin_run_decode_identity,
             pin_special_luts, pin_bruteforce_tiny, pin_constant_lut, pin_onehot_x,
-            pin_route_bruteforce, pin_tile_map, pin_bf16_rne]
+            pin_route_bruteforce, pin_tile_map, pin_bf16_rne, pin_router_topk]

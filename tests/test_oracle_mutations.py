@@ -112,7 +112,26 @@ def _bf16_ties_away(y32):
     return ((u + 0x8000) >> 16).astype(np.uint16)
 
 
+def _topk_ties_high(logits, top_k):
+    lg = np.asarray(logits, dtype=np.float32).astype(np.float64)
+    n, E = lg.shape
+    order = np.lexsort((-np.broadcast_to(np.arange(E), (n, E)), -lg), axis=1)[:, :top_k]
+    sel = np.take_along_axis(lg, order, axis=1)
+    z = np.exp(sel - sel[:, :1])
+    return order.astype(np.int32), z / z.sum(axis=1, keepdims=True)
+
+
+def _topk_softmax_all(logits, top_k):
+    ids, _ = orig["router_topk"](logits, top_k)
+    lg = np.asarray(logits, dtype=np.float64)
+    z = np.exp(lg - lg.max(axis=1, keepdims=True))
+    full = z / z.sum(axis=1, keepdims=True)
+    return ids, np.take_along_axis(full, ids.astype(np.int64), axis=1)
+
+
 MUTATIONS = {
+    "topk_ties_high": ("router_topk", _topk_ties_high),
+    "topk_softmax_over_all": ("router_topk", _topk_softmax_all),
     "symbol_off_by_one": ("symbols", _symbols_off_by_one),
     "state_mask": ("states_window", _window_wrong_mask),
     "window_too_wide": ("states_window", _window_too_wide),

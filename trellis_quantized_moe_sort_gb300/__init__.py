@@ -18,7 +18,7 @@ import os
 __all__ = [
     "TQError", "lib", "lib_path", "tq_init", "tq_arch_witness", "tq_pairs_per_woken_expert",
     "tq_tiles_amortize", "tq_grouped_min_tokens", "tq_tile_map_capacity", "tq_select_arm",
-    "tq_route", "tq_build_tile_map", "tq_gather_rows", "tq_grouped_gemm", "tq_gemv", "tq_combine",
+    "tq_route", "tq_router_topk", "tq_route_logits", "tq_build_tile_map", "tq_gather_rows", "tq_grouped_gemm", "tq_gemv", "tq_combine",
     "tq_moe_workspace_size", "tq_moe_forward", "tq_moe_forward_static", "tq_device_error", "tq_launch_counts",
     "tq_status_string", "tq_probe_lut_rate", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "EXPORTED_SYMBOLS",
 ]
@@ -41,6 +41,8 @@ _SIGS = {
     "tq_select_arm": (_c_int, [_c_i64, _c_int, _c_int, _c_int, _c_int]),
     "tq_route": (_c_int, [_c_p, _c_i64, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p]),
     "tq_build_tile_map": (_c_int, [_c_p, _c_int, _c_int, _c_p, _c_p, _c_i64, _c_p]),
+    "tq_router_topk": (_c_int, [_c_p, _c_i64, _c_int, _c_int, _c_p, _c_p, _c_p]),
+    "tq_route_logits": (_c_int, [_c_p, _c_i64, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
     "tq_grouped_gemm": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64,
                                  _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p]),
     "tq_gemv": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int, _c_int,
@@ -186,6 +188,35 @@ def tq_route(topk_ids, E: int, counts=None, offsets=None, sorted_pairs=None, str
                           _dev_ptr(sorted_pairs, (torch.int32,), "sorted_pairs"), _stream(stream)),
            "tq_route")
     return counts, offsets, sorted_pairs[: n * k]
+
+
+def tq_router_topk(logits, top_k: int, topk_ids=None, topk_w=None, stream=None):
+    """Per-token top_k experts and softmax weights from fp32 logits [n, E]."""
+    torch = _torch()
+    n, E = logits.shape
+    topk_ids = torch.empty((n, top_k), dtype=torch.int32, device=logits.device) if topk_ids is None else topk_ids
+    topk_w = torch.empty((n, top_k), dtype=torch.float32, device=logits.device) if topk_w is None else topk_w
+    _check(lib().tq_router_topk(_dev_ptr(logits, (torch.float32,), "logits"), n, E, top_k,
+                                _dev_ptr(topk_ids, (torch.int32,), "topk_ids"),
+                                _dev_ptr(topk_w, (torch.float32,), "topk_w"), _stream(stream)), "tq_router_topk")
+    return topk_ids, topk_w
+
+
+def tq_route_logits(logits, top_k: int, stream=None):
+    """Router top-k then the routing sort -> (ids, w, counts, offsets, sorted_pairs)."""
+    torch = _torch()
+    n, E = logits.shape
+    dev = logits.device
+    ids = torch.empty((n, top_k), dtype=torch.int32, device=dev)
+    w = torch.empty((n, top_k), dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sp = torch.empty(max(n * top_k, 1), dtype=torch.int32, device=dev)
+    _check(lib().tq_route_logits(_dev_ptr(logits, (torch.float32,), "logits"), n, E, top_k,
+                                 _dev_ptr(ids, (torch.int32,), "topk_ids"), _dev_ptr(w, (torch.float32,), "topk_w"),
+                                 _dev_ptr(counts, (torch.int32,), "counts"), _dev_ptr(offsets, (torch.int32,), "offsets"),
+                                 _dev_ptr(sp, (torch.int32,), "sorted_pairs"), _stream(stream)), "tq_route_logits")
+    return ids, w, counts, offsets, sp[: n * top_k]
 
 
 def tq_build_tile_map(offsets, tile_m: int, cap: int, tiles=None, num_tiles=None, stream=None):
@@ -341,6 +372,6 @@ def tq_device_error() -> tuple[int, int]:
 
 
 def tq_launch_counts() -> dict:
-    arr = (ctypes.c_int64 * 6)()
+    arr = (ctypes.c_int64 * 7)()
     lib().tq_launch_counts(arr)
-    return dict(zip(("route", "tile_map", "grouped", "gemv", "combine", "gather"), list(arr)))
+    return dict(zip(("route", "tile_map", "grouped", "gemv", "combine", "gather", "router"), list(arr)))

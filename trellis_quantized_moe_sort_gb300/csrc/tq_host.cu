@@ -262,6 +262,24 @@ int tq_route(const int32_t* topk_ids, int64_t n, int top_k, int E, int32_t* coun
   return launch_route(topk_ids, static_cast<int>(P), E, counts, offsets, sorted_pairs, err, s);
 }
 
+int tq_router_topk(const float* logits, int64_t n, int E, int top_k, int32_t* topk_ids, float* topk_w,
+                   tq_stream_t stream) {
+  if (bad_shape(top_k, E) || E > 1024 || top_k > 32 || n < 0 || n >= (static_cast<int64_t>(1) << 31))
+    return TQ_ERR_INVALID_ARG;
+  if (n > 0 && (!logits || !topk_ids || !topk_w)) return TQ_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int rc = require_sm103(s);
+  if (rc != TQ_OK) return rc;
+  return launch_router(logits, static_cast<int>(n), E, top_k, topk_ids, topk_w, s);
+}
+
+int tq_route_logits(const float* logits, int64_t n, int E, int top_k, int32_t* topk_ids, float* topk_w,
+                    int32_t* counts, int32_t* offsets, int32_t* sorted_pairs, tq_stream_t stream) {
+  int rc = tq_router_topk(logits, n, E, top_k, topk_ids, topk_w, stream);
+  if (rc != TQ_OK) return rc;
+  return tq_route(topk_ids, n, top_k, E, counts, offsets, sorted_pairs, stream);
+}
+
 int tq_build_tile_map(const int32_t* offsets, int E, int tile_m, int32_t* tiles, int32_t* num_tiles,
                       int64_t cap, tq_stream_t stream) {
   if (E < 1 || E > 1024 || tile_m < 1 || tile_m > 256 || cap < 1 || cap >= (static_cast<int64_t>(1) << 31))
@@ -455,7 +473,7 @@ int tq_device_error(int* code, int* where) {
   return TQ_OK;
 }
 
-void tq_launch_counts(int64_t out[6]) {
+void tq_launch_counts(int64_t out[7]) {
   if (!out) return;
   for (int i = 0; i < kCntNum; ++i) out[i] = g_counts[i].load();
 }

@@ -18,7 +18,7 @@ int require_sm103(cudaStream_t stream);
 // Converts the last launch error into a status and clears it.
 int launch_status();
 
-enum Counter { kCntRoute = 0, kCntTileMap, kCntGrouped, kCntGemv, kCntCombine, kCntGather, kCntNum };
+enum Counter { kCntRoute = 0, kCntTileMap, kCntGrouped, kCntGemv, kCntCombine, kCntGather, kCntRouter, kCntNum };
 void count_launch(Counter c);
 
 // Number of SMs of the current device (cached per device).
@@ -31,6 +31,7 @@ int launch_route(const int32_t* topk_ids, int P, int E, int32_t* counts, int32_t
 int launch_tile_map(const int32_t* offsets, int E, int tile_m, int32_t* tiles, int32_t* num_tiles,
                     int64_t cap, int* err, cudaStream_t s);
 int launch_combine(const float* y32, uint16_t* y, int64_t count, cudaStream_t s);
+int launch_router(const float* logits, int n, int E, int top_k, int32_t* ids, float* w, cudaStream_t s);
 int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top_k, int K,
                   uint16_t* x_sorted, int* err, cudaStream_t s);
 int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,

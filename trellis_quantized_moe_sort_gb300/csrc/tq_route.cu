@@ -199,7 +199,79 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* _
   }
 }
 
+// Router top-k: one warp per token.  Lane l holds logits l, l+32, ... ;
+// top_k rounds of a warp arg-max (larger logit wins, equal logits go to the
+// lower expert id, taken experts are skipped) pick the experts in descending
+// order; the weights are a softmax over the picked logits in fp32.
+// Non-finite logits count as -infinity; a row with no finite logit gets
+// equal weights.
+template <int PER_LANE>
+__global__ void router_topk_kernel(const float* __restrict__ logits, int n, int E, int top_k,
+                                   int32_t* __restrict__ ids, float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < n; t += gridDim.x * warps) {
+    float v[PER_LANE];
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+      const int e = lane + 32 * i;
+      const float x = (e < E) ? logits[static_cast<size_t>(t) * E + e] : -INFINITY;
+      v[i] = (x == x && x != INFINITY) ? x : -INFINITY;
+    }
+    uint32_t taken = 0;
+    float top0 = 0.f, sum = 0.f, mine = 0.f;
+    int mine_e = 0;
+    for (int j = 0; j < top_k; ++j) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < PER_LANE; ++i) {
+        const int e = lane + 32 * i;
+        const bool free = e < E && !((taken >> i) & 1u);
+        if (free && (v[i] > bv || (v[i] == bv && e < be))) {
+          bv = v[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (j == 0) top0 = bv;
+      const float ex = (top0 == -INFINITY) ? 1.f : expf(bv - top0);
+      sum += ex;
+      if (j == lane) {
+        mine = ex;
+        mine_e = be;
+      }
+    }
+    if (lane < top_k) {
+      ids[static_cast<size_t>(t) * top_k + lane] = mine_e;
+      w[static_cast<size_t>(t) * top_k + lane] = mine / sum;
+    }
+  }
+}
+
 }  // namespace
+
+int launch_router(const float* logits, int n, int E, int top_k, int32_t* ids, float* w, cudaStream_t s) {
+  if (n == 0) return TQ_OK;
+  const int threads = 256, warps = threads / 32;
+  const int blocks = std::max(1, std::min((n + warps - 1) / warps, sm_count() * 8));
+  if (E <= 256)
+    router_topk_kernel<8><<<blocks, threads, 0, s>>>(logits, n, E, top_k, ids, w);
+  else
+    router_topk_kernel<32><<<blocks, threads, 0, s>>>(logits, n, E, top_k, ids, w);
+  const int st = launch_status();
+  if (st == TQ_OK) count_launch(kCntRouter);
+  return st;
+}
 
 int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top_k, int K, uint16_t* x_sorted,
                   int* err, cudaStream_t s) {
