@@ -565,6 +565,57 @@ def run_gate_study(args):
         print(json.dumps(row), flush=True)
 
 
+def run_mlp_sweep(args):
+    """Whole SwiGLU expert MLP (tq_moe_mlp_forward) per workload: median time
+    per call after an L2 flush, with the lookup count it decodes."""
+    import torch
+    import trellis_quantized_moe_sort_gb300 as tq
+    from trellis_quantized_moe_sort_gb300 import build as b
+    b.build()
+    torch.cuda.set_device(0)
+    tq.tq_init(0)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    rate = tq.tq_probe_lut_rate(8)
+    for name in moe_inputs.MLP_WORKLOADS:
+        prob = moe_inputs.make_mlp_problem(name)
+        c = lambda a: _cuda(torch, a)
+        x, ids, w = c(prob.x_bits.view(np.int16)), c(prob.topk_ids), c(prob.topk_w)
+        pgu, lgu = c(prob.packed_gu), c(prob.lut_gu.view(np.int16))
+        pd, ld = c(prob.packed_down), c(prob.lut_down.view(np.int16))
+        T = args.tile_m if prob.n <= 1024 else 128
+        ws = torch.empty(tq.tq_moe_mlp_workspace_size(prob.n, prob.top_k, prob.E, prob.H, prob.I, T),
+                         dtype=torch.uint8, device="cuda")
+        y = torch.empty((prob.n, prob.H), dtype=torch.bfloat16, device="cuda")
+        call = lambda: tq.tq_moe_mlp_forward(x, pgu, lgu, pd, ld, ids, w, tile_m=T, workspace=ws, y=y)
+        call()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            call()
+            b_.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b_) * 1e3)
+        code, where = tq.tq_device_error()
+        if code:
+            raise RuntimeError(f"device error {code} at {where} ({name})")
+        counts = np.bincount(prob.topk_ids.reshape(-1), minlength=prob.E)
+        tiles = int(np.sum(-(-counts // T)))
+        lookups = tiles * (2 * prob.I * prob.H + prob.H * prob.I)
+        us = float(np.median(ts))
+        ceiling = lookups / (152 * rate * 2.07e9) * 1e6
+        flops = 2 * prob.n * prob.top_k * 3 * prob.H * prob.I
+        print(json.dumps({"workload": name, "tile_m": T, "n": prob.n, "pairs": prob.n * prob.top_k, "m_tiles": tiles,
+                          "us_per_call": round(us, 1), "tokens_per_s": round(prob.n / (us * 1e-6), 1),
+                          "lookups": lookups, "decode_ceiling_us": round(ceiling, 1),
+                          "decode_frac": round(ceiling / us, 3),
+                          "tensor_roofline_us": round(flops / (measured_peaks()[2] * 1e12) * 1e6, 1)}), flush=True)
+        del x, pgu, pd, ws, y
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -583,6 +634,7 @@ def main(argv=None):
     ap.add_argument("--sweep-tiles", default="16,128", help="TILE_M values for --sweep")
     ap.add_argument("--sweep-no-gemv", action="store_true", help="skip the GEMV arm in --sweep")
     ap.add_argument("--gate-study", action="store_true", help="both arms across token counts (V4 up shape)")
+    ap.add_argument("--mlp-sweep", action="store_true", help="whole SwiGLU expert MLP per workload")
     ap.add_argument("--gate-ns", default="1,2,4,8,9,16,32,64,128,256,512,682,683,1024")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes (read+write) per grouped launch, if captured for this build")
@@ -605,6 +657,9 @@ def main(argv=None):
         return
     if args.gate_study:
         run_gate_study(args)
+        return
+    if args.mlp_sweep:
+        run_mlp_sweep(args)
         return
     if args.impl == "reference":
         line = run_reference(args, rank, world)

@@ -285,6 +285,38 @@ int tq_moe_forward_static(const uint16_t* x, const uint8_t* packed, const uint16
                           uint16_t* y, int* arm_used, tq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The whole expert MLP (SwiGLU experts).  The routed-expert grouped GEMM
+ * above is one of an expert's three projections; these calls chain them:
+ *   gate|up_p = W_gu,e x_t,  h_p = silu(gate_p) * up_p,
+ *   y_t = sum_j w_tj W_down,e h_(t,j).
+ * packed_gu (device) uint8 [E][2I][H/4]: rows 0..I-1 the gate, I..2I-1 the
+ * up projection; packed_down (device) uint8 [E][H][I/4]; one LUT each
+ * (fp16 [2^L]); the same L.
+ *
+ * tq_grouped_gemm_pairs: the grouped GEMM with per-pair outputs and no
+ *   router weight: out32[slot][:] += W_e x_sorted[slot] for every sorted
+ *   slot (out32 (device) fp32 [n*top_k][N], 16-byte aligned, zero it first).
+ * tq_swiglu: h[s][i] = bf16(silu(g) * u), g = gate_up[s][i],
+ *   u = gate_up[s][I + i]; gate_up (device) fp32 [P][2I], h (device) bf16
+ *   [P][I]; I % 4 == 0.
+ * tq_moe_mlp_forward: route, tile map, gather, gate|up (per pair), SwiGLU,
+ *   down (combined per token with the router weights), bf16 y [n][H]; the
+ *   grouped arm only.  H % 128 == 0, I % 64 == 0.  workspace (device) >=
+ *   tq_moe_mlp_workspace_size(...) bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------- */
+int tq_grouped_gemm_pairs(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
+                          const int32_t* sorted_pairs, const int32_t* tiles, const int32_t* num_tiles,
+                          int64_t cap, int64_t n, int top_k, int E, int K, int N, int tile_m,
+                          float* out32, tq_stream_t stream);
+int tq_swiglu(const float* gate_up, int64_t P, int I, uint16_t* h, tq_stream_t stream);
+size_t tq_moe_mlp_workspace_size(int64_t n, int top_k, int E, int H, int I, int tile_m);
+int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16_t* lut_gu,
+                       const uint8_t* packed_down, const uint16_t* lut_down, int L,
+                       const int32_t* topk_ids, const float* topk_w,
+                       int64_t n, int top_k, int E, int H, int I, int tile_m,
+                       void* workspace, size_t workspace_bytes, uint16_t* y, tq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Diagnostics
  * ------------------------------------------------------------------------- */
 

@@ -170,3 +170,48 @@ def make_custom(E: int, top_k: int, n: int, K: int, N: int, L: int, seed: int,
     ids, w = draw_routing(rr, n, E, top_k, routing)
     return Problem(shp, x, ids, w, draw_packed(rp, E, N, K), draw_lut(rl, L, K),
                    (seed,))
+
+
+# ---------------------------------------------------------------------------
+# Whole expert MLP: y = sum_j w_j * W_down,e (silu(W_gate,e x) * (W_up,e x)).
+# The gate and up matrices of an expert are stored as one [2I, H] bitstream
+# block (rows 0..I-1 gate, I..2I-1 up), the down matrix as [H, I].
+# ---------------------------------------------------------------------------
+
+@dataclass
+class MLPProblem:
+    name: str
+    E: int
+    top_k: int
+    n: int
+    H: int          # hidden size (gate/up input, down output)
+    I: int          # expert intermediate size
+    L: int
+    x_bits: np.ndarray
+    topk_ids: np.ndarray
+    topk_w: np.ndarray
+    packed_gu: np.ndarray      # uint8 [E, 2I, H/4]
+    lut_gu: np.ndarray         # fp16 bits [2^L], N(0, 1/H)
+    packed_down: np.ndarray    # uint8 [E, H, I/4]
+    lut_down: np.ndarray       # fp16 bits [2^L], N(0, 1/I)
+
+
+MLP_WORKLOADS = {
+    # name: (E, top_k, n, H, I, L, routing)
+    "tiny_mlp_e8_k2_n16": (8, 2, 16, 256, 128, 12, "uniform"),
+    "v4_mlp_n32": (256, 6, 32, 4096, 2048, 16, "uniform"),
+    "v4_mlp_n128": (256, 6, 128, 4096, 2048, 16, "uniform"),
+    "v4_mlp_prefill_n8192": (256, 6, 8192, 4096, 2048, 16, "zipf"),
+}
+
+
+def make_mlp_problem(name: str, n: int | None = None, layer: int = 0) -> MLPProblem:
+    E, k, n0, H, I, L, routing = MLP_WORKLOADS[name]
+    n = n0 if n is None else n
+    ss = np.random.SeedSequence([BASE_SEED, 777, list(MLP_WORKLOADS).index(name), layer, n])
+    rx, rr, rg, rlg, rd, rld = [np.random.Generator(np.random.PCG64(s)) for s in ss.spawn(6)]
+    x = draw_x(rx, n, H)
+    ids, w = draw_routing(rr, n, E, k, routing)
+    return MLPProblem(name, E, k, n, H, I, L, x, ids, w,
+                      draw_packed(rg, E, 2 * I, H), draw_lut(rlg, L, H),
+                      draw_packed(rd, E, H, I), draw_lut(rld, L, I))

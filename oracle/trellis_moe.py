@@ -49,6 +49,7 @@ __all__ = [
     "bf16_bits_to_f64", "route", "tile_map", "expected_woken_experts",
     "pairs_per_woken_expert", "tile_fill", "tiles_amortize", "grouped_min_tokens",
     "tile_map_capacity", "dispatch_arm", "moe_forward", "bf16_rne_bits", "router_topk",
+    "silu", "moe_mlp",
     "DECODE_REGIME_MAX_TOKENS",
 ]
 
@@ -287,3 +288,40 @@ def bf16_rne_bits(y32: np.ndarray) -> np.ndarray:
     dl, dh = mag - mag_lo, mag_hi - mag
     pick_hi = (dh < dl) | ((dh == dl) & ((lo & 1) == 1))
     return np.where(pick_hi, hi, lo).astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# The whole expert MLP  (reading R14: the routed-expert GEMM is one of three
+# projections of a SwiGLU expert; gate and up share the input, down takes
+# silu(gate) * up of the same pair)
+# ---------------------------------------------------------------------------
+
+def silu(v):
+    """x * sigmoid(x) = x / (1 + e^-x)."""
+    return v / (1.0 + np.exp(-v))
+
+
+def moe_mlp(x_bits, topk_ids, topk_w, packed_gu, lut_gu, packed_down, lut_down, L, tokens=None):
+    """Y[t] = sum_j w[t,j] * W_down,e (silu(W_gate,e x_t) * (W_up,e x_t)), fp64.
+
+    packed_gu [E, 2I, H/4] holds each expert's gate rows (0..I-1) then up rows
+    (I..2I-1); packed_down [E, H, I/4].  ``tokens`` restricts the output to
+    those tokens (only their experts are decoded).  Returns [len(tokens), H]."""
+    x = bf16_bits_to_f64(x_bits)
+    ids = np.asarray(topk_ids)
+    w = np.asarray(topk_w, dtype=np.float32).astype(np.float64)
+    tokens = np.arange(ids.shape[0]) if tokens is None else np.asarray(tokens)
+    I = packed_gu.shape[1] // 2
+    H = packed_down.shape[1]
+    Y = np.zeros((len(tokens), H), dtype=np.float64)
+    sub = ids[tokens]
+    for e in np.unique(sub):
+        Wgu = decode_rows(packed_gu[e], lut_gu, L)            # [2I, H]
+        Wd = decode_rows(packed_down[e], lut_down, L)         # [H, I]
+        ti, ji = np.nonzero(sub == e)
+        gu = x[tokens[ti]] @ Wgu.T                            # [m, 2I]
+        h = silu(gu[:, :I]) * gu[:, I:]
+        out = h @ Wd.T                                        # [m, H]
+        for m in range(len(ti)):
+            Y[ti[m]] += w[tokens[ti[m]], ji[m]] * out[m]
+    return Y

@@ -406,7 +406,40 @@ def pin_router_topk():
     assert ids[1].tolist() == [0, 1, 2] and np.allclose(w[1], 1 / 3)
 
 
+def pin_mlp_bruteforce():
+    """The MLP oracle against pure-Python loops (bit-sliced weights, math.exp
+    silu, fsum) on a tiny problem, and its token subset against the full."""
+    rng = np.random.Generator(np.random.PCG64(66))
+    E, k, n, H, I, L = 3, 2, 3, 16, 8, 8
+    ids = np.array([[0, 2], [1, 0], [2, 1]], np.int32)
+    w = rng.random((n, k)).astype(np.float32)
+    x = moe_inputs.fp32_to_bf16_bits(rng.standard_normal((n, H)).astype(np.float32))
+    pgu = rng.integers(0, 256, (E, 2 * I, H // 4), dtype=np.uint8)
+    pd = rng.integers(0, 256, (E, H, I // 4), dtype=np.uint8)
+    lgu = (rng.standard_normal(1 << L) / 4).astype(np.float16).view(np.uint16)
+    ld = (rng.standard_normal(1 << L) / 3).astype(np.float16).view(np.uint16)
+    got = T.moe_mlp(x, ids, w, pgu, lgu, pd, ld, L)
+    xs = [[_bf16(b) for b in row] for row in x]
+    for t in range(n):
+        for r in range(H):
+            terms = []
+            for j in range(k):
+                e = int(ids[t, j])
+                h = []
+                for i in range(I):
+                    g = math.fsum(_fp16(lgu[s]) * xv for s, xv in zip(_bitfield_states(pgu[e, i].tobytes(), L), xs[t]))
+                    u = math.fsum(_fp16(lgu[s]) * xv for s, xv in zip(_bitfield_states(pgu[e, I + i].tobytes(), L), xs[t]))
+                    h.append(g / (1.0 + math.exp(-g)) * u)
+                d = math.fsum(_fp16(ld[s]) * hv for s, hv in zip(_bitfield_states(pd[e, r].tobytes(), L), h))
+                terms.append(float(np.float32(w[t, j])) * d)
+            want = math.fsum(terms)
+            assert abs(got[t, r] - want) <= 1e-9 * max(1.0, abs(want)), (t, r, got[t, r], want)
+    sub = T.moe_mlp(x, ids, w, pgu, lgu, pd, ld, L, tokens=[2, 0])
+    assert np.allclose(sub, got[[2, 0]], rtol=1e-12, atol=1e-12)
+
+
 ALL_PINS = [pin_fill_table, pin_gate_points, pin_gate_closed_forms, pin_min_tokens_flip,
             pin_capacity_bound, pin_decode_bitfield, pin_run_decode_identity,
             pin_special_luts, pin_bruteforce_tiny, pin_constant_lut, pin_onehot_x,
-            pin_route_bruteforce, pin_tile_map, pin_bf16_rne, pin_router_topk]
+            pin_route_bruteforce, pin_tile_map, pin_bf16_rne, pin_router_topk,
+            pin_mlp_bruteforce]

@@ -1,0 +1,89 @@
+"""The whole SwiGLU expert MLP (gate|up grouped GEMM per pair, SwiGLU, down
+grouped GEMM combined per token) against the oracle, and its two new pieces
+on their own: the per-pair grouped GEMM and the SwiGLU kernel.  Tolerance
+max|y - ref| / max|ref| <= 1e-2 (bf16 weights and bf16 h on the GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs
+import oracle.trellis_moe as O
+import trellis_quantized_moe_sort_gb300 as tq
+from gpu_util import to_device, normwise, check_no_device_error
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from trellis_quantized_moe_sort_gb300 import build
+    build.build()
+    tq.tq_init(0)
+
+
+def _mlp_dev(prob):
+    import warnings
+    with warnings.catch_warnings():
+        warnings.simplefilter("ignore")
+        c = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        return dict(x=c(prob.x_bits.view(np.int16)), ids=c(prob.topk_ids), w=c(prob.topk_w),
+                    pgu=c(prob.packed_gu), lgu=c(prob.lut_gu.view(np.int16)),
+                    pd=c(prob.packed_down), ld=c(prob.lut_down.view(np.int16)))
+
+
+@pytest.mark.parametrize("tile_m", [16, 64])
+def test_mlp_tiny_all_outputs(tile_m):
+    prob = moe_inputs.make_mlp_problem("tiny_mlp_e8_k2_n16")
+    d = _mlp_dev(prob)
+    y = tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"], tile_m=tile_m)
+    check_no_device_error()
+    ref = O.moe_mlp(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed_gu, prob.lut_gu, prob.packed_down,
+                    prob.lut_down, prob.L)
+    assert normwise(y.float().cpu().numpy(), ref) <= TOL
+
+
+def test_mlp_v4_n32_sampled_tokens():
+    prob = moe_inputs.make_mlp_problem("v4_mlp_n32")
+    d = _mlp_dev(prob)
+    y = tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"], tile_m=16)
+    check_no_device_error()
+    tokens = [0, 17, 31]
+    ref = O.moe_mlp(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed_gu, prob.lut_gu, prob.packed_down,
+                    prob.lut_down, prob.L, tokens=tokens)
+    assert normwise(y[tokens].float().cpu().numpy(), ref) <= TOL
+
+
+def test_grouped_gemm_pairs_all_outputs():
+    prob = moe_inputs.make_custom(8, 2, 24, 256, 256, 12, seed=91)
+    d = to_device(prob)
+    s = prob.shape
+    _, offsets, sp = tq.tq_route(d["ids"], s.E)
+    cap = tq.tq_tile_map_capacity(s.n, s.top_k, s.E, 16)
+    tiles, nt = tq.tq_build_tile_map(offsets, 16, cap)
+    xs = tq.tq_gather_rows(d["x"], sp, s.top_k)
+    out = torch.zeros((s.pairs, s.N), dtype=torch.float32, device="cuda")
+    p = lambda t: __import__("ctypes").c_void_p(t.data_ptr())
+    rc = tq.lib().tq_grouped_gemm_pairs(p(xs), p(d["packed"]), p(d["lut"]), s.L, p(sp), p(tiles), p(nt), cap,
+                                        s.n, s.top_k, s.E, s.K, s.N, 16, p(out),
+                                        __import__("ctypes").c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    check_no_device_error()
+    x = O.bf16_bits_to_f64(prob.x_bits)
+    spn = sp.cpu().numpy()
+    ref = np.zeros((s.pairs, s.N))
+    for slot, pair in enumerate(spn):
+        t, e = pair // s.top_k, int(prob.topk_ids.reshape(-1)[pair])
+        ref[slot] = O.decode_rows(prob.packed[e], prob.lut_bits, s.L) @ x[t]
+    assert normwise(out.cpu().numpy(), ref) <= TOL
+
+
+def test_swiglu_kernel():
+    rng = np.random.Generator(np.random.PCG64(3))
+    gu = (rng.standard_normal((37, 2 * 96)) * 3).astype(np.float32)
+    h = tq.tq_swiglu(torch.from_numpy(gu).cuda())
+    check_no_device_error()
+    g, u = gu[:, :96].astype(np.float64), gu[:, 96:].astype(np.float64)
+    ref = O.silu(g) * u
+    got = h.float().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30)

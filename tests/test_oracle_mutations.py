@@ -129,7 +129,24 @@ def _topk_softmax_all(logits, top_k):
     return ids, np.take_along_axis(full, ids.astype(np.int64), axis=1)
 
 
+def _mlp_sigmoid_only(*a, **kw):
+    saved = T.silu
+    T.silu = lambda v: 1.0 / (1.0 + np.exp(-v))
+    try:
+        return orig["moe_mlp"](*a, **kw)
+    finally:
+        T.silu = saved
+
+
+def _mlp_swapped_halves(x_bits, topk_ids, topk_w, packed_gu, lut_gu, packed_down, lut_down, L, tokens=None):
+    I = packed_gu.shape[1] // 2
+    swapped = np.concatenate([packed_gu[:, I:], packed_gu[:, :I]], axis=1)
+    return orig["moe_mlp"](x_bits, topk_ids, topk_w, swapped, lut_gu, packed_down, lut_down, L, tokens)
+
+
 MUTATIONS = {
+    "mlp_sigmoid_for_silu": ("moe_mlp", _mlp_sigmoid_only),
+    "mlp_gate_up_swapped": ("moe_mlp", _mlp_swapped_halves),
     "topk_ties_high": ("router_topk", _topk_ties_high),
     "topk_softmax_over_all": ("router_topk", _topk_softmax_all),
     "symbol_off_by_one": ("symbols", _symbols_off_by_one),

@@ -20,7 +20,8 @@ __all__ = [
     "tq_tiles_amortize", "tq_grouped_min_tokens", "tq_tile_map_capacity", "tq_select_arm",
     "tq_route", "tq_router_topk", "tq_route_logits", "tq_build_tile_map", "tq_gather_rows", "tq_grouped_gemm", "tq_gemv", "tq_combine",
     "tq_moe_workspace_size", "tq_moe_forward", "tq_moe_forward_static", "tq_device_error", "tq_launch_counts",
-    "tq_status_string", "tq_probe_lut_rate", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "EXPORTED_SYMBOLS",
+    "tq_status_string", "tq_probe_lut_rate", "tq_grouped_gemm_pairs", "tq_swiglu",
+    "tq_moe_mlp_workspace_size", "tq_moe_mlp_forward", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "EXPORTED_SYMBOLS",
 ]
 
 ARM_AUTO, ARM_GEMV, ARM_GROUPED = 0, 1, 2
@@ -56,6 +57,12 @@ _SIGS = {
     "tq_moe_forward_static": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int,
                                        _c_int, _c_int, _c_int, _c_int, _c_p, ctypes.POINTER(_c_int), _c_p]),
     "tq_probe_lut_rate": (_c_int, [_c_p, _c_int, _c_int, _c_p, _c_p, _c_p]),
+    "tq_grouped_gemm_pairs": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_int, _c_int,
+                                       _c_int, _c_int, _c_int, _c_p, _c_p]),
+    "tq_swiglu": (_c_int, [_c_p, _c_i64, _c_int, _c_p, _c_p]),
+    "tq_moe_mlp_workspace_size": (_c_sz, [_c_i64, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "tq_moe_mlp_forward": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int, _c_int,
+                                    _c_int, _c_int, _c_p, _c_sz, _c_p, _c_p]),
     "tq_device_error": (_c_int, [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
     "tq_launch_counts": (None, [ctypes.POINTER(_c_i64)]),
 }
@@ -362,6 +369,47 @@ def tq_probe_lut_rate(warps_per_sm: int = 8, iters: int = 512, stream=None) -> f
     torch.cuda.synchronize()
     c = float(cycles.double().mean())
     return warps_per_sm * 32 * iters * 16 / c
+
+
+def tq_moe_mlp_workspace_size(n: int, top_k: int, E: int, H: int, I: int, tile_m: int) -> int:
+    return int(lib().tq_moe_mlp_workspace_size(n, top_k, E, H, I, tile_m))
+
+
+def tq_moe_mlp_forward(x, packed_gu, lut_gu, packed_down, lut_down, topk_ids, topk_w, tile_m: int = 16,
+                       workspace=None, y=None, stream=None):
+    """Whole SwiGLU expert MLP -> y bf16 [n, H]."""
+    torch = _torch()
+    n, H = x.shape
+    E, I2, hb = packed_gu.shape
+    I = I2 // 2
+    if hb * 4 != H or tuple(packed_down.shape) != (E, H, I // 4):
+        raise ValueError("packed_gu must be [E, 2I, H/4] and packed_down [E, H, I/4]")
+    L = lut_gu.numel().bit_length() - 1
+    if lut_down.numel() != lut_gu.numel():
+        raise ValueError("both LUTs need 2^L entries")
+    top_k = topk_ids.shape[1]
+    need = tq_moe_mlp_workspace_size(n, top_k, E, H, I, tile_m)
+    workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device) if workspace is None else workspace
+    y = torch.empty((n, H), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _check(lib().tq_moe_mlp_forward(_dev_ptr(x, _bits16(), "x"), _dev_ptr(packed_gu, (torch.uint8,), "packed_gu"),
+                                    _dev_ptr(lut_gu, _bits16(), "lut_gu"),
+                                    _dev_ptr(packed_down, (torch.uint8,), "packed_down"),
+                                    _dev_ptr(lut_down, _bits16(), "lut_down"), L,
+                                    _dev_ptr(topk_ids, (torch.int32,), "topk_ids"),
+                                    _dev_ptr(topk_w, (torch.float32,), "topk_w"), n, top_k, E, H, I, tile_m,
+                                    _dev_ptr(workspace, (torch.uint8,), "workspace"), workspace.numel(),
+                                    _dev_ptr(y, _bits16(), "y"), _stream(stream)), "tq_moe_mlp_forward")
+    return y
+
+
+def tq_swiglu(gate_up, h=None, stream=None):
+    """h = bf16(silu(gate) * up) for gate_up fp32 [P, 2I]."""
+    torch = _torch()
+    P, I2 = gate_up.shape
+    h = torch.empty((P, I2 // 2), dtype=torch.bfloat16, device=gate_up.device) if h is None else h
+    _check(lib().tq_swiglu(_dev_ptr(gate_up, (torch.float32,), "gate_up"), P, I2 // 2, _dev_ptr(h, _bits16(), "h"),
+                           _stream(stream)), "tq_swiglu")
+    return h
 
 
 def tq_device_error() -> tuple[int, int]:

@@ -88,6 +88,7 @@ struct Params {
   int top_k, N, K;
   int row_blocks;
   int rb_group;     // row blocks per ordering group (row_blocks = plain tile-major order)
+  int pair_out;     // 0: y32[token] += w * D (combine); 1: y32[sorted slot] += D (per pair)
   int n_mma_max;    // largest MMA N (tile_m rounded up to 16)
   int pk_stages;    // packed super-stage buffers
   int act_stages;   // activation k-step buffers
@@ -476,12 +477,13 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
           if (qb & 2) x1 = t; else x3 = t;
           const int col = c0 + 4 * k + qb;
           if (col < rows) {
-            const int pair = p.sorted_pairs[slot0 + col];
+            const int pair = p.pair_out ? 0 : p.sorted_pairs[slot0 + col];
             if (pair < 0 || pair >= p.P) {
               record_error(p.err, TQ_ERR_INVALID_ARG, kWhereGroupedEpilogue);
             } else {
-              const float wt = p.topk_w[pair];
-              float* dst = yrow + static_cast<size_t>(pair / p.top_k) * p.N;
+              const float wt = p.pair_out ? 1.f : p.topk_w[pair];
+              const size_t out_row = p.pair_out ? static_cast<size_t>(slot0 + col) : static_cast<size_t>(pair / p.top_k);
+              float* dst = yrow + out_row * p.N;
               asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x0 * wt),
                            "f"(x1 * wt), "f"(x2 * wt), "f"(x3 * wt)
                            : "memory");
@@ -621,7 +623,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
                    const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                    const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
-                   int tile_m, float* y32, int* err, cudaStream_t s) {
+                   int tile_m, float* y32, int* err, cudaStream_t s, int pair_out) {
   auto encode = encode_fn();
   if (!encode) return TQ_ERR_CUDA;
   void* kfn = grouped_kernel_for(L);
@@ -646,8 +648,10 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
   p.row_blocks = N / kBlockRows;
   // Order by row-block groups only when the fp32 output is too large to stay
   // in L2 while six scattered partial sums per element arrive.
+  p.pair_out = pair_out;
   p.rb_group = p.row_blocks;
-  if (static_cast<long long>(n) * N * 4 > (24ll << 20)) {
+  const long long out_rows = pair_out ? n * static_cast<long long>(top_k) : n;
+  if (out_rows * N * 4 > (24ll << 20)) {
     for (int g = 8; g >= 1; g >>= 1) {
       if (p.row_blocks % g == 0) {
         p.rb_group = g;

@@ -37,7 +37,8 @@ int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top
 int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
                    const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                    const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
-                   int tile_m, float* y32, int* err, cudaStream_t s);
+                   int tile_m, float* y32, int* err, cudaStream_t s, int pair_out = 0);
+int launch_swiglu(const float* gate_up, int64_t P, int I, uint16_t* h, cudaStream_t s);
 int launch_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
                 const int32_t* topk_ids, const float* topk_w, int64_t n, int top_k, int E, int K,
                 int N, float* y32, int* err, cudaStream_t s);
