@@ -170,17 +170,12 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
   asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+__device__ __forceinline__ uint4 lds_u128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
   return v;
 }
-__device__ __forceinline__ uint64_t lds_u64(uint32_t addr) {
-  uint64_t v;
-  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
-  return v;
-}
-
 // The 32 bf16 weights of one run: window states of the 4 bytes before the run
 // (prev) and the run's 8 bytes (cur), looked up in the shared-memory LUT and
 // packed two per 32-bit word (even symbol in the low half).
@@ -527,26 +522,22 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
         }
         const uint32_t buf = pk0 + pk.stage * kPkStageBytes;
         const int nks = min(kSSSteps, ksteps - ss * kSSSteps);
-        // packed words of k-step i: run bytes [16i + 8h, +8) and the 4 bytes
-        // before them; loaded one k-step ahead so their latency overlaps
-        auto load_cur = [&](int i) { return lds_u64(buf + sw128(row, 16 * i + 8 * h)); };
-        auto load_prev = [&](int i) {
-          return h == 1 ? lds_u32(buf + sw128(row, 16 * i + 4))
-                        : (i == 0 ? carry : lds_u32(buf + sw128(row, 16 * i - 4)));
-        };
-        uint64_t cur_n = load_cur(0);
-        uint32_t prev_n = load_prev(0);
-        if (h == 0 && nks == kSSSteps) carry = lds_u32(buf + sw128(row, kSSBytes - 4));
+        // k-step i's 16 stream bytes per row (one conflict-free 16-byte load,
+        // one k-step ahead): half h decodes bytes [8h, 8h + 8); the 4 bytes
+        // before them are bytes 4..7 of the same chunk (h = 1) or bytes
+        // 12..15 of the previous chunk (h = 0; `carry` before a super-stage).
+        uint4 chunk_n = lds_u128(buf + sw128(row, 0));
+        uint32_t last = carry;
         for (int i = 0; i < nks && ok; ++i) {
-          const uint64_t cur = cur_n;
-          const uint32_t prev = prev_n;
+          const uint4 chunk = chunk_n;
+          const uint64_t cur = h ? (static_cast<uint64_t>(chunk.w) << 32 | chunk.z)
+                                 : (static_cast<uint64_t>(chunk.y) << 32 | chunk.x);
+          const uint32_t prev = h ? chunk.y : last;
+          last = chunk.w;
           // issue this k-step's LUT loads first, then the next k-step's packed words
           uint32_t w[16];
           lookup_run<L>(lut_s, prev, cur, w);
-          if (i + 1 < nks) {
-            cur_n = load_cur(i + 1);
-            prev_n = load_prev(i + 1);
-          }
+          if (i + 1 < nks) chunk_n = lds_u128(buf + sw128(row, 16 * (i + 1)));
           // while the loads are in flight: hand the previous k-step's weights to the MMA
           if (pending_afull >= 0) {
             tmem_wait_st();
@@ -564,6 +555,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
           pending_afull = apipe.stage;
           apipe.advance(kNumAStages);
         }
+        carry = last;   // bytes 124..127 of this super-stage, the next one's history
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_pkempty + 8 * pk.stage);
         pk.advance(SP);
