@@ -448,7 +448,11 @@ def run_sweep(args):
         arms = [("grouped", T) for T in tiles_list]
         if s.n <= 1024 and not args.sweep_no_gemv:
             arms.append(("gemv", None))
+        if args.sweep_dequant:
+            arms += [("dequant", T) for T in tiles_list]
+        w_dense = None
         for arm, T in arms:
+            extra = {}
             if arm == "grouped":
                 _, offsets, sp = tq.tq_route(d["ids"], s.E)
                 cap = tq.tq_tile_map_capacity(s.n, s.top_k, s.E, T)
@@ -460,6 +464,32 @@ def run_sweep(args):
                 us = timed(lambda: tq.tq_grouped_gemm(xs, d["packed"], d["lut"], sp, d["w"], tiles, nt,
                                                        s.top_k, T, y32))
                 staged = ntiles * s.N * s.K // 4
+            elif arm == "dequant":
+                # dequantize-materialize comparator: every woken expert decoded
+                # to dense bf16 (slot = expert id; other slots skipped), then the
+                # same grouped GEMM with A read from the dense copy
+                _, offsets, sp = tq.tq_route(d["ids"], s.E)
+                cap = tq.tq_tile_map_capacity(s.n, s.top_k, s.E, T)
+                tiles, nt = tq.tq_build_tile_map(offsets, T, cap)
+                xs = tq.tq_gather_rows(d["x"], sp, s.top_k)
+                woken_ids = np.unique(prob.topk_ids)
+                ids = np.full(s.E, -1, dtype=np.int32)
+                ids[woken_ids] = woken_ids
+                ids_d = _cuda(torch, ids)
+                if w_dense is None:
+                    w_dense = torch.empty((s.E, s.N, s.K), dtype=torch.bfloat16, device="cuda")
+                torch.cuda.synchronize()
+                ntiles = int(nt.item())
+                gather_us = timed(lambda: tq.tq_gather_rows(d["x"], sp, s.top_k, xs))
+                deq_us = timed(lambda: tq.tq_dequantize(d["packed"], d["lut"], expert_ids=ids_d, w_out=w_dense))
+                gemm_us = timed(lambda: tq.tq_grouped_gemm_dense(xs, w_dense, sp, d["w"], tiles, nt, s.top_k, T, y32))
+                us = deq_us + gemm_us
+                staged = ntiles * s.N * s.K // 4
+                mat = len(woken_ids) * s.N * s.K * 2
+                extra = {"dequant_us": round(deq_us, 1), "dense_gemm_us": round(gemm_us, 1),
+                         "materialized_GB": round(mat / 1e9, 3),
+                         "dequant_write_GBps": round(mat / (deq_us * 1e-6) / 1e9, 1),
+                         "dense_gemm_weight_GBps": round(ntiles * s.N * s.K * 2 / (gemm_us * 1e-6) / 1e9, 1)}
             else:
                 us = timed(lambda: tq.tq_gemv(d["x"], d["packed"], d["lut"], d["ids"], d["w"], y32))
                 ntiles = None
@@ -475,7 +505,9 @@ def run_sweep(args):
             t_hbm = alg / (hbm * 1e9) * 1e6
             t_tc = flops / (bf16_sus * 1e12) * 1e6
             lookups = (ntiles if ntiles is not None else s.pairs) * s.N * s.K
-            print(json.dumps({
+            if arm == "dequant":
+                lookups = woken * s.N * s.K
+            print(json.dumps({**extra, 
                 "workload": name, "arm": arm, "tile_m": T, "n": s.n, "pairs": s.pairs, "woken": woken,
                 "m_tiles": ntiles, "us": round(us, 1), "gather_us": gather_us, "pairs_per_s": round(s.pairs / (us * 1e-6), 1),
                 "staged_packed_GBps": round(staged / (us * 1e-6) / 1e9, 1),
@@ -483,7 +515,7 @@ def run_sweep(args):
                 "frac": round(max(t_hbm, t_tc) / us, 4),
                 "decode_lookups_per_clk_per_sm": round(lookups / (us * 1e-6) / 152 / 2.07e9, 2),
                 "peak_source": peak_src}), flush=True)
-        del d, y32
+        del d, y32, w_dense
         torch.cuda.empty_cache()
 
 
@@ -633,6 +665,8 @@ def main(argv=None):
     ap.add_argument("--sweep-workloads", default="", help="comma-separated subset for --sweep")
     ap.add_argument("--sweep-tiles", default="16,128", help="TILE_M values for --sweep")
     ap.add_argument("--sweep-no-gemv", action="store_true", help="skip the GEMV arm in --sweep")
+    ap.add_argument("--sweep-dequant", action="store_true",
+                    help="add the dequantize-materialize comparator (dense bf16 experts + the same grouped GEMM) to --sweep")
     ap.add_argument("--gate-study", action="store_true", help="both arms across token counts (V4 up shape)")
     ap.add_argument("--mlp-sweep", action="store_true", help="whole SwiGLU expert MLP per workload")
     ap.add_argument("--gate-ns", default="1,2,4,8,9,16,32,64,128,256,512,682,683,1024")

@@ -317,6 +317,44 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
                        void* workspace, size_t workspace_bytes, uint16_t* y, tq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Dequantize-materialize comparator  ([P1] "Tests": the dequantize path that
+ * dispatch falls through to outside the fused arms' ranges; [P2] "The two
+ * changes": the fused design never materialises full-size weights).  These
+ * calls build that path so it can be measured against the fused arms; the
+ * selection of tq_select_arm never picks it.
+ *
+ * tq_dequantize: w_out[i] = bf16(W_{expert_ids[i]}) for i < m, each a dense
+ *   row-major [N][K] matrix: the trellis decode of the bitstreams above and
+ *   fp16 -> bf16 nearest-even, bit-identical to the values the fused kernels
+ *   feed their MMAs.  expert_ids (device) int32 [m], or NULL for experts
+ *   0..m-1 (then m <= E); an id < 0 leaves its slot untouched; an id >= E
+ *   leaves it untouched and sets TQ_ERR_INVALID_ARG in the device error word.
+ *   packed, lut, w_out (device) 16-byte aligned; K % 8 == 0; L even in
+ *   [2, 16].  w_out holds m*N*K bf16 values (16 MiB per expert at
+ *   4096 x 2048).
+ * tq_grouped_gemm_dense: tq_grouped_gemm with dense bf16 weights
+ *   w_dense (device) [E][N][K] (16-byte aligned) in place of packed + lut;
+ *   same m-tiles, MMA and epilogue (y32 += w * W_e x).
+ * tq_moe_forward_dequant: zero y32, route, tile map, gather, dequantize every
+ *   expert with at least one pair into slot e of an [E][N][K] bf16 buffer in
+ *   the workspace, tq_grouped_gemm_dense, combine to bf16 y [n][N].
+ *   workspace (device) >= tq_moe_dequant_workspace_size(...) bytes (the
+ *   tq_moe_workspace_size regions followed by E*N*K*2 bytes), 256-byte
+ *   aligned.  Requires K % 64 == 0, N % 128 == 0, E <= 1024.
+ * ------------------------------------------------------------------------- */
+int tq_dequantize(const uint8_t* packed, const uint16_t* lut, int L, const int32_t* expert_ids, int m,
+                  int E, int N, int K, uint16_t* w_out, tq_stream_t stream);
+int tq_grouped_gemm_dense(const uint16_t* x_sorted, const uint16_t* w_dense, const int32_t* sorted_pairs,
+                          const float* topk_w, const int32_t* tiles, const int32_t* num_tiles, int64_t cap,
+                          int64_t n, int top_k, int E, int K, int N, int tile_m, float* y32,
+                          tq_stream_t stream);
+size_t tq_moe_dequant_workspace_size(int64_t n, int top_k, int E, int K, int N, int tile_m);
+int tq_moe_forward_dequant(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
+                           const int32_t* topk_ids, const float* topk_w,
+                           int64_t n, int top_k, int E, int K, int N, int tile_m,
+                           void* workspace, size_t workspace_bytes, uint16_t* y, tq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Diagnostics
  * ------------------------------------------------------------------------- */
 
@@ -336,10 +374,10 @@ int tq_probe_lut_rate(const uint16_t* table, int warps_per_sm, int iters, uint32
                       unsigned long long* cycles, tq_stream_t stream);
 
 /* Host-side counts of successful launches since process start, per kernel:
- * out[0] route, out[1] tile map, out[2] grouped GEMM, out[3] GEMV,
- * out[4] combine, out[5] activation gather, out[6] router top-k ([P3]:
- * counters prove which arm ran). */
-void tq_launch_counts(int64_t out[7]);
+ * out[0] route, out[1] tile map, out[2] grouped GEMM (trellis or dense),
+ * out[3] GEMV, out[4] combine, out[5] activation gather, out[6] router
+ * top-k, out[7] dequantize ([P3]: counters prove which arm ran). */
+void tq_launch_counts(int64_t out[8]);
 
 #ifdef __cplusplus
 }

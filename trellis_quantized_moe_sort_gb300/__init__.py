@@ -21,7 +21,8 @@ __all__ = [
     "tq_route", "tq_router_topk", "tq_route_logits", "tq_build_tile_map", "tq_gather_rows", "tq_grouped_gemm", "tq_gemv", "tq_combine",
     "tq_moe_workspace_size", "tq_moe_forward", "tq_moe_forward_static", "tq_device_error", "tq_launch_counts",
     "tq_status_string", "tq_probe_lut_rate", "tq_grouped_gemm_pairs", "tq_swiglu",
-    "tq_moe_mlp_workspace_size", "tq_moe_mlp_forward", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "EXPORTED_SYMBOLS",
+    "tq_moe_mlp_workspace_size", "tq_moe_mlp_forward", "tq_dequantize", "tq_grouped_gemm_dense",
+    "tq_moe_dequant_workspace_size", "tq_moe_forward_dequant", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "EXPORTED_SYMBOLS",
 ]
 
 ARM_AUTO, ARM_GEMV, ARM_GROUPED = 0, 1, 2
@@ -63,6 +64,12 @@ _SIGS = {
     "tq_moe_mlp_workspace_size": (_c_sz, [_c_i64, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "tq_moe_mlp_forward": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int, _c_int,
                                     _c_int, _c_int, _c_p, _c_sz, _c_p, _c_p]),
+    "tq_dequantize": (_c_int, [_c_p, _c_p, _c_int, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p]),
+    "tq_grouped_gemm_dense": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_int, _c_int, _c_int,
+                                       _c_int, _c_int, _c_p, _c_p]),
+    "tq_moe_dequant_workspace_size": (_c_sz, [_c_i64, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "tq_moe_forward_dequant": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int, _c_int,
+                                        _c_int, _c_int, _c_p, _c_sz, _c_p, _c_p]),
     "tq_device_error": (_c_int, [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
     "tq_launch_counts": (None, [ctypes.POINTER(_c_i64)]),
 }
@@ -412,6 +419,66 @@ def tq_swiglu(gate_up, h=None, stream=None):
     return h
 
 
+def tq_dequantize(packed, lut, expert_ids=None, w_out=None, stream=None):
+    """Materialized bf16 weights [m, N, K] of the listed experts (all E when
+    expert_ids is None) -- the dequantize-materialize comparator's first step."""
+    torch = _torch()
+    E, N, kb = packed.shape
+    K = kb * 4
+    L = lut.numel().bit_length() - 1
+    if lut.numel() != (1 << L):
+        raise ValueError("lut must have 2^L entries")
+    m = E if expert_ids is None else expert_ids.numel()
+    w_out = torch.empty((m, N, K), dtype=torch.bfloat16, device=packed.device) if w_out is None else w_out
+    ids = None if expert_ids is None else _dev_ptr(expert_ids, (torch.int32,), "expert_ids")
+    _check(lib().tq_dequantize(_dev_ptr(packed, (torch.uint8,), "packed"), _dev_ptr(lut, _bits16(), "lut"), L, ids,
+                               m, E, N, K, _dev_ptr(w_out, _bits16(), "w_out"), _stream(stream)), "tq_dequantize")
+    return w_out
+
+
+def tq_grouped_gemm_dense(x_sorted, w_dense, sorted_pairs, topk_w, tiles, num_tiles, top_k: int, tile_m: int,
+                          y32, stream=None) -> None:
+    """y32 += grouped product with dense bf16 weights w_dense [E, N, K]."""
+    torch = _torch()
+    P, K = x_sorted.shape
+    E, N, K2 = w_dense.shape
+    if K2 != K:
+        raise ValueError(f"w_dense has K = {K2}, x_sorted has {K}")
+    if P % top_k:
+        raise ValueError("x_sorted must have n*top_k rows")
+    _check(lib().tq_grouped_gemm_dense(_dev_ptr(x_sorted, _bits16(), "x_sorted"), _dev_ptr(w_dense, _bits16(), "w_dense"),
+                                       _dev_ptr(sorted_pairs, (torch.int32,), "sorted_pairs"),
+                                       _dev_ptr(topk_w, (torch.float32,), "topk_w"),
+                                       _dev_ptr(tiles, (torch.int32,), "tiles"),
+                                       _dev_ptr(num_tiles, (torch.int32,), "num_tiles"), tiles.shape[0], P // top_k,
+                                       top_k, E, K, N, tile_m, _dev_ptr(y32, (torch.float32,), "y32"),
+                                       _stream(stream)), "tq_grouped_gemm_dense")
+
+
+def tq_moe_dequant_workspace_size(n: int, top_k: int, E: int, K: int, N: int, tile_m: int) -> int:
+    return int(lib().tq_moe_dequant_workspace_size(n, top_k, E, K, N, tile_m))
+
+
+def tq_moe_forward_dequant(x, packed, lut, topk_ids, topk_w, tile_m: int = 16, workspace=None, y=None,
+                           stream=None):
+    """Dequantize-materialize comparator: the routed-expert product through
+    dense bf16 copies of the woken experts -> y bf16 [n, N]."""
+    torch = _torch()
+    n, K, E, N, L = _shapes(x, packed, lut)
+    top_k = topk_ids.shape[1]
+    need = tq_moe_dequant_workspace_size(n, top_k, E, K, N, tile_m)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    y = torch.empty((n, N), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _check(lib().tq_moe_forward_dequant(_dev_ptr(x, _bits16(), "x"), _dev_ptr(packed, (torch.uint8,), "packed"),
+                                        _dev_ptr(lut, _bits16(), "lut"), L,
+                                        _dev_ptr(topk_ids, (torch.int32,), "topk_ids"),
+                                        _dev_ptr(topk_w, (torch.float32,), "topk_w"), n, top_k, E, K, N, tile_m,
+                                        _dev_ptr(workspace, (torch.uint8,), "workspace"), workspace.numel(),
+                                        _dev_ptr(y, _bits16(), "y"), _stream(stream)), "tq_moe_forward_dequant")
+    return y
+
+
 def tq_device_error() -> tuple[int, int]:
     """(code, where) of the first device-side error since the last call; clears it."""
     code, where = ctypes.c_int(0), ctypes.c_int(0)
@@ -420,6 +487,6 @@ def tq_device_error() -> tuple[int, int]:
 
 
 def tq_launch_counts() -> dict:
-    arr = (ctypes.c_int64 * 7)()
+    arr = (ctypes.c_int64 * 8)()
     lib().tq_launch_counts(arr)
-    return dict(zip(("route", "tile_map", "grouped", "gemv", "combine", "gather", "router"), list(arr)))
+    return dict(zip(("route", "tile_map", "grouped", "gemv", "combine", "gather", "router", "dequant"), list(arr)))

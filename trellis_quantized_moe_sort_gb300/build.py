@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtqmoe.so")
-SOURCES = ["tq_host.cu", "tq_route.cu", "tq_grouped.cu", "tq_gemv.cu", "tq_noalloc.cu", "tq_probe.cu", "tq_mlp.cu"]
+SOURCES = ["tq_host.cu", "tq_route.cu", "tq_grouped.cu", "tq_gemv.cu", "tq_noalloc.cu", "tq_probe.cu", "tq_mlp.cu", "tq_dequant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

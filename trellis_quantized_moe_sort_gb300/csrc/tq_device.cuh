@@ -12,7 +12,7 @@ namespace tq {
 // Location tags stored next to an error code in the device error word.
 enum ErrWhere : int {
   kWhereRoute = 1, kWhereTileMap = 2, kWhereGroupedProducer = 3, kWhereGroupedDecode = 4,
-  kWhereGroupedMma = 5, kWhereGroupedEpilogue = 6, kWhereGroupedTeardown = 7,
+  kWhereGroupedMma = 5, kWhereGroupedEpilogue = 6, kWhereGroupedTeardown = 7, kWhereDequant = 8,
 };
 
 // A wait gives up after this long (ns of %globaltimer) and reports
@@ -115,6 +115,16 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Same product with A also in shared memory (K-major, 128-byte swizzle).
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Arrive once on `bar` when every MMA issued so far by this thread has completed.

@@ -217,7 +217,11 @@ __device__ __forceinline__ void drain_ring(uint32_t bar0, Pipe pipe, int nstages
   }
 }
 
-template <int L>
+// kDense: the comparator mode.  A comes from materialized bf16 weights
+// [E][N][K] through TMA (one 128 x 64 box per k-step into the same ring the
+// packed bytes use) and the MMA reads it from shared memory; the decode warps
+// and the LUT stay idle.
+template <int L, bool kDense>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_constant__ CUtensorMap tm_xs,
                const Params p) {
@@ -249,7 +253,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   if (threadIdx.x == 0) {
     for (int s = 0; s < SP; ++s) {
       mbar_init(bar_pkfull + 8 * s, 1);
-      mbar_init(bar_pkempty + 8 * s, kNumDecodeWarps);
+      mbar_init(bar_pkempty + 8 * s, kDense ? 1 : kNumDecodeWarps);
     }
     for (int s = 0; s < SA; ++s) {
       mbar_init(bar_actfull + 8 * s, 1);
@@ -270,7 +274,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   if (warp == kWarpProducer) tmem_alloc(smem_u32(tmem_holder), static_cast<uint32_t>(p.tmem_cols));
 
   // LUT: fp16 (global) -> bf16 (shared), nearest-even.
-  {
+  if constexpr (!kDense) {
     constexpr int kEntries = 1 << L;
     uint16_t* lut_dst = reinterpret_cast<uint16_t*>(gbase + p.off_lut);
     if constexpr (kEntries >= 8) {
@@ -326,7 +330,11 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
         continue;
       }
       const int row_g = tl.e * p.N + sg.rb * kBlockRows;
-      for (int ss = sg.ss0; ss < sg.ss1; ++ss) {
+      // One ring slot per super-stage of packed bytes, or per k-step of dense
+      // bf16 weights (128 rows x 64 values = the same 16 KiB).
+      const int i0 = kDense ? sg.ss0 * kSSSteps : sg.ss0;
+      const int i1 = kDense ? min(ksteps, sg.ss1 * kSSSteps) : sg.ss1;
+      for (int i = i0; i < i1; ++i) {
         if (!mbar_wait(bar_pkempty + 8 * pk.stage, pk.phase ^ 1u, abort_flag, p.err, kWhereGroupedProducer)) {
           ok = false;
           break;
@@ -334,7 +342,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
         if (lane == 0) {
           const uint32_t full = bar_pkfull + 8 * pk.stage;
           mbar_arrive_expect_tx(full, kPkStageBytes);
-          tma_load_2d(pk0 + pk.stage * kPkStageBytes, &tm_packed, ss * kSSBytes, row_g, full);
+          tma_load_2d(pk0 + pk.stage * kPkStageBytes, &tm_packed, kDense ? i * kKStep : i * kSSBytes, row_g, full);
         }
         ++pk_issued;
         pk.advance(SP);
@@ -380,6 +388,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     Pipe act, apipe, accp;
+    Pipe& wpipe = apipe;   // kDense: the A ring is the packed-byte ring
     bool ok = true;
     for (long long g = g_beg; g < g_end && ok;) {
       const Segment sg = segment_at(g, g_end, n_ss, num_tiles, rb_group);
@@ -396,26 +405,38 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(accp.stage * p.n_mma_max);
       const int ks0 = sg.ss0 * kSSSteps, ks1 = min(ksteps, sg.ss1 * kSSSteps);
       for (int ks = ks0; ks < ks1; ++ks) {
+        const uint32_t bar_wfull = kDense ? bar_pkfull : bar_afull;
         if (!mbar_wait(bar_actfull + 8 * act.stage, act.phase, abort_flag, p.err, kWhereGroupedMma) ||
-            !mbar_wait(bar_afull + 8 * apipe.stage, apipe.phase, abort_flag, p.err, kWhereGroupedMma)) {
+            !mbar_wait(bar_wfull + 8 * wpipe.stage, wpipe.phase, abort_flag, p.err, kWhereGroupedMma)) {
           ok = false;
           break;
         }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t a_tmem = tmem_base + acol0 + static_cast<uint32_t>(apipe.stage * kATmemCols);
           const uint32_t b_smem = act0 + static_cast<uint32_t>(act.stage * p.n_mma_max * kActRowBytes);
+          if constexpr (kDense) {
+            const uint32_t a_smem = pk0 + wpipe.stage * kPkStageBytes;
 #pragma unroll
-          for (int kk = 0; kk < kKStep / 16; ++kk) {
-            mma_bf16_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b_smem + kk * 32), idesc,
-                        (ks != ks0 || kk != 0) ? 1u : 0u);
+            for (int kk = 0; kk < kKStep / 16; ++kk) {
+              mma_bf16_ss(d_tmem, smem_desc_sw128(a_smem + kk * 32), smem_desc_sw128(b_smem + kk * 32), idesc,
+                          (ks != ks0 || kk != 0) ? 1u : 0u);
+            }
+            mma_commit(bar_actempty + 8 * act.stage);
+            mma_commit(bar_pkempty + 8 * wpipe.stage);
+          } else {
+            const uint32_t a_tmem = tmem_base + acol0 + static_cast<uint32_t>(apipe.stage * kATmemCols);
+#pragma unroll
+            for (int kk = 0; kk < kKStep / 16; ++kk) {
+              mma_bf16_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b_smem + kk * 32), idesc,
+                          (ks != ks0 || kk != 0) ? 1u : 0u);
+            }
+            mma_commit(bar_actempty + 8 * act.stage);
+            mma_commit(bar_aempty + 8 * apipe.stage);
           }
-          mma_commit(bar_actempty + 8 * act.stage);
-          mma_commit(bar_aempty + 8 * apipe.stage);
         }
         __syncwarp();
         act.advance(SA);
-        apipe.advance(kNumAStages);
+        wpipe.advance(kDense ? SP : kNumAStages);
       }
       if (!ok) break;
       if (lane == 0) mma_commit(bar_accfull + 8 * accp.stage);
@@ -491,7 +512,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
       if (lane == 0) mbar_arrive(bar_accempty + 8 * accp.stage);
       accp.advance(p.nacc);
     }
-  } else {
+  } else if constexpr (!kDense) {
     // ------------------------------------------------------------ decode
     const int dw = warp - kWarpDec0;
     const int q = warp & 3;
@@ -579,7 +600,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
 
 template <int L>
 void* kernel_ptr() {
-  return reinterpret_cast<void*>(&grouped_kernel<L>);
+  return reinterpret_cast<void*>(&grouped_kernel<L, false>);
 }
 
 void* grouped_kernel_for(int L) {
@@ -615,10 +636,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
                    const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                    const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
-                   int tile_m, float* y32, int* err, cudaStream_t s, int pair_out) {
+                   int tile_m, float* y32, int* err, cudaStream_t s, int pair_out, const uint16_t* dense_w) {
   auto encode = encode_fn();
   if (!encode) return TQ_ERR_CUDA;
-  void* kfn = grouped_kernel_for(L);
+  const bool dense = dense_w != nullptr;
+  void* kfn = dense ? reinterpret_cast<void*>(&grouped_kernel<2, true>) : grouped_kernel_for(L);
   if (!kfn) return TQ_ERR_INVALID_ARG;
 
   Params p{};
@@ -652,8 +674,9 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
     }
   }
   p.n_mma_max = (tile_m + 15) & ~15;
-  p.nacc = (2 * p.n_mma_max + kNumAStages * kATmemCols <= 512) ? 2 : 1;
-  const int cols_needed = p.nacc * p.n_mma_max + kNumAStages * kATmemCols;
+  const int a_cols = dense ? 0 : kNumAStages * kATmemCols;   // decoded A stages in tensor memory
+  p.nacc = (2 * p.n_mma_max + a_cols <= 512) ? 2 : 1;
+  const int cols_needed = p.nacc * p.n_mma_max + a_cols;
   int cols = 32;
   while (cols < cols_needed) cols <<= 1;
   p.tmem_cols = cols;
@@ -661,7 +684,7 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
   // Shared memory: activation stages, packed super-stages, LUT, barriers.
   // Prefer 3 packed buffers and up to 8 activation stages; shrink to fit.
   const uint32_t act_stage = static_cast<uint32_t>(p.n_mma_max * kActRowBytes);
-  const uint32_t lut_bytes = std::max<uint32_t>(16u, 2u << L);
+  const uint32_t lut_bytes = dense ? 16u : std::max<uint32_t>(16u, 2u << L);
   const uint32_t bar_bytes = 8 * kNumBars + 16;
   auto total_for = [&](int sp, int sa) {
     return 1024u + sa * act_stage + sp * kPkStageBytes + lut_bytes + bar_bytes;
@@ -687,7 +710,17 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
   const uint32_t smem = std::max<uint32_t>(total_for(SP, SA), 120u * 1024u);
 
   CUtensorMap tm_packed, tm_xs;
-  {
+  if (dense) {
+    // Materialized weights: bf16 [E*N][K], one 64 x 128 box per k-step.
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(E) * N};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {kKStep, kBlockRows};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tm_packed, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(dense_w), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return TQ_ERR_INVALID_ARG;
+  } else {
     // Box wider than a short row (K/4 < 128) reads zeros past the row end.
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 4), static_cast<cuuint64_t>(E) * N};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 4)};

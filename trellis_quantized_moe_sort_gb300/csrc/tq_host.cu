@@ -161,6 +161,22 @@ int sm_count() {
   return v;
 }
 
+// Every region is 256-byte aligned and sized as in tq_moe_workspace_size.
+MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K, int N, int64_t cap) {
+  const size_t P = static_cast<size_t>(n) * top_k;
+  MoeScratch m{};
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  m.counts = reinterpret_cast<int32_t*>(w);        w += align256(sizeof(int32_t) * E);
+  m.offsets = reinterpret_cast<int32_t*>(w);       w += align256(sizeof(int32_t) * (E + 1));
+  m.sorted_pairs = reinterpret_cast<int32_t*>(w);  w += align256(sizeof(int32_t) * std::max<size_t>(P, 1));
+  m.tiles = reinterpret_cast<int32_t*>(w);         w += align256(sizeof(int32_t) * 3 * std::max<int64_t>(cap, 1));
+  m.num_tiles = reinterpret_cast<int32_t*>(w);     w += align256(sizeof(int32_t));
+  m.y32 = reinterpret_cast<float*>(w);             w += align256(sizeof(float) * static_cast<size_t>(n) * N);
+  m.x_sorted = reinterpret_cast<uint16_t*>(w);     w += align256(sizeof(uint16_t) * P * K);
+  m.end = w;
+  return m;
+}
+
 }  // namespace tq
 
 using namespace tq;
@@ -415,14 +431,14 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
 
   const int64_t cap = tq_tile_map_capacity(n, top_k, E, tile_m);
   const size_t P = static_cast<size_t>(n) * top_k;
-  uint8_t* w = static_cast<uint8_t*>(workspace);
-  int32_t* counts = reinterpret_cast<int32_t*>(w);            w += align256(sizeof(int32_t) * E);
-  int32_t* offsets = reinterpret_cast<int32_t*>(w);           w += align256(sizeof(int32_t) * (E + 1));
-  int32_t* sorted_pairs = reinterpret_cast<int32_t*>(w);      w += align256(sizeof(int32_t) * P);
-  int32_t* tiles = reinterpret_cast<int32_t*>(w);             w += align256(sizeof(int32_t) * 3 * cap);
-  int32_t* num_tiles = reinterpret_cast<int32_t*>(w);         w += align256(sizeof(int32_t));
-  float* y32 = reinterpret_cast<float*>(w);                   w += align256(sizeof(float) * static_cast<size_t>(n) * N);
-  uint16_t* x_sorted = reinterpret_cast<uint16_t*>(w);
+  const MoeScratch ws = carve_moe_scratch(workspace, n, top_k, E, K, N, cap);
+  int32_t* counts = ws.counts;
+  int32_t* offsets = ws.offsets;
+  int32_t* sorted_pairs = ws.sorted_pairs;
+  int32_t* tiles = ws.tiles;
+  int32_t* num_tiles = ws.num_tiles;
+  float* y32 = ws.y32;
+  uint16_t* x_sorted = ws.x_sorted;
 
   if (cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(n) * N, s) != cudaSuccess) {
     cudaGetLastError();
@@ -473,7 +489,7 @@ int tq_device_error(int* code, int* where) {
   return TQ_OK;
 }
 
-void tq_launch_counts(int64_t out[7]) {
+void tq_launch_counts(int64_t out[8]) {
   if (!out) return;
   for (int i = 0; i < kCntNum; ++i) out[i] = g_counts[i].load();
 }

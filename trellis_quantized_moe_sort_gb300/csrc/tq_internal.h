@@ -18,7 +18,10 @@ int require_sm103(cudaStream_t stream);
 // Converts the last launch error into a status and clears it.
 int launch_status();
 
-enum Counter { kCntRoute = 0, kCntTileMap, kCntGrouped, kCntGemv, kCntCombine, kCntGather, kCntRouter, kCntNum };
+enum Counter {
+  kCntRoute = 0, kCntTileMap, kCntGrouped, kCntGemv, kCntCombine, kCntGather, kCntRouter, kCntDequant,
+  kCntNum
+};
 void count_launch(Counter c);
 
 // Number of SMs of the current device (cached per device).
@@ -37,7 +40,28 @@ int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top
 int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
                    const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                    const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
-                   int tile_m, float* y32, int* err, cudaStream_t s, int pair_out = 0);
+                   int tile_m, float* y32, int* err, cudaStream_t s, int pair_out = 0,
+                   const uint16_t* dense_w = nullptr);
+// Materializes weights: out[i] = bf16(W_{e_i}) [N][K] for slot i < m, e_i =
+// expert_ids[i] (or i when expert_ids is null); a slot whose expert has
+// counts[e_i] == 0 (when counts is given) or e_i < 0 is skipped.
+int launch_dequant(const uint8_t* packed, const uint16_t* lut, int L, const int32_t* expert_ids,
+                   const int32_t* counts, int m, int E, int N, int K, uint16_t* out, int* err, cudaStream_t s);
+
+// The scratch regions of tq_moe_forward inside a caller workspace (layout of
+// tq_moe_workspace_size: counts, offsets, sorted pairs, tiles, num_tiles, y32,
+// x_sorted, each 256-byte aligned); `end` is the first byte after them.
+struct MoeScratch {
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_pairs;
+  int32_t* tiles;
+  int32_t* num_tiles;
+  float* y32;
+  uint16_t* x_sorted;
+  uint8_t* end;
+};
+MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K, int N, int64_t cap);
 int launch_swiglu(const float* gate_up, int64_t P, int I, uint16_t* h, cudaStream_t s);
 int launch_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
                 const int32_t* topk_ids, const float* topk_w, int64_t n, int top_k, int E, int K,
