@@ -68,6 +68,7 @@ constexpr int kWarpDec0 = kWarpEpi0 + kNumEpiWarps;
 constexpr int kWarpActProducer = kWarpDec0 + kNumDecodeWarps;
 constexpr int kThreads = 32 * (kWarpActProducer + 1);  // 480
 constexpr int kMaxPkStages = 6;
+constexpr int kActPrefetch = 8;                       // k-steps of activations asked into L2 ahead
 constexpr int kMaxActStages = 8;
 constexpr int kSmemLimit = 232448;                   // 227 KiB opt-in per block
 constexpr int kNumBars = 2 * kMaxPkStages + 2 * kMaxActStages + 2 * kNumAStages + 2 + 2 + 1;
@@ -367,6 +368,11 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
       const int ks0 = sg.ss0 * kSSSteps, ks1 = min(ksteps, sg.ss1 * kSSSteps);
+      // Activations of a tile are read by several CTAs at different times and
+      // may have left L2: ask for them kActPrefetch k-steps before the copy
+      // into shared memory needs them.
+      if (lane == 0)
+        for (int j = ks0; j < min(ks1, ks0 + kActPrefetch); ++j) tma_prefetch_l2_2d(&tm_xs, j * kKStep, tl.slot0);
       for (int ks = ks0; ks < ks1; ++ks) {
         if (!mbar_wait(bar_actempty + 8 * act.stage, act.phase ^ 1u, abort_flag, p.err,
                        kWhereGroupedProducer)) {
@@ -378,6 +384,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
           mbar_arrive_expect_tx(full, act_tx);
           tma_load_2d(act0 + static_cast<uint32_t>(act.stage * p.n_mma_max * kActRowBytes), &tm_xs,
                       ks * kKStep, tl.slot0, full);
+          if (ks + kActPrefetch < ks1) tma_prefetch_l2_2d(&tm_xs, (ks + kActPrefetch) * kKStep, tl.slot0);
         }
         ++act_issued;
         act.advance(SA);
@@ -465,6 +472,32 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
       const int slot0 = tl.slot0, rows = tl.rows;
+      // Output row and weight of every column of the tile, loaded while the
+      // MMAs run: lane j holds columns j + 32i (i < 8; tile_m <= 256), and the
+      // drain below takes them by shuffle.  -1 = no output (past the tile, or
+      // a pair id out of range, which is reported).
+      int orow[8];
+      float owt[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int col = lane + 32 * i;
+        orow[i] = -1;
+        owt[i] = 0.f;
+        if (col < rows) {
+          if (p.pair_out) {
+            orow[i] = slot0 + col;
+            owt[i] = 1.f;
+          } else {
+            const int pair = __ldg(p.sorted_pairs + slot0 + col);
+            if (pair < 0 || pair >= p.P) {
+              record_error(p.err, TQ_ERR_INVALID_ARG, kWhereGroupedEpilogue);
+            } else {
+              orow[i] = pair / p.top_k;
+              owt[i] = __ldg(p.topk_w + pair);
+            }
+          }
+        }
+      }
       if (!mbar_wait(bar_accfull + 8 * accp.stage, accp.phase, abort_flag, p.err, kWhereGroupedEpilogue)) break;
       tc_fence_after();
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
@@ -474,32 +507,31 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
       // pair and adds them with one 16-byte vector reduction.
       const int qa = lane >> 2, qb = lane & 3;
       float* const yrow = p.y32 + static_cast<size_t>(sg.rb) * kBlockRows + 32 * q + 4 * qa;
-      for (int c0 = 0; c0 < rows; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(t_acc + c0, v);
-        tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (c0 + 4 * k >= rows) break;
-          float x0 = __uint_as_float(v[4 * k]), x1 = __uint_as_float(v[4 * k + 1]);
-          float x2 = __uint_as_float(v[4 * k + 2]), x3 = __uint_as_float(v[4 * k + 3]);
-          float t = __shfl_xor_sync(0xffffffffu, (qb & 1) ? x0 : x1, 1);
-          if (qb & 1) x0 = t; else x1 = t;
-          t = __shfl_xor_sync(0xffffffffu, (qb & 1) ? x2 : x3, 1);
-          if (qb & 1) x2 = t; else x3 = t;
-          t = __shfl_xor_sync(0xffffffffu, (qb & 2) ? x0 : x2, 2);
-          if (qb & 2) x0 = t; else x2 = t;
-          t = __shfl_xor_sync(0xffffffffu, (qb & 2) ? x1 : x3, 2);
-          if (qb & 2) x1 = t; else x3 = t;
-          const int col = c0 + 4 * k + qb;
-          if (col < rows) {
-            const int pair = p.pair_out ? 0 : p.sorted_pairs[slot0 + col];
-            if (pair < 0 || pair >= p.P) {
-              record_error(p.err, TQ_ERR_INVALID_ARG, kWhereGroupedEpilogue);
-            } else {
-              const float wt = p.pair_out ? 1.f : p.topk_w[pair];
-              const size_t out_row = p.pair_out ? static_cast<size_t>(slot0 + col) : static_cast<size_t>(pair / p.top_k);
-              float* dst = yrow + out_row * p.N;
+      for (int b = 0; b < 8; ++b) {
+        if (32 * b >= rows) break;
+        for (int c0 = 32 * b; c0 < min(rows, 32 * b + 32); c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(t_acc + c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (c0 + 4 * k >= rows) break;
+            float x0 = __uint_as_float(v[4 * k]), x1 = __uint_as_float(v[4 * k + 1]);
+            float x2 = __uint_as_float(v[4 * k + 2]), x3 = __uint_as_float(v[4 * k + 3]);
+            float t = __shfl_xor_sync(0xffffffffu, (qb & 1) ? x0 : x1, 1);
+            if (qb & 1) x0 = t; else x1 = t;
+            t = __shfl_xor_sync(0xffffffffu, (qb & 1) ? x2 : x3, 1);
+            if (qb & 1) x2 = t; else x3 = t;
+            t = __shfl_xor_sync(0xffffffffu, (qb & 2) ? x0 : x2, 2);
+            if (qb & 2) x0 = t; else x2 = t;
+            t = __shfl_xor_sync(0xffffffffu, (qb & 2) ? x1 : x3, 2);
+            if (qb & 2) x1 = t; else x3 = t;
+            const int src = (c0 & 31) + 4 * k + qb;   // lane holding this column's metadata
+            const int out_row = __shfl_sync(0xffffffffu, orow[b], src);
+            const float wt = __shfl_sync(0xffffffffu, owt[b], src);
+            if (out_row >= 0) {
+              float* dst = yrow + static_cast<size_t>(out_row) * p.N;
               asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x0 * wt),
                            "f"(x1 * wt), "f"(x2 * wt), "f"(x3 * wt)
                            : "memory");
