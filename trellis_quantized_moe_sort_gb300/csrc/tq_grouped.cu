@@ -510,10 +510,16 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
         if (32 * b >= rows) break;
-        for (int c0 = 32 * b; c0 < min(rows, 32 * b + 32); c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(t_acc + c0, v);
-          tmem_wait_ld();
+        // both 16-column halves of the block in flight before one wait
+        uint32_t v2[2][16];
+        tmem_ld16(t_acc + 32 * b, v2[0]);
+        if (32 * b + 16 < rows) tmem_ld16(t_acc + 32 * b + 16, v2[1]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int c0 = 32 * b + 16 * hf;
+          if (c0 >= rows) break;
+          const uint32_t (&v)[16] = v2[hf];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             if (c0 + 4 * k >= rows) break;
