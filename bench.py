@@ -614,7 +614,7 @@ def run_mlp_sweep(args):
         x, ids, w = c(prob.x_bits.view(np.int16)), c(prob.topk_ids), c(prob.topk_w)
         pgu, lgu = c(prob.packed_gu), c(prob.lut_gu.view(np.int16))
         pd, ld = c(prob.packed_down), c(prob.lut_down.view(np.int16))
-        T = args.tile_m if prob.n <= 1024 else 128
+        T = args.tile_m if prob.n <= 1024 else 256
         ws = torch.empty(tq.tq_moe_mlp_workspace_size(prob.n, prob.top_k, prob.E, prob.H, prob.I, T),
                          dtype=torch.uint8, device="cuda")
         y = torch.empty((prob.n, prob.H), dtype=torch.bfloat16, device="cuda")
