@@ -246,6 +246,10 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   const uint32_t bar_afull = bar_actempty + 8 * kMaxActStages;
   const uint32_t bar_aempty = bar_afull + 8 * kNumAStages;
   const uint32_t bar_accfull = bar_aempty + 8 * kNumAStages;
+  // When the activation ring and the A ring have the same depth they advance
+  // in lockstep (one stage of each per k-step): the MMA's one commit on the
+  // activation stage then also releases the A stage of the same index.
+  const uint32_t bar_arel = (SA == kNumAStages) ? bar_actempty : bar_aempty;
   const uint32_t bar_accempty = bar_accfull + 16;
   const uint32_t bar_drain = bar_accempty + 16;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + p.off_bar + 8 * kNumBars);
@@ -438,7 +442,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
                           (ks != ks0 || kk != 0) ? 1u : 0u);
             }
             mma_commit(bar_actempty + 8 * act.stage);
-            mma_commit(bar_aempty + 8 * apipe.stage);
+            if (SA != kNumAStages) mma_commit(bar_aempty + 8 * apipe.stage);
           }
         }
         __syncwarp();
@@ -605,7 +609,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
             if (lane == 0) mbar_arrive(bar_afull + 8 * pending_afull);
             pending_afull = -1;
           }
-          if (!mbar_wait(bar_aempty + 8 * apipe.stage, apipe.phase ^ 1u, abort_flag, p.err, kWhereGroupedDecode)) {
+          if (!mbar_wait(bar_arel + 8 * apipe.stage, apipe.phase ^ 1u, abort_flag, p.err, kWhereGroupedDecode)) {
             ok = false;
             break;
           }
