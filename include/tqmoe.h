@@ -116,9 +116,17 @@ int64_t tq_tile_map_capacity(int64_t n, int top_k, int E, int tile_m);
 
 /* Arm selection ([P1] post-merge note): TQ_ARM_GEMV when n <= 8 or the tiles
  * do not amortize, TQ_ARM_GROUPED otherwise; `pin` forces an arm.  Negative
- * on invalid arguments. */
-enum tq_arm { TQ_ARM_AUTO = 0, TQ_ARM_GEMV = 1, TQ_ARM_GROUPED = 2 };
+ * on invalid arguments.
+ * pin = TQ_ARM_MEASURED selects by the crossover measured on GB300 instead
+ * ([P3] "Two things that were built, correct, and switched off": the tile-fill
+ * gate does not reproduce): this library's grouped kernel decodes each woken
+ * expert once per m-tile whatever the tile's fill, so it wins as soon as
+ * experts are shared; the arms tie at 1.04 pairs per woken expert (V4 up
+ * shape, n = 4) and the grouped arm is chosen from there on, with no floor.
+ * tq_moe_forward reports TQ_ARM_GEMV or TQ_ARM_GROUPED as the arm used. */
+enum tq_arm { TQ_ARM_AUTO = 0, TQ_ARM_GEMV = 1, TQ_ARM_GROUPED = 2, TQ_ARM_MEASURED = 3 };
 #define TQ_DECODE_REGIME_MAX_TOKENS 8
+#define TQ_MEASURED_CROSSOVER_PPW 1.04
 int tq_select_arm(int64_t n, int top_k, int E, int tile_m, int pin);
 
 /* ---------------------------------------------------------------------------

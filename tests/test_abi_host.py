@@ -66,7 +66,7 @@ def test_gate_and_flip_bitexact(tq):
                     continue
                 assert tq.tq_tiles_amortize(n, k, E, T) == O.tiles_amortize(n, k, E, T)
                 assert tq.tq_tile_map_capacity(n, k, E, T) == O.tile_map_capacity(n, k, E, T)
-                for pin, name in ((0, "auto"), (1, "gemv"), (2, "grouped")):
+                for pin, name in ((0, "auto"), (1, "gemv"), (2, "grouped"), (3, "measured")):
                     arm = tq.tq_select_arm(n, k, E, T, pin)
                     assert {1: "gemv", 2: "grouped"}[arm] == O.dispatch_arm(n, k, E, T, name)
     assert tq.tq_grouped_min_tokens(6, 256, 16) == 683

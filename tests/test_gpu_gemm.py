@@ -158,3 +158,22 @@ def test_moe_forward_empty_batch():
     y, arm = tq.tq_moe_forward(x0, d["packed"], d["lut"], d["ids"][:0], d["w"][:0])
     check_no_device_error()
     assert tuple(y.shape) == (0, 128)
+
+
+def test_moe_forward_measured_policy():
+    """pin = ARM_MEASURED: the GEMV for a lone token (1 pair per woken expert),
+    the grouped GEMM once experts are shared (3 tokens of top-2 of 8: 1.30),
+    with the launch counters proving the arm and the output within tolerance."""
+    for n, want_arm in ((1, 1), (3, 2), (40, 2)):
+        prob = moe_inputs.make_custom(8, 2, n, 256, 128, 12, seed=70 + n)
+        d = to_device(prob)
+        before = tq.tq_launch_counts()
+        y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=16,
+                                   pin=tq.ARM_MEASURED)
+        check_no_device_error()
+        after = tq.tq_launch_counts()
+        assert arm == want_arm
+        ran = "grouped" if arm == 2 else "gemv"
+        assert after[ran] == before[ran] + 1
+        ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, 12)
+        assert normwise(y.float().cpu().numpy(), ref) <= TOL

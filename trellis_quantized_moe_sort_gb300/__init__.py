@@ -22,10 +22,10 @@ __all__ = [
     "tq_moe_workspace_size", "tq_moe_forward", "tq_moe_forward_static", "tq_device_error", "tq_launch_counts",
     "tq_status_string", "tq_probe_lut_rate", "tq_grouped_gemm_pairs", "tq_swiglu",
     "tq_moe_mlp_workspace_size", "tq_moe_mlp_forward", "tq_dequantize", "tq_grouped_gemm_dense",
-    "tq_moe_dequant_workspace_size", "tq_moe_forward_dequant", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "EXPORTED_SYMBOLS",
+    "tq_moe_dequant_workspace_size", "tq_moe_forward_dequant", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "ARM_MEASURED", "EXPORTED_SYMBOLS",
 ]
 
-ARM_AUTO, ARM_GEMV, ARM_GROUPED = 0, 1, 2
+ARM_AUTO, ARM_GEMV, ARM_GROUPED, ARM_MEASURED = 0, 1, 2, 3
 _HERE = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_HERE, "libtqmoe.so")
 

@@ -259,6 +259,9 @@ int64_t tq_tile_map_capacity(int64_t n, int top_k, int E, int tile_m) {
 int tq_select_arm(int64_t n, int top_k, int E, int tile_m, int pin) {
   if (bad_shape(top_k, E) || tile_m < 1 || n < 0) return TQ_ERR_INVALID_ARG;
   if (pin == TQ_ARM_GEMV || pin == TQ_ARM_GROUPED) return pin;
+  if (pin == TQ_ARM_MEASURED)
+    return (n > 0 && tq_pairs_per_woken_expert(n, top_k, E) >= TQ_MEASURED_CROSSOVER_PPW) ? TQ_ARM_GROUPED
+                                                                                         : TQ_ARM_GEMV;
   if (pin != TQ_ARM_AUTO) return TQ_ERR_INVALID_ARG;
   if (n <= TQ_DECODE_REGIME_MAX_TOKENS) return TQ_ARM_GEMV;
   return tq_tiles_amortize(n, top_k, E, tile_m) == 1 ? TQ_ARM_GROUPED : TQ_ARM_GEMV;
@@ -400,9 +403,10 @@ static int env_pin(int pin) {
   if (!v || !*v || !std::strcmp(v, "auto")) return TQ_ARM_AUTO;
   if (!std::strcmp(v, "gemv")) return TQ_ARM_GEMV;
   if (!std::strcmp(v, "grouped")) return TQ_ARM_GROUPED;
+  if (!std::strcmp(v, "measured")) return TQ_ARM_MEASURED;
   static std::once_flag warned;
   std::call_once(warned, [v] {
-    std::fprintf(stderr, "tqmoe: unknown TQ_FORCE_ARM=%s (expected auto|gemv|grouped); keeping auto\n", v);
+    std::fprintf(stderr, "tqmoe: unknown TQ_FORCE_ARM=%s (expected auto|gemv|grouped|measured); keeping auto\n", v);
   });
   return TQ_ARM_AUTO;
 }
