@@ -571,7 +571,9 @@ def run_gate_study(args):
 
         row = {"n": n, "pairs": n * s.top_k, "woken": int(len(np.unique(prob.topk_ids))),
                "pairs_per_woken_expert": round(tq.tq_pairs_per_woken_expert(n, s.top_k, s.E), 3),
-               "predicate_arm_T16": {1: "gemv", 2: "grouped"}[tq.tq_select_arm(n, s.top_k, s.E, 16)]}
+               "predicate_arm_T16": {1: "gemv", 2: "grouped"}[tq.tq_select_arm(n, s.top_k, s.E, 16)],
+               "measured_policy_arm": {1: "gemv", 2: "grouped"}[tq.tq_select_arm(n, s.top_k, s.E, 16,
+                                                                                  tq.ARM_MEASURED)]}
         row["gemv_us"] = round(timed(lambda: tq.tq_gemv(x, packed, lut, ids, w, y32)), 1)
         for T in (16, 128):
             _, offsets, sp = tq.tq_route(ids, s.E)
