@@ -77,16 +77,16 @@ def pin_gate_points():
 
 def pin_measured_policy():
     """The GB300 policy: grouped iff the expected pairs per woken expert reach
-    1.04.  k == E gives exactly n pairs per expert, so it selects from n = 2;
+    1.01.  k == E gives exactly n pairs per expert, so it selects from n = 2;
     at the V4 shape (top-6 of 256) pairs per woken expert is about
     1 + (n - 1) k / (2E) = 1 + 3(n - 1)/256 for small n (first order in k/E),
-    so n <= 4 stays below 1.04 and n = 5 reaches it."""
+    so n = 1 stays below 1.01 and n = 2 (1.0117) reaches it."""
     for E in (1, 4, 64):
         assert T.dispatch_arm(1, E, E, 16, pin="measured") == "gemv"
         assert T.dispatch_arm(2, E, E, 16, pin="measured") == "grouped"
     assert T.dispatch_arm(0, 6, 256, 16, pin="measured") == "gemv"
     arms = [T.dispatch_arm(n, 6, 256, 16, pin="measured") for n in range(1, 40)]
-    assert arms[:4] == ["gemv"] * 4 and set(arms[4:]) == {"grouped"}, arms
+    assert arms[:1] == ["gemv"] and set(arms[1:]) == {"grouped"}, arms
     # independent of TILE_M (the policy has no tile-fill term)
     assert all(T.dispatch_arm(n, 6, 256, tm, pin="measured") == T.dispatch_arm(n, 6, 256, 16, pin="measured")
                for n in (3, 5, 100) for tm in (1, 64, 256))
