@@ -121,12 +121,13 @@ int64_t tq_tile_map_capacity(int64_t n, int top_k, int E, int tile_m);
  * ([P3] "Two things that were built, correct, and switched off": the tile-fill
  * gate does not reproduce): this library's grouped kernel decodes each woken
  * expert once per m-tile whatever the tile's fill, so it wins as soon as
- * experts are shared; the arms tie at 1.01 pairs per woken expert (V4 up
- * shape, n = 2) and the grouped arm is chosen from there on, with no floor.
+ * experts are shared enough; the arms tie near 1.16 pairs per woken expert
+ * (V4 up shape, n ~ 14) and the grouped arm is chosen from there on, with no
+ * token floor.
  * tq_moe_forward reports TQ_ARM_GEMV or TQ_ARM_GROUPED as the arm used. */
 enum tq_arm { TQ_ARM_AUTO = 0, TQ_ARM_GEMV = 1, TQ_ARM_GROUPED = 2, TQ_ARM_MEASURED = 3 };
 #define TQ_DECODE_REGIME_MAX_TOKENS 8
-#define TQ_MEASURED_CROSSOVER_PPW 1.01
+#define TQ_MEASURED_CROSSOVER_PPW 1.16
 int tq_select_arm(int64_t n, int top_k, int E, int tile_m, int pin);
 
 /* ---------------------------------------------------------------------------

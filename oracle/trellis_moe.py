@@ -204,14 +204,14 @@ def tile_map_capacity(n: int, top_k: int, E: int, tile_m: int) -> int:
     return min(P, P // tile_m + min(E, P))
 
 
-MEASURED_CROSSOVER_PPW = 1.01
+MEASURED_CROSSOVER_PPW = 1.16
 
 
 def dispatch_arm(n: int, top_k: int, E: int, tile_m: int, pin: str = "auto") -> str:
     """[P1] post-merge note: n <= 8 or not amortized -> per-pair GEMV, else the
     grouped GEMM; ``pin`` forces an arm (the pages' A/B knob).  ``pin =
     "measured"``: the grouped GEMM once the expected pairs per woken expert
-    reach the crossover measured on GB300 (1.01), no floor ([P3] "Two things
+    reach the crossover measured on GB300 (1.16), no floor ([P3] "Two things
     that were built, correct, and switched off")."""
     if pin in ("gemv", "grouped"):
         return pin

@@ -77,16 +77,16 @@ def pin_gate_points():
 
 def pin_measured_policy():
     """The GB300 policy: grouped iff the expected pairs per woken expert reach
-    1.01.  k == E gives exactly n pairs per expert, so it selects from n = 2;
-    at the V4 shape (top-6 of 256) pairs per woken expert is about
-    1 + (n - 1) k / (2E) = 1 + 3(n - 1)/256 for small n (first order in k/E),
-    so n = 1 stays below 1.01 and n = 2 (1.0117) reaches it."""
+    1.16.  k == E gives exactly n pairs per expert, so it selects from n = 2;
+    at the V4 shape (top-6 of 256) pairs per woken expert grows by about
+    k / (2E) = 3/256 per token (first order in k/E): n = 13 gives 1.148 and
+    n = 14 gives 1.161 by the closed form, so the flip is at 14."""
     for E in (1, 4, 64):
         assert T.dispatch_arm(1, E, E, 16, pin="measured") == "gemv"
         assert T.dispatch_arm(2, E, E, 16, pin="measured") == "grouped"
     assert T.dispatch_arm(0, 6, 256, 16, pin="measured") == "gemv"
     arms = [T.dispatch_arm(n, 6, 256, 16, pin="measured") for n in range(1, 40)]
-    assert arms[:1] == ["gemv"] and set(arms[1:]) == {"grouped"}, arms
+    assert arms[:13] == ["gemv"] * 13 and set(arms[13:]) == {"grouped"}, arms
     # independent of TILE_M (the policy has no tile-fill term)
     assert all(T.dispatch_arm(n, 6, 256, tm, pin="measured") == T.dispatch_arm(n, 6, 256, 16, pin="measured")
                for n in (3, 5, 100) for tm in (1, 64, 256))

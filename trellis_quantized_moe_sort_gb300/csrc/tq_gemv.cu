@@ -6,13 +6,14 @@
 // its own GEMV, re-reading and re-decoding the expert once per pair (no
 // de-duplication across pairs).
 //
-// GB300 design: one CTA per SM holds the fp16 LUT in shared memory.  A warp
-// takes a work item (pair, group of RG consecutive weight rows).  It keeps the
-// token's activations in registers (lane l holds the 64-element chunks
-// l, l+32, ... of x[t]) and, for each row, loads the row's packed bytes with
-// coalesced 16-byte loads (lane l takes bytes [16c, 16c+16) of chunk c), gets
-// the 4 bytes before its chunk from the neighbour lane by shuffle (lane 0 from
-// lane 31 of the previous pass, zero at the row start), decodes its 64
+// GB300 design: one CTA per SM holds the fp16 LUT (and, for small batches,
+// every token's activations) in shared memory.  A warp takes a contiguous
+// range of (pair, weight row) items.  It keeps the current token's
+// activations in registers (lane l holds the 64-element chunks l, l+32, ...
+// of x[t]) and, for each row, loads the row's packed bytes with coalesced
+// 16-byte loads (lane l takes bytes [16c, 16c+16) of chunk c) one row ahead,
+// gets the 4 bytes before its chunk from the neighbour lane by shuffle (lane 0
+// from lane 31 of the previous pass, zero at the row start), decodes its 64
 // symbols by window identity, multiplies in fp32 (fp16 weights widened
 // exactly) and reduces the row over the warp with xor shuffles.
 #include <cuda_fp16.h>
@@ -35,16 +36,27 @@ template <int L, int CPL, int THREADS>
 __global__ void __launch_bounds__(THREADS, 1)
 gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
             const uint16_t* __restrict__ lut, const int32_t* __restrict__ topk_ids,
-            const float* __restrict__ topk_w, int P, int top_k, int E, int K, int N, int rg,
+            const float* __restrict__ topk_w, int P, int top_k, int E, int K, int N, int x_in_smem,
             float* __restrict__ y32, int* err) {
   extern __shared__ __align__(16) uint16_t lut_s[];
   constexpr int kEntries = 1 << L;
+  constexpr int kLutBytes = (kEntries * 2 + 15) & ~15;
   if constexpr (kEntries >= 8) {
     const uint4* src = reinterpret_cast<const uint4*>(lut);
     uint4* dst = reinterpret_cast<uint4*>(lut_s);
     for (int i = threadIdx.x; i < kEntries / 8; i += THREADS) dst[i] = __ldg(src + i);
   } else {
     for (int i = threadIdx.x; i < kEntries; i += THREADS) lut_s[i] = lut[i];
+  }
+  // Small batches: every token's activations staged once per CTA (after the
+  // LUT), so a warp that moves to another pair refills its registers from
+  // shared memory instead of waiting on global memory.
+  const int n_tok = P / top_k;
+  uint4* xs = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(lut_s) + kLutBytes);
+  if (x_in_smem) {
+    const uint4* src = reinterpret_cast<const uint4*>(x);
+    const int n16 = n_tok * K / 8;
+    for (int i = threadIdx.x; i < n16; i += THREADS) xs[i] = __ldg(src + i);
   }
   __syncthreads();
   const uint32_t lut_base = smem_u32(lut_s);
@@ -53,79 +65,105 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
   const int warps_per_block = THREADS / 32;
   const long long gwarp = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
   const long long nwarps = static_cast<long long>(gridDim.x) * warps_per_block;
-  const int groups = N / rg;
-  const long long items = static_cast<long long>(P) * groups;
   const int nchunks = K / kChunkSyms;
   const size_t row_bytes = static_cast<size_t>(K / 4);
+  // This warp's contiguous range of (pair, row) items: consecutive rows of
+  // one pair share the token's activations.
+  const long long items = static_cast<long long>(P) * N;
+  const long long i0 = items * gwarp / nwarps, i1 = items * (gwarp + 1) / nwarps;
 
-  for (long long it = gwarp; it < items; it += nwarps) {
-    const int pair = static_cast<int>(it / groups);
-    const int g = static_cast<int>(it - static_cast<long long>(pair) * groups);
-    const int tok = pair / top_k;
-    const int e = topk_ids[pair];
-    if (e < 0 || e >= E) {
-      if (lane == 0 && g == 0) record_error(err, TQ_ERR_INVALID_ARG, kWhereRoute);
-      continue;
-    }
-    const float wt = topk_w[pair];
-
-    // activations of this token: chunk c = lane + 32 i, 64 bf16 = 32 words
-    uint32_t xr[CPL][32];
+  // packed bytes of item `it` (zeros for a bad expert id, reported once per pair)
+  auto load_row = [&](long long it, uint4 (&q)[CPL]) {
+    const int pair = static_cast<int>(it / N);
+    const int r = static_cast<int>(it - static_cast<long long>(pair) * N);
+    const int e = __ldg(topk_ids + pair);
+    const bool ok = e >= 0 && e < E;
+    const uint4* rp = reinterpret_cast<const uint4*>(packed + (static_cast<size_t>(ok ? e : 0) * N + r) * row_bytes);
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
       const int c = lane + 32 * i;
-      if (c < nchunks) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(tok) * K + c * kChunkSyms);
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 q = __ldg(src + v);
-          xr[i][4 * v] = q.x;
-          xr[i][4 * v + 1] = q.y;
-          xr[i][4 * v + 2] = q.z;
-          xr[i][4 * v + 3] = q.w;
-        }
-      } else {
-#pragma unroll
-        for (int v = 0; v < 32; ++v) xr[i][v] = 0u;
-      }
+      q[i] = (ok && c < nchunks) ? __ldg(rp + c) : make_uint4(0u, 0u, 0u, 0u);
     }
+  };
 
-    const uint8_t* erow = packed + (static_cast<size_t>(e) * N + static_cast<size_t>(g) * rg) * row_bytes;
-    for (int r = 0; r < rg; ++r) {
-      const uint8_t* rowp = erow + static_cast<size_t>(r) * row_bytes;
-      float acc = 0.f;
-      uint32_t carry = 0u;  // last word of chunk (32 i - 1), held by lane 31
+  int cur_pair = -1, tok = 0;
+  float wt = 0.f;
+  bool pair_ok = false;
+  uint32_t xr[CPL][32];
+  auto process = [&](long long it, const uint4 (&qv)[CPL]) {
+    const int pair = static_cast<int>(it / N);
+    const int r = static_cast<int>(it - static_cast<long long>(pair) * N);
+    if (pair != cur_pair) {
+      cur_pair = pair;
+      tok = pair / top_k;
+      const int e = __ldg(topk_ids + pair);
+      pair_ok = e >= 0 && e < E;
+      if (!pair_ok && lane == 0 && (r == 0 || it == i0)) record_error(err, TQ_ERR_INVALID_ARG, kWhereRoute);
+      wt = __ldg(topk_w + pair);
+      // activations of this token: chunk c = lane + 32 i, 64 bf16 = 32 words
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
         const int c = lane + 32 * i;
-        uint4 q = make_uint4(0u, 0u, 0u, 0u);
-        if (c < nchunks) q = __ldg(reinterpret_cast<const uint4*>(rowp) + c);
-        uint32_t prev = __shfl_up_sync(0xffffffffu, q.w, 1);
-        if (lane == 0) prev = carry;
-        carry = __shfl_sync(0xffffffffu, q.w, 31);
         if (c < nchunks) {
-          const uint32_t words[5] = {prev, q.x, q.y, q.z, q.w};
+          const size_t off16 = (static_cast<size_t>(tok) * K + static_cast<size_t>(c) * kChunkSyms) / 8;
 #pragma unroll
-          for (int wi = 0; wi < 4; ++wi) {
-            const uint64_t lo64 = static_cast<uint64_t>(words[wi]) | (static_cast<uint64_t>(words[wi + 1]) << 32);
+          for (int v = 0; v < 8; ++v) {
+            const uint4 q = x_in_smem ? xs[off16 + v] : __ldg(reinterpret_cast<const uint4*>(x) + off16 + v);
+            xr[i][4 * v] = q.x;
+            xr[i][4 * v + 1] = q.y;
+            xr[i][4 * v + 2] = q.z;
+            xr[i][4 * v + 3] = q.w;
+          }
+        } else {
 #pragma unroll
-            for (int m = 0; m < 16; m += 2) {
-              const uint32_t o0 = static_cast<uint32_t>(lo64 >> (33 + 2 * m - L)) & ((1u << (L + 1)) - 2u);
-              const uint32_t o1 = static_cast<uint32_t>(lo64 >> (35 + 2 * m - L)) & ((1u << (L + 1)) - 2u);
-              uint32_t h0, h1;
-              asm volatile("ld.shared.u16 %0, [%1];" : "=r"(h0) : "r"(lut_base + o0));
-              asm volatile("ld.shared.u16 %0, [%1];" : "=r"(h1) : "r"(lut_base + o1));
-              const uint32_t xv = xr[i][wi * 8 + m / 2];
-              acc = fmaf(__half2float(__ushort_as_half(static_cast<unsigned short>(h0))), bf16lo(xv), acc);
-              acc = fmaf(__half2float(__ushort_as_half(static_cast<unsigned short>(h1))), bf16hi(xv), acc);
-            }
+          for (int v = 0; v < 32; ++v) xr[i][v] = 0u;
+        }
+      }
+    }
+    if (!pair_ok) return;
+    float acc = 0.f;
+    uint32_t carry = 0u;  // last word of chunk (32 i - 1), held by lane 31
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      const uint4 q = qv[i];
+      uint32_t prev = __shfl_up_sync(0xffffffffu, q.w, 1);
+      if (lane == 0) prev = carry;
+      carry = __shfl_sync(0xffffffffu, q.w, 31);
+      if (c < nchunks) {
+        const uint32_t words[5] = {prev, q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          const uint64_t lo64 = static_cast<uint64_t>(words[wi]) | (static_cast<uint64_t>(words[wi + 1]) << 32);
+#pragma unroll
+          for (int m = 0; m < 16; m += 2) {
+            const uint32_t o0 = static_cast<uint32_t>(lo64 >> (33 + 2 * m - L)) & ((1u << (L + 1)) - 2u);
+            const uint32_t o1 = static_cast<uint32_t>(lo64 >> (35 + 2 * m - L)) & ((1u << (L + 1)) - 2u);
+            uint32_t h0, h1;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=r"(h0) : "r"(lut_base + o0));
+            asm volatile("ld.shared.u16 %0, [%1];" : "=r"(h1) : "r"(lut_base + o1));
+            const uint32_t xv = xr[i][wi * 8 + m / 2];
+            acc = fmaf(__half2float(__ushort_as_half(static_cast<unsigned short>(h0))), bf16lo(xv), acc);
+            acc = fmaf(__half2float(__ushort_as_half(static_cast<unsigned short>(h1))), bf16hi(xv), acc);
           }
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) atomicAdd(y32 + static_cast<size_t>(tok) * N + static_cast<size_t>(g) * rg + r, acc * wt);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) atomicAdd(y32 + static_cast<size_t>(tok) * N + r, acc * wt);
+  };
+
+  // The next row's bytes are in flight while this row decodes (two register
+  // sets used in turn, so no copy waits for a load).
+  uint4 qa[CPL], qb[CPL];
+  if (i0 < i1) load_row(i0, qa);
+  for (long long it = i0; it < i1; it += 2) {
+    if (it + 1 < i1) load_row(it + 1, qb);
+    process(it, qa);
+    if (it + 1 >= i1) break;
+    if (it + 2 < i1) load_row(it + 2, qa);
+    process(it + 1, qb);
   }
 }
 
@@ -133,22 +171,22 @@ template <int L, int CPL>
 int launch_one(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, const int32_t* ids,
                const float* w, int P, int top_k, int E, int K, int N, float* y32, int* err,
                cudaStream_t s) {
-  constexpr int kThreads = (CPL >= 2) ? 256 : 512;
+  constexpr int kThreads = (CPL >= 4) ? 256 : 512;
   auto kfn = gemv_kernel<L, CPL, kThreads>;
-  const size_t smem = std::max<size_t>(16, sizeof(uint16_t) << L);
+  const size_t lut_bytes = ((sizeof(uint16_t) << L) + 15) & ~static_cast<size_t>(15);
+  const size_t x_bytes = static_cast<size_t>(P / top_k) * K * 2;
+  // activations go to shared memory when they fit beside the LUT (small batches)
+  const int x_in_smem = (lut_bytes + x_bytes <= 200u * 1024u) ? 1 : 0;
+  const size_t smem = std::max<size_t>(16, lut_bytes + (x_in_smem ? x_bytes : 0));
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess) {
     cudaGetLastError();
     return TQ_ERR_CUDA;
   }
   const int sms = sm_count();
-  const long long warps = static_cast<long long>(sms) * (kThreads / 32);
-  // rows per work item: as many as keep >= 4 items per warp (1..16, divides N)
-  int rg = 16;
-  while (rg > 1 && (static_cast<long long>(P) * (N / rg) < 4 * warps || N % rg != 0)) rg >>= 1;
-  const long long items = static_cast<long long>(P) * (N / rg);
+  const long long items = static_cast<long long>(P) * N;
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(sms, (items + kThreads / 32 - 1) / (kThreads / 32))));
-  kfn<<<grid, kThreads, smem, s>>>(x, packed, lut, ids, w, P, top_k, E, K, N, rg, y32, err);
+  kfn<<<grid, kThreads, smem, s>>>(x, packed, lut, ids, w, P, top_k, E, K, N, x_in_smem, y32, err);
   return launch_status();
 }
 
