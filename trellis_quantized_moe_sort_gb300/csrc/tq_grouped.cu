@@ -90,6 +90,7 @@ struct Params {
   int row_blocks;
   int rb_group;     // row blocks per ordering group (row_blocks = plain tile-major order)
   int pair_out;     // 0: y32[token] += w * D (combine); 1: y32[sorted slot] += D (per pair)
+  int allow_interleave;  // whole units round-robin over CTAs when there are many (blocked order only)
   int n_mma_max;    // largest MMA N (tile_m rounded up to 16)
   int pk_stages;    // packed super-stage buffers
   int act_stages;   // activation k-step buffers
@@ -147,6 +148,43 @@ __device__ __forceinline__ Segment segment_at(long long g, long long g_end, int 
   sg.tile = static_cast<int>(r / rb_group);
   sg.rb = static_cast<int>(grp * rb_group + (r - static_cast<long long>(sg.tile) * rb_group));
   return sg;
+}
+
+// A CTA's walk over its work.  Contiguous (step == 0): an equal share of the
+// flattened (unit, super-stage) positions, split at any super-stage, so every
+// CTA gets the same number of super-stages.  Interleaved (step == grid): whole
+// units blockIdx.x, blockIdx.x + grid, ...: the CTAs running at one time take
+// consecutive units, i.e. the row blocks of the same few m-tiles, so a tile's
+// activations are read from L2 by all of them instead of from DRAM once per
+// row block; used when every CTA has many units (the imbalance is at most one
+// unit in many).
+struct Walk {
+  long long g, g_end, step;
+};
+__device__ __forceinline__ Walk walk_begin(long long units, int n_ss, bool interleave) {
+  Walk w;
+  if (interleave) {
+    w.g = blockIdx.x;
+    w.g_end = units;
+    w.step = gridDim.x;
+  } else {
+    const long long total = units * n_ss;
+    w.g = total * blockIdx.x / gridDim.x;
+    w.g_end = total * (blockIdx.x + 1) / gridDim.x;
+    w.step = 0;
+  }
+  return w;
+}
+__device__ __forceinline__ bool walk_next(Walk& w, int n_ss, int num_tiles, int rb_group, Segment& sg) {
+  if (w.g >= w.g_end) return false;
+  if (w.step == 0) {
+    sg = segment_at(w.g, w.g_end, n_ss, num_tiles, rb_group);
+    w.g += sg.ss1 - sg.ss0;
+  } else {
+    sg = segment_at(w.g * n_ss, (w.g + 1) * n_ss, n_ss, num_tiles, rb_group);
+    w.g += w.step;
+  }
+  return true;
 }
 
 // Byte offset of logical byte b of staged row r (128-byte pitch) in the
@@ -314,11 +352,10 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   const int n_ss = (ksteps + kSSSteps - 1) / kSSSteps;
   const uint32_t acol0 = static_cast<uint32_t>(p.nacc * p.n_mma_max);
   const int rb_group = p.rb_group;
-  // This CTA's equal share of the flattened (unit, super-stage) work; every
-  // role walks it in the same order, one segment at a time.
-  const long long total = static_cast<long long>(num_tiles) * p.row_blocks * n_ss;
-  const long long g_beg = total * blockIdx.x / gridDim.x;
-  const long long g_end = total * (blockIdx.x + 1) / gridDim.x;
+  // This CTA's share of the (unit, super-stage) work; every role walks it in
+  // the same order, one segment at a time.
+  const long long units = static_cast<long long>(num_tiles) * p.row_blocks;
+  const Walk walk0 = walk_begin(units, n_ss, p.allow_interleave && units >= 16ll * gridDim.x);
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ packed-byte producer
@@ -326,9 +363,9 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     Pipe pk;
     long long pk_issued = 0;
     bool ok = true;
-    for (long long g = g_beg; g < g_end && ok;) {
-      const Segment sg = segment_at(g, g_end, n_ss, num_tiles, rb_group);
-      g += sg.ss1 - sg.ss0;
+    Walk w = walk0;
+    Segment sg;
+    while (ok && walk_next(w, n_ss, num_tiles, rb_group, sg)) {
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) {
         if (lane == 0) record_error(p.err, TQ_ERR_INVALID_ARG, kWhereGroupedProducer);
@@ -366,9 +403,9 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     long long act_issued = 0;
     bool ok = true;
     const uint32_t act_tx = static_cast<uint32_t>(p.n_mma_max) * kActRowBytes;
-    for (long long g = g_beg; g < g_end && ok;) {
-      const Segment sg = segment_at(g, g_end, n_ss, num_tiles, rb_group);
-      g += sg.ss1 - sg.ss0;
+    Walk w = walk0;
+    Segment sg;
+    while (ok && walk_next(w, n_ss, num_tiles, rb_group, sg)) {
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
       const int ks0 = sg.ss0 * kSSSteps, ks1 = min(ksteps, sg.ss1 * kSSSteps);
@@ -401,9 +438,9 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     Pipe act, apipe, accp;
     Pipe& wpipe = apipe;   // kDense: the A ring is the packed-byte ring
     bool ok = true;
-    for (long long g = g_beg; g < g_end && ok;) {
-      const Segment sg = segment_at(g, g_end, n_ss, num_tiles, rb_group);
-      g += sg.ss1 - sg.ss0;
+    Walk w = walk0;
+    Segment sg;
+    while (ok && walk_next(w, n_ss, num_tiles, rb_group, sg)) {
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
       const uint32_t n_mma = static_cast<uint32_t>((tl.rows + 15) & ~15);
@@ -470,9 +507,9 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     Pipe accp;
-    for (long long g = g_beg; g < g_end;) {
-      const Segment sg = segment_at(g, g_end, n_ss, num_tiles, rb_group);
-      g += sg.ss1 - sg.ss0;
+    Walk w = walk0;
+    Segment sg;
+    while (walk_next(w, n_ss, num_tiles, rb_group, sg)) {
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
       const int slot0 = tl.slot0, rows = tl.rows;
@@ -566,9 +603,9 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     Pipe pk, apipe;
     int pending_afull = -1;   // A stage stored but not yet handed to the MMA
     bool ok = true;
-    for (long long g = g_beg; g < g_end && ok;) {
-      const Segment sg = segment_at(g, g_end, n_ss, num_tiles, rb_group);
-      g += sg.ss1 - sg.ss0;
+    Walk w = walk0;
+    Segment sg;
+    while (ok && walk_next(w, n_ss, num_tiles, rb_group, sg)) {
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
       // 4 stream bytes before the first symbol of the segment (zero at the
@@ -714,6 +751,7 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
         break;
       }
     }
+    p.allow_interleave = 1;
   }
   p.n_mma_max = (tile_m + 15) & ~15;
   const int a_cols = dense ? 0 : kNumAStages * kATmemCols;   // decoded A stages in tensor memory
