@@ -191,10 +191,8 @@ def run_ours(args, rank, world, dist):
 
     def step(i, timed_slot=None):
         s = sets[i % args.weight_sets]
-        y32.zero_()
-        tq.tq_route(s["ids"], E, counts, offsets, sorted_pairs)
-        tq.tq_build_tile_map(offsets, T, cap, tiles, num_tiles)
-        tq.tq_gather_rows(s["x"], sorted_pairs, k, x_sorted)
+        # route + tile map (one launch), gather clearing y32 (one launch)
+        tq.tq_prepare(s["ids"], s["x"], E, T, cap, counts, offsets, sorted_pairs, tiles, num_tiles, x_sorted, y32)
         if timed_slot is not None:
             gev[timed_slot][0].record(stream)
         tq.tq_grouped_gemm(x_sorted, s["packed"], s["lut"], sorted_pairs, s["w"], tiles, num_tiles, k, T, y32)

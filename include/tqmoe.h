@@ -196,6 +196,20 @@ int tq_gather_rows(const uint16_t* x, const int32_t* sorted_pairs, int64_t n, in
                    uint16_t* x_sorted, tq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Everything the grouped GEMM needs, in two launches: tq_route and
+ * tq_build_tile_map fused into one single-block kernel (the tile map takes
+ * each expert's slot range from the sort's registers), then tq_gather_rows,
+ * which also clears y32[0 .. y32_count) (the fp32 accumulator; 16-byte
+ * aligned and y32_count % 4 == 0 for the fused clear, otherwise it is
+ * cleared by a separate memset).  Results are those of the three calls.
+ * Arguments as in tq_route, tq_build_tile_map and tq_gather_rows; y32 may be
+ * NULL when y32_count == 0.
+ * ------------------------------------------------------------------------- */
+int tq_prepare(const int32_t* topk_ids, const uint16_t* x, int64_t n, int top_k, int E, int K, int tile_m,
+               int32_t* counts, int32_t* offsets, int32_t* sorted_pairs, int32_t* tiles, int32_t* num_tiles,
+               int64_t cap, uint16_t* x_sorted, float* y32, int64_t y32_count, tq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Grouped GEMM  ([P1] m-tiles; [P2] contiguous-run decode, decode fused into
  * the multiply)
  *
@@ -384,9 +398,10 @@ int tq_probe_lut_rate(const uint16_t* table, int warps_per_sm, int iters, uint32
 
 /* Host-side counts of successful launches since process start, per kernel:
  * out[0] route, out[1] tile map, out[2] grouped GEMM (trellis or dense),
- * out[3] GEMV, out[4] combine, out[5] activation gather, out[6] router
- * top-k, out[7] dequantize ([P3]: counters prove which arm ran). */
-void tq_launch_counts(int64_t out[8]);
+ * out[3] GEMV, out[4] combine, out[5] activation gather (alone or clearing
+ * y32), out[6] router top-k, out[7] dequantize, out[8] route and tile map
+ * fused in one launch ([P3]: counters prove which arm ran). */
+void tq_launch_counts(int64_t out[9]);
 
 #ifdef __cplusplus
 }

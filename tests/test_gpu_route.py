@@ -109,3 +109,34 @@ def test_combine_bitexact():
         check_no_device_error()
         got = y.view(torch.int16).cpu().numpy().view(np.uint16)
         assert np.array_equal(got, O.bf16_rne_bits(arr))
+
+
+def test_prepare_equals_separate_calls():
+    """tq_prepare (route + tile map in one launch, gather clearing y32) gives
+    bit for bit what tq_route, tq_build_tile_map and tq_gather_rows give, and
+    leaves y32 zero."""
+    import moe_inputs
+    for name, T in (("v4_decode_n32", 16), ("v4_prefill_n8192_up", 256)):
+        prob = moe_inputs.make_problem(name, with_packed=False)
+        s = prob.shape
+        ids = torch.from_numpy(np.ascontiguousarray(prob.topk_ids)).cuda()
+        x = torch.from_numpy(prob.x_bits.view(np.int16)).cuda()
+        cap = tq.tq_tile_map_capacity(s.n, s.top_k, s.E, T)
+        c1, o1, sp1 = tq.tq_route(ids, s.E)
+        t1, nt1 = tq.tq_build_tile_map(o1, T, cap)
+        xs1 = tq.tq_gather_rows(x, sp1, s.top_k)
+        c2 = torch.empty_like(c1); o2 = torch.empty_like(o1); sp2 = torch.empty_like(sp1)
+        t2 = torch.full_like(t1, -7); nt2 = torch.empty_like(nt1); xs2 = torch.empty_like(xs1)
+        y32 = torch.full((s.n, s.N), 3.0, dtype=torch.float32, device="cuda")
+        before = tq.tq_launch_counts()
+        tq.tq_prepare(ids, x, s.E, T, cap, c2, o2, sp2, t2, nt2, xs2, y32)
+        torch.cuda.synchronize()
+        after = tq.tq_launch_counts()
+        assert after["route_tile_map"] == before["route_tile_map"] + 1
+        assert after["gather"] == before["gather"] + 1
+        assert tq.tq_device_error() == (0, 0)
+        for a, b in ((c1, c2), (o1, o2), (sp1, sp2), (nt1, nt2), (xs1, xs2)):
+            assert torch.equal(a, b)
+        ntiles = int(nt1.item())
+        assert torch.equal(t1[:ntiles], t2[:ntiles])
+        assert torch.count_nonzero(y32).item() == 0

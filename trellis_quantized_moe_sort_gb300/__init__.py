@@ -18,7 +18,7 @@ import os
 __all__ = [
     "TQError", "lib", "lib_path", "tq_init", "tq_arch_witness", "tq_pairs_per_woken_expert",
     "tq_tiles_amortize", "tq_grouped_min_tokens", "tq_tile_map_capacity", "tq_select_arm",
-    "tq_route", "tq_router_topk", "tq_route_logits", "tq_build_tile_map", "tq_gather_rows", "tq_grouped_gemm", "tq_gemv", "tq_combine",
+    "tq_route", "tq_router_topk", "tq_route_logits", "tq_build_tile_map", "tq_gather_rows", "tq_prepare", "tq_grouped_gemm", "tq_gemv", "tq_combine",
     "tq_moe_workspace_size", "tq_moe_forward", "tq_moe_forward_static", "tq_device_error", "tq_launch_counts",
     "tq_status_string", "tq_probe_lut_rate", "tq_grouped_gemm_pairs", "tq_swiglu",
     "tq_moe_mlp_workspace_size", "tq_moe_mlp_forward", "tq_dequantize", "tq_grouped_gemm_dense",
@@ -51,6 +51,8 @@ _SIGS = {
                          _c_int, _c_p, _c_p]),
     "tq_combine": (_c_int, [_c_p, _c_p, _c_i64, _c_p]),
     "tq_gather_rows": (_c_int, [_c_p, _c_p, _c_i64, _c_int, _c_int, _c_p, _c_p]),
+    "tq_prepare": (_c_int, [_c_p, _c_p, _c_i64, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p,
+                            _c_i64, _c_p, _c_p, _c_i64, _c_p]),
     "tq_moe_workspace_size": (_c_sz, [_c_i64, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "tq_moe_forward": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int,
                                 _c_int, _c_int, _c_int, _c_int, _c_p, _c_sz, _c_p,
@@ -270,6 +272,23 @@ def tq_gather_rows(x, sorted_pairs, top_k: int, x_sorted=None, stream=None):
     return x_sorted[:P]
 
 
+def tq_prepare(topk_ids, x, E: int, tile_m: int, cap: int, counts, offsets, sorted_pairs, tiles, num_tiles,
+               x_sorted, y32=None, stream=None) -> None:
+    """Route + tile map (one launch) and the activation gather, clearing y32
+    (fp32) in the same launch when it is given."""
+    torch = _torch()
+    n, top_k = topk_ids.shape
+    K = x.shape[1]
+    y32_ptr = None if y32 is None else _dev_ptr(y32, (torch.float32,), "y32")
+    _check(lib().tq_prepare(_dev_ptr(topk_ids, (torch.int32,), "topk_ids"), _dev_ptr(x, _bits16(), "x"), n, top_k,
+                            E, K, tile_m, _dev_ptr(counts, (torch.int32,), "counts"),
+                            _dev_ptr(offsets, (torch.int32,), "offsets"),
+                            _dev_ptr(sorted_pairs, (torch.int32,), "sorted_pairs"),
+                            _dev_ptr(tiles, (torch.int32,), "tiles"), _dev_ptr(num_tiles, (torch.int32,), "num_tiles"),
+                            cap, _dev_ptr(x_sorted, _bits16(), "x_sorted"), y32_ptr,
+                            0 if y32 is None else y32.numel(), _stream(stream)), "tq_prepare")
+
+
 def tq_grouped_gemm(x_sorted, packed, lut, sorted_pairs, topk_w, tiles, num_tiles, top_k: int, tile_m: int,
                     y32, stream=None) -> None:
     """y32 += grouped product (y32 fp32 [n, N], zero it for a plain product).
@@ -487,6 +506,7 @@ def tq_device_error() -> tuple[int, int]:
 
 
 def tq_launch_counts() -> dict:
-    arr = (ctypes.c_int64 * 8)()
+    arr = (ctypes.c_int64 * 9)()
     lib().tq_launch_counts(arr)
-    return dict(zip(("route", "tile_map", "grouped", "gemv", "combine", "gather", "router", "dequant"), list(arr)))
+    return dict(zip(("route", "tile_map", "grouped", "gemv", "combine", "gather", "router", "dequant",
+                     "route_tile_map"), list(arr)))

@@ -223,13 +223,12 @@ int tq_moe_forward_dequant(const uint16_t* x, const uint8_t* packed, const uint1
   const int P = static_cast<int>(n * top_k);
   const MoeScratch ws = carve_moe_scratch(workspace, n, top_k, E, K, N, cap);
   uint16_t* w_dense = reinterpret_cast<uint16_t*>(ws.end);   // [E][N][K]; slot e = expert e
-  if (cudaMemsetAsync(ws.y32, 0, sizeof(float) * static_cast<size_t>(n) * N, s) != cudaSuccess) {
-    cudaGetLastError();
-    return TQ_ERR_CUDA;
-  }
-  if ((rc = launch_route(topk_ids, P, E, ws.counts, ws.offsets, ws.sorted_pairs, err, s)) != TQ_OK) return rc;
-  if ((rc = launch_tile_map(ws.offsets, E, tile_m, ws.tiles, ws.num_tiles, cap, err, s)) != TQ_OK) return rc;
-  if ((rc = launch_gather(x, ws.sorted_pairs, P, top_k, K, ws.x_sorted, err, s)) != TQ_OK) return rc;
+  if ((rc = launch_route_tile_map(topk_ids, P, E, tile_m, ws.counts, ws.offsets, ws.sorted_pairs, ws.tiles,
+                                  ws.num_tiles, cap, err, s)) != TQ_OK)
+    return rc;
+  if ((rc = launch_gather_zero(x, ws.sorted_pairs, P, top_k, K, ws.x_sorted, ws.y32, static_cast<int64_t>(n) * N,
+                               err, s)) != TQ_OK)
+    return rc;
   // Materialize every woken expert (experts no pair routes to are skipped).
   if ((rc = launch_dequant(packed, lut, L, nullptr, ws.counts, E, E, N, K, w_dense, err, s)) != TQ_OK) return rc;
   if ((rc = launch_grouped(ws.x_sorted, nullptr, nullptr, 2, ws.sorted_pairs, topk_w, ws.tiles, ws.num_tiles, cap,

@@ -346,6 +346,10 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+  // Launched as a programmatic dependent of the kernel before it on the
+  // stream (inside tq_moe_forward): the prologue above read only the LUT,
+  // which that kernel does not write; everything below may depend on it.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int num_tiles = static_cast<int>(min(static_cast<long long>(*p.num_tiles), p.cap));
   const int ksteps = p.K / kKStep;
@@ -715,7 +719,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
                    const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                    const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
-                   int tile_m, float* y32, int* err, cudaStream_t s, int pair_out, const uint16_t* dense_w) {
+                   int tile_m, float* y32, int* err, cudaStream_t s, int pair_out, const uint16_t* dense_w,
+                   bool pdl) {
   auto encode = encode_fn();
   if (!encode) return TQ_ERR_CUDA;
   const bool dense = dense_w != nullptr;
@@ -831,7 +836,21 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
   const long long work = cap * static_cast<long long>(p.row_blocks) * n_ss;
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(work, sm_count())));
   void* args[] = {&tm_packed, &tm_xs, &p};
-  if (cudaLaunchKernel(kfn, dim3(grid), dim3(kThreads), args, smem, s) != cudaSuccess) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    // may start while the previous kernel on the stream finishes; the kernel
+    // waits for it (griddepcontrol.wait) after its prologue
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (cudaLaunchKernelExC(&cfg, kfn, args) != cudaSuccess) {
     cudaGetLastError();
     return TQ_ERR_LAUNCH;
   }

@@ -339,6 +339,29 @@ int tq_gather_rows(const uint16_t* x, const int32_t* sorted_pairs, int64_t n, in
   return launch_gather(x, sorted_pairs, static_cast<int>(P), top_k, K, x_sorted, err, s);
 }
 
+int tq_prepare(const int32_t* topk_ids, const uint16_t* x, int64_t n, int top_k, int E, int K, int tile_m,
+               int32_t* counts, int32_t* offsets, int32_t* sorted_pairs, int32_t* tiles, int32_t* num_tiles,
+               int64_t cap, uint16_t* x_sorted, float* y32, int64_t y32_count, tq_stream_t stream) {
+  if (bad_shape(top_k, E) || E > 1024 || n < 0 || tile_m < 1 || K < 8 || K % 8 != 0 || y32_count < 0)
+    return TQ_ERR_INVALID_ARG;
+  if (cap < 1 || cap >= (static_cast<int64_t>(1) << 31)) return TQ_ERR_INVALID_ARG;
+  const int64_t P = n * top_k;
+  if (P >= (static_cast<int64_t>(1) << 31)) return TQ_ERR_INVALID_ARG;
+  if (!counts || !offsets || !tiles || !num_tiles) return TQ_ERR_INVALID_ARG;
+  if (P > 0 && (!topk_ids || !x || !sorted_pairs || !x_sorted || !aligned16(x) || !aligned16(x_sorted)))
+    return TQ_ERR_INVALID_ARG;
+  if (y32_count > 0 && !y32) return TQ_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int rc = require_sm103(s);
+  if (rc != TQ_OK) return rc;
+  int* err = error_word(&rc);
+  if (!err) return rc;
+  rc = launch_route_tile_map(topk_ids, static_cast<int>(P), E, tile_m, counts, offsets, sorted_pairs, tiles,
+                             num_tiles, cap, err, s);
+  if (rc != TQ_OK) return rc;
+  return launch_gather_zero(x, sorted_pairs, static_cast<int>(P), top_k, K, x_sorted, y32, y32_count, err, s);
+}
+
 int tq_grouped_gemm(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
                     const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                     const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
@@ -444,19 +467,18 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
   float* y32 = ws.y32;
   uint16_t* x_sorted = ws.x_sorted;
 
-  if (cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(n) * N, s) != cudaSuccess) {
-    cudaGetLastError();
-    return TQ_ERR_CUDA;
-  }
   if (arm == TQ_ARM_GROUPED) {
-    rc = launch_route(topk_ids, static_cast<int>(P), E, counts, offsets, sorted_pairs, err, s);
+    // route + tile map in one launch, the gather clearing y32, then the
+    // grouped kernel as a programmatic dependent of the gather (its prologue
+    // overlaps the gather's tail)
+    rc = launch_route_tile_map(topk_ids, static_cast<int>(P), E, tile_m, counts, offsets, sorted_pairs, tiles,
+                               num_tiles, cap, err, s);
     if (rc != TQ_OK) return rc;
-    rc = launch_tile_map(offsets, E, tile_m, tiles, num_tiles, cap, err, s);
-    if (rc != TQ_OK) return rc;
-    rc = launch_gather(x, sorted_pairs, static_cast<int>(P), top_k, K, x_sorted, err, s);
+    rc = launch_gather_zero(x, sorted_pairs, static_cast<int>(P), top_k, K, x_sorted, y32,
+                            static_cast<int64_t>(n) * N, err, s);
     if (rc != TQ_OK) return rc;
     rc = launch_grouped(x_sorted, packed, lut, L, sorted_pairs, topk_w, tiles, num_tiles, cap, n, top_k, E, K,
-                        N, tile_m, y32, err, s);
+                        N, tile_m, y32, err, s, 0, nullptr, true);
     if (rc != TQ_OK) return rc;
     std::call_once(g_log_once, [&] {
       const char* q = std::getenv("TQ_QUIET");
@@ -470,6 +492,10 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
                    static_cast<long long>(tq_grouped_min_tokens(top_k, E, tile_m)));
     });
   } else {
+    if (cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(n) * N, s) != cudaSuccess) {
+      cudaGetLastError();
+      return TQ_ERR_CUDA;
+    }
     rc = launch_gemv(x, packed, lut, L, topk_ids, topk_w, n, top_k, E, K, N, y32, err, s);
     if (rc != TQ_OK) return rc;
   }
@@ -493,7 +519,7 @@ int tq_device_error(int* code, int* where) {
   return TQ_OK;
 }
 
-void tq_launch_counts(int64_t out[8]) {
+void tq_launch_counts(int64_t out[9]) {
   if (!out) return;
   for (int i = 0; i < kCntNum; ++i) out[i] = g_counts[i].load();
 }

@@ -20,7 +20,7 @@ int launch_status();
 
 enum Counter {
   kCntRoute = 0, kCntTileMap, kCntGrouped, kCntGemv, kCntCombine, kCntGather, kCntRouter, kCntDequant,
-  kCntNum
+  kCntRouteTileMap, kCntNum
 };
 void count_launch(Counter c);
 
@@ -37,11 +37,18 @@ int launch_combine(const float* y32, uint16_t* y, int64_t count, cudaStream_t s)
 int launch_router(const float* logits, int n, int E, int top_k, int32_t* ids, float* w, cudaStream_t s);
 int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top_k, int K,
                   uint16_t* x_sorted, int* err, cudaStream_t s);
+// The gather, also clearing y32[0 .. y32_count) in the same launch.
+int launch_gather_zero(const uint16_t* x, const int32_t* sorted_pairs, int P, int top_k, int K,
+                       uint16_t* x_sorted, float* y32, int64_t y32_count, int* err, cudaStream_t s);
+// Route and tile map in one launch.
+int launch_route_tile_map(const int32_t* topk_ids, int P, int E, int tile_m, int32_t* counts, int32_t* offsets,
+                          int32_t* sorted_pairs, int32_t* tiles, int32_t* num_tiles, int64_t cap, int* err,
+                          cudaStream_t s);
 int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
                    const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                    const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
                    int tile_m, float* y32, int* err, cudaStream_t s, int pair_out = 0,
-                   const uint16_t* dense_w = nullptr);
+                   const uint16_t* dense_w = nullptr, bool pdl = false);
 // Materializes weights: out[i] = bf16(W_{e_i}) [N][K] for slot i < m, e_i =
 // expert_ids[i] (or i when expert_ids is null); a slot whose expert has
 // counts[e_i] == 0 (when counts is given) or e_i < 0 is skipped.

@@ -146,14 +146,15 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
   uint16_t* h = reinterpret_cast<uint16_t*>(w);         w += align256(sizeof(uint16_t) * P * I);
   float* y32 = reinterpret_cast<float*>(w);
 
-  if (cudaMemsetAsync(gate_up, 0, sizeof(float) * P * 2 * I, s) != cudaSuccess ||
-      cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(n) * H, s) != cudaSuccess) {
+  if (cudaMemsetAsync(gate_up, 0, sizeof(float) * P * 2 * I, s) != cudaSuccess) {
     cudaGetLastError();
     return TQ_ERR_CUDA;
   }
-  rc = launch_route(topk_ids, static_cast<int>(P), E, counts, offsets, sorted_pairs, err, s);
-  if (rc == TQ_OK) rc = launch_tile_map(offsets, E, tile_m, tiles, num_tiles, cap, err, s);
-  if (rc == TQ_OK) rc = launch_gather(x, sorted_pairs, static_cast<int>(P), top_k, H, x_sorted, err, s);
+  rc = launch_route_tile_map(topk_ids, static_cast<int>(P), E, tile_m, counts, offsets, sorted_pairs, tiles,
+                             num_tiles, cap, err, s);
+  if (rc == TQ_OK)
+    rc = launch_gather_zero(x, sorted_pairs, static_cast<int>(P), top_k, H, x_sorted, y32,
+                            static_cast<int64_t>(n) * H, err, s);
   if (rc == TQ_OK)
     rc = launch_grouped(x_sorted, packed_gu, lut_gu, L, sorted_pairs, nullptr, tiles, num_tiles, cap, n, top_k, E,
                         H, 2 * I, tile_m, gate_up, err, s, /*pair_out=*/1);

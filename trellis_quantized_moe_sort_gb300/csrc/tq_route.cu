@@ -56,9 +56,12 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total) {
   return excl;
 }
 
-__global__ void __launch_bounds__(kBlock, 1)
-route_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ counts,
-             int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pairs, int* err) {
+// The routing sort of one block; thread e < E returns expert e's first sorted
+// slot in *first and its pair count in *count.
+__device__ __forceinline__ void route_block(const int32_t* __restrict__ ids, int P, int E,
+                                            int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                            int32_t* __restrict__ sorted_pairs, int* err, int* first,
+                                            int* count) {
   extern __shared__ int32_t wcnt[];  // [kWarps][E]: per-warp count, then per-warp base
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kWarps * E; i += kBlock) wcnt[i] = 0;
@@ -104,6 +107,8 @@ route_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict_
     for (int w = 0; w < kWarps; ++w) wcnt[w * E + e] += excl;
   }
   if (threadIdx.x == 0) offsets[E] = all;
+  *first = excl;
+  *count = e < E ? total : 0;
   __syncthreads();
 
   // 3. stable scatter: rank among equal experts of lower lanes, then advance
@@ -128,15 +133,17 @@ route_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict_
 }
 
 __global__ void __launch_bounds__(kBlock, 1)
-tile_map_kernel(const int32_t* __restrict__ offsets, int E, int tile_m, int32_t* __restrict__ tiles,
-                int32_t* __restrict__ num_tiles, long long cap, int* err) {
+route_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ counts,
+             int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pairs, int* err) {
+  int first, count;
+  route_block(ids, P, E, counts, offsets, sorted_pairs, err, &first, &count);
+}
+
+// The m-tile map of one block from expert e's (first slot, count) in thread e.
+__device__ __forceinline__ void tile_map_block(int E, int off, int cnt, int tile_m, int32_t* __restrict__ tiles,
+                                               int32_t* __restrict__ num_tiles, long long cap, int* err) {
   const int e = threadIdx.x;
-  int cnt = 0, nt = 0, off = 0;
-  if (e < E) {
-    off = offsets[e];
-    cnt = offsets[e + 1] - off;
-    nt = (cnt + tile_m - 1) / tile_m;
-  }
+  const int nt = e < E ? (cnt + tile_m - 1) / tile_m : 0;
   int total = 0;
   const int start = block_exclusive_scan(nt, &total);
   for (int i = 0; i < nt; ++i) {
@@ -155,6 +162,29 @@ tile_map_kernel(const int32_t* __restrict__ offsets, int E, int tile_m, int32_t*
       *num_tiles = total;
     }
   }
+}
+
+__global__ void __launch_bounds__(kBlock, 1)
+tile_map_kernel(const int32_t* __restrict__ offsets, int E, int tile_m, int32_t* __restrict__ tiles,
+                int32_t* __restrict__ num_tiles, long long cap, int* err) {
+  const int e = threadIdx.x;
+  int off = 0, cnt = 0;
+  if (e < E) {
+    off = offsets[e];
+    cnt = offsets[e + 1] - off;
+  }
+  tile_map_block(E, off, cnt, tile_m, tiles, num_tiles, cap, err);
+}
+
+// Route and tile map in one launch: the tile map takes each expert's slot
+// range from the sort's registers, not from memory.
+__global__ void __launch_bounds__(kBlock, 1)
+route_tile_map_kernel(const int32_t* __restrict__ ids, int P, int E, int tile_m, int32_t* __restrict__ counts,
+                      int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pairs,
+                      int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles, long long cap, int* err) {
+  int first, count;
+  route_block(ids, P, E, counts, offsets, sorted_pairs, err, &first, &count);
+  tile_map_block(E, first, count, tile_m, tiles, num_tiles, cap, err);
 }
 
 __global__ void combine_kernel_v4(const float4* __restrict__ y32, uint2* __restrict__ y, long long n4) {
@@ -181,8 +211,14 @@ __global__ void combine_kernel_scalar(const float* __restrict__ y32, uint16_t* _
 
 // x_sorted[slot] = x[sorted_pairs[slot] / top_k]: the activations in pair-sorted
 // order, 16 bytes per thread step; an out-of-range pair id yields a zero row.
+// When zero_n4 > 0 the same threads also clear zero4[0 .. zero_n4) (the fp32
+// accumulator of the grouped GEMM that follows), saving a launch.
 __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_pairs,
-                                   int P, int top_k, int row_vecs, uint4* __restrict__ x_sorted, int* err) {
+                                   int P, int top_k, int row_vecs, uint4* __restrict__ x_sorted, int* err,
+                                   float4* __restrict__ zero4, long long zero_n4) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < zero_n4;
+       i += (long long)gridDim.x * blockDim.x)
+    zero4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   const long long total = static_cast<long long>(P) * row_vecs;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
@@ -281,9 +317,49 @@ int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<long long>((total + threads - 1) / threads, sm_count() * 8));
   gather_rows_kernel<<<blocks, threads, 0, s>>>(reinterpret_cast<const uint4*>(x), sorted_pairs, P, top_k,
-                                                row_vecs, reinterpret_cast<uint4*>(x_sorted), err);
+                                                row_vecs, reinterpret_cast<uint4*>(x_sorted), err, nullptr, 0);
   const int st = launch_status();
   if (st == TQ_OK) count_launch(kCntGather);
+  return st;
+}
+
+int launch_gather_zero(const uint16_t* x, const int32_t* sorted_pairs, int P, int top_k, int K,
+                       uint16_t* x_sorted, float* y32, int64_t y32_count, int* err, cudaStream_t s) {
+  if (y32_count % 4 != 0 || (reinterpret_cast<uintptr_t>(y32) & 15u) != 0) {
+    // the accumulator cannot be cleared in 16-byte steps: clear it separately
+    if (y32_count > 0 && cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(y32_count), s) != cudaSuccess) {
+      cudaGetLastError();
+      return TQ_ERR_CUDA;
+    }
+    return launch_gather(x, sorted_pairs, P, top_k, K, x_sorted, err, s);
+  }
+  const long long z4 = y32_count / 4;
+  const int row_vecs = K / 8;
+  const long long total = std::max(static_cast<long long>(P) * row_vecs, z4);
+  if (total == 0) return TQ_OK;
+  const int threads = 256;
+  const int blocks = static_cast<int>(std::max<long long>(1, std::min<long long>((total + threads - 1) / threads, sm_count() * 8)));
+  gather_rows_kernel<<<blocks, threads, 0, s>>>(reinterpret_cast<const uint4*>(x), sorted_pairs, P, top_k,
+                                                row_vecs, reinterpret_cast<uint4*>(x_sorted), err,
+                                                reinterpret_cast<float4*>(y32), z4);
+  const int st = launch_status();
+  if (st == TQ_OK) count_launch(kCntGather);
+  return st;
+}
+
+int launch_route_tile_map(const int32_t* topk_ids, int P, int E, int tile_m, int32_t* counts, int32_t* offsets,
+                          int32_t* sorted_pairs, int32_t* tiles, int32_t* num_tiles, int64_t cap, int* err,
+                          cudaStream_t s) {
+  const size_t smem = sizeof(int32_t) * kWarps * E;
+  if (cudaFuncSetAttribute(route_tile_map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(sizeof(int32_t) * kWarps * 1024)) != cudaSuccess) {
+    cudaGetLastError();
+    return TQ_ERR_CUDA;
+  }
+  route_tile_map_kernel<<<1, kBlock, smem, s>>>(topk_ids, P, E, tile_m, counts, offsets, sorted_pairs, tiles,
+                                               num_tiles, (long long)cap, err);
+  const int st = launch_status();
+  if (st == TQ_OK) count_launch(kCntRouteTileMap);
   return st;
 }
 
