@@ -42,3 +42,33 @@ def test_lut_probe_rate_is_sane():
     rate = tq.tq_probe_lut_rate(8, 128)
     # between random-address bank conflicts at their worst and 32 banks per clock
     assert 2.0 < rate <= 32.0, rate
+
+
+@pytest.mark.parametrize("pin", [tq.ARM_GROUPED, tq.ARM_GEMV])
+def test_moe_forward_in_cuda_graph(pin):
+    """tq_moe_forward captured in a CUDA graph (its grouped kernel is a
+    programmatic dependent of the gather) replays to the eager result, on new
+    inputs copied into the captured buffers, within the fp32 summation-order
+    noise of the atomics."""
+    s = moe_inputs.shape("v4_decode_n32")
+    probs = [moe_inputs.make_problem("v4_decode_n32", layer=i) for i in range(2)]
+    devs = [to_device(p) for p in probs]
+    d = {k: v.clone() for k, v in devs[0].items()}
+    ws = torch.empty(tq.tq_moe_workspace_size(s.n, s.top_k, s.E, s.K, s.N, 16), dtype=torch.uint8, device="cuda")
+    y = torch.empty((s.n, s.N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=16, pin=pin, workspace=ws, y=y)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=16, pin=pin, workspace=ws, y=y)
+    for src in devs + devs[:1]:
+        for k in d:
+            d[k].copy_(src[k])
+        g.replay()
+        torch.cuda.synchronize()
+        check_no_device_error()
+        eager, _ = tq.tq_moe_forward(src["x"], src["packed"], src["lut"], src["ids"], src["w"], tile_m=16, pin=pin)
+        torch.cuda.synchronize()
+        assert normwise(y.float().cpu().numpy(), eager.float().cpu().numpy()) <= 1e-2
