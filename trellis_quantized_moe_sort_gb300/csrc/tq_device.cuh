@@ -19,6 +19,14 @@ enum ErrWhere : int {
 // TQ_ERR_DEVICE_TIMEOUT; no correct launch comes near it.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
+// Programmatic dependent launch.  pdl_wait: block until the grid this one
+// depends on (the previous kernel on the stream, when launched with
+// programmatic stream serialization) has finished and its writes are
+// visible; returns at once otherwise.  pdl_trigger: let the next such grid
+// start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void record_error(int* err, int code, int where) {
   // err[0] = first code, err[1] = its location.
   if (atomicCAS(err, 0, code) == 0) atomicExch(err + 1, where);

@@ -91,6 +91,7 @@ struct Params {
   int rb_group;     // row blocks per ordering group (row_blocks = plain tile-major order)
   int pair_out;     // 0: y32[token] += w * D (combine); 1: y32[sorted slot] += D (per pair)
   int allow_interleave;  // whole units round-robin over CTAs when there are many (blocked order only)
+  int early_prologue;    // the previous kernel writes nothing the prologue reads (LUT): overlap it
   int n_mma_max;    // largest MMA N (tile_m rounded up to 16)
   int pk_stages;    // packed super-stage buffers
   int act_stages;   // activation k-step buffers
@@ -269,6 +270,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
 
+  if (!p.early_prologue) pdl_wait();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int SP = p.pk_stages;
@@ -347,9 +349,9 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
   // Launched as a programmatic dependent of the kernel before it on the
-  // stream (inside tq_moe_forward): the prologue above read only the LUT,
-  // which that kernel does not write; everything below may depend on it.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // stream: with early_prologue the prologue above (which reads only the
+  // LUT) ran while that kernel finished; everything below may depend on it.
+  pdl_wait();
 
   const int num_tiles = static_cast<int>(min(static_cast<long long>(*p.num_tiles), p.cap));
   const int ksteps = p.K / kKStep;
@@ -673,6 +675,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     }
   }
 
+  pdl_trigger();   // the next kernel (the combine) may launch while this grid tears down
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpProducer) {
@@ -747,6 +750,7 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
   // Order by row-block groups only when the fp32 output is too large to stay
   // in L2 while six scattered partial sums per element arrive.
   p.pair_out = pair_out;
+  p.early_prologue = pdl ? 1 : 0;
   p.rb_group = p.row_blocks;
   const long long out_rows = pair_out ? n * static_cast<long long>(top_k) : n;
   if (out_rows * N * 4 > (24ll << 20)) {
@@ -841,15 +845,14 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
+  // The kernel may start while the previous kernel on the stream finishes; it
+  // waits for it (pdl_wait) at its start, or after its prologue when the
+  // caller knows that kernel does not write the LUT (early_prologue).
   cudaLaunchAttribute attr[1];
-  if (pdl) {
-    // may start while the previous kernel on the stream finishes; the kernel
-    // waits for it (griddepcontrol.wait) after its prologue
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (cudaLaunchKernelExC(&cfg, kfn, args) != cudaSuccess) {
     cudaGetLastError();
     return TQ_ERR_LAUNCH;

@@ -27,6 +27,28 @@ void count_launch(Counter c);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Launches `kernel` with programmatic stream serialization: it may begin while
+// the previous kernel on the stream finishes, so it must call pdl_wait()
+// before touching anything that kernel writes.  Returns the launch status.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    return TQ_ERR_LAUNCH;
+  }
+  return TQ_OK;
+}
+
 // Kernel launchers (defined in their own translation units).  Arguments are
 // validated by the caller; these only configure and launch.
 int launch_route(const int32_t* topk_ids, int P, int E, int32_t* counts, int32_t* offsets,

@@ -135,6 +135,8 @@ __device__ __forceinline__ void route_block(const int32_t* __restrict__ ids, int
 __global__ void __launch_bounds__(kBlock, 1)
 route_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ counts,
              int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pairs, int* err) {
+  pdl_wait();
+  pdl_trigger();
   int first, count;
   route_block(ids, P, E, counts, offsets, sorted_pairs, err, &first, &count);
 }
@@ -167,6 +169,8 @@ __device__ __forceinline__ void tile_map_block(int E, int off, int cnt, int tile
 __global__ void __launch_bounds__(kBlock, 1)
 tile_map_kernel(const int32_t* __restrict__ offsets, int E, int tile_m, int32_t* __restrict__ tiles,
                 int32_t* __restrict__ num_tiles, long long cap, int* err) {
+  pdl_wait();
+  pdl_trigger();
   const int e = threadIdx.x;
   int off = 0, cnt = 0;
   if (e < E) {
@@ -182,12 +186,15 @@ __global__ void __launch_bounds__(kBlock, 1)
 route_tile_map_kernel(const int32_t* __restrict__ ids, int P, int E, int tile_m, int32_t* __restrict__ counts,
                       int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pairs,
                       int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles, long long cap, int* err) {
+  pdl_wait();
+  pdl_trigger();
   int first, count;
   route_block(ids, P, E, counts, offsets, sorted_pairs, err, &first, &count);
   tile_map_block(E, first, count, tile_m, tiles, num_tiles, cap, err);
 }
 
 __global__ void combine_kernel_v4(const float4* __restrict__ y32, uint2* __restrict__ y, long long n4) {
+  pdl_wait();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
     const float4 v = y32[i];
@@ -202,6 +209,7 @@ __global__ void combine_kernel_v4(const float4* __restrict__ y32, uint2* __restr
 
 __global__ void combine_kernel_scalar(const float* __restrict__ y32, uint16_t* __restrict__ y,
                                       long long n) {
+  pdl_wait();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const __nv_bfloat16 b = __float2bfloat16_rn(y32[i]);
@@ -216,6 +224,8 @@ __global__ void combine_kernel_scalar(const float* __restrict__ y32, uint16_t* _
 __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_pairs,
                                    int P, int top_k, int row_vecs, uint4* __restrict__ x_sorted, int* err,
                                    float4* __restrict__ zero4, long long zero_n4) {
+  pdl_wait();
+  pdl_trigger();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < zero_n4;
        i += (long long)gridDim.x * blockDim.x)
     zero4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -316,9 +326,10 @@ int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top
   const long long total = static_cast<long long>(P) * row_vecs;
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<long long>((total + threads - 1) / threads, sm_count() * 8));
-  gather_rows_kernel<<<blocks, threads, 0, s>>>(reinterpret_cast<const uint4*>(x), sorted_pairs, P, top_k,
-                                                row_vecs, reinterpret_cast<uint4*>(x_sorted), err, nullptr, 0);
-  const int st = launch_status();
+  int st = launch_pdl(gather_rows_kernel, dim3(blocks), dim3(threads), 0, s, reinterpret_cast<const uint4*>(x),
+                      sorted_pairs, P, top_k, row_vecs, reinterpret_cast<uint4*>(x_sorted), err,
+                      static_cast<float4*>(nullptr), 0ll);
+  if (st == TQ_OK) st = launch_status();
   if (st == TQ_OK) count_launch(kCntGather);
   return st;
 }
@@ -339,10 +350,10 @@ int launch_gather_zero(const uint16_t* x, const int32_t* sorted_pairs, int P, in
   if (total == 0) return TQ_OK;
   const int threads = 256;
   const int blocks = static_cast<int>(std::max<long long>(1, std::min<long long>((total + threads - 1) / threads, sm_count() * 8)));
-  gather_rows_kernel<<<blocks, threads, 0, s>>>(reinterpret_cast<const uint4*>(x), sorted_pairs, P, top_k,
-                                                row_vecs, reinterpret_cast<uint4*>(x_sorted), err,
-                                                reinterpret_cast<float4*>(y32), z4);
-  const int st = launch_status();
+  int st = launch_pdl(gather_rows_kernel, dim3(blocks), dim3(threads), 0, s, reinterpret_cast<const uint4*>(x),
+                      sorted_pairs, P, top_k, row_vecs, reinterpret_cast<uint4*>(x_sorted), err,
+                      reinterpret_cast<float4*>(y32), z4);
+  if (st == TQ_OK) st = launch_status();
   if (st == TQ_OK) count_launch(kCntGather);
   return st;
 }
@@ -356,9 +367,9 @@ int launch_route_tile_map(const int32_t* topk_ids, int P, int E, int tile_m, int
     cudaGetLastError();
     return TQ_ERR_CUDA;
   }
-  route_tile_map_kernel<<<1, kBlock, smem, s>>>(topk_ids, P, E, tile_m, counts, offsets, sorted_pairs, tiles,
-                                               num_tiles, (long long)cap, err);
-  const int st = launch_status();
+  int st = launch_pdl(route_tile_map_kernel, dim3(1), dim3(kBlock), smem, s, topk_ids, P, E, tile_m, counts, offsets,
+                      sorted_pairs, tiles, num_tiles, static_cast<long long>(cap), err);
+  if (st == TQ_OK) st = launch_status();
   if (st == TQ_OK) count_launch(kCntRouteTileMap);
   return st;
 }
@@ -371,16 +382,17 @@ int launch_route(const int32_t* topk_ids, int P, int E, int32_t* counts, int32_t
     cudaGetLastError();
     return TQ_ERR_CUDA;
   }
-  route_kernel<<<1, kBlock, smem, s>>>(topk_ids, P, E, counts, offsets, sorted_pairs, err);
-  const int st = launch_status();
+  int st = launch_pdl(route_kernel, dim3(1), dim3(kBlock), smem, s, topk_ids, P, E, counts, offsets, sorted_pairs, err);
+  if (st == TQ_OK) st = launch_status();
   if (st == TQ_OK) count_launch(kCntRoute);
   return st;
 }
 
 int launch_tile_map(const int32_t* offsets, int E, int tile_m, int32_t* tiles, int32_t* num_tiles,
                     int64_t cap, int* err, cudaStream_t s) {
-  tile_map_kernel<<<1, kBlock, 0, s>>>(offsets, E, tile_m, tiles, num_tiles, (long long)cap, err);
-  const int st = launch_status();
+  int st = launch_pdl(tile_map_kernel, dim3(1), dim3(kBlock), 0, s, offsets, E, tile_m, tiles, num_tiles,
+                      static_cast<long long>(cap), err);
+  if (st == TQ_OK) st = launch_status();
   if (st == TQ_OK) count_launch(kCntTileMap);
   return st;
 }
@@ -394,11 +406,14 @@ int launch_combine(const float* y32, uint16_t* y, int64_t count, cudaStream_t s)
   if (vec) {
     const long long n4 = count / 4;
     const int blocks = static_cast<int>(std::min<long long>((n4 + threads - 1) / threads, max_blocks));
-    combine_kernel_v4<<<blocks, threads, 0, s>>>(reinterpret_cast<const float4*>(y32),
-                                                 reinterpret_cast<uint2*>(y), n4);
+    const int st = launch_pdl(combine_kernel_v4, dim3(blocks), dim3(threads), 0, s,
+                              reinterpret_cast<const float4*>(y32), reinterpret_cast<uint2*>(y), n4);
+    if (st != TQ_OK) return st;
   } else {
     const int blocks = static_cast<int>(std::min<long long>((count + threads - 1) / threads, max_blocks));
-    combine_kernel_scalar<<<blocks, threads, 0, s>>>(y32, y, count);
+    const int st = launch_pdl(combine_kernel_scalar, dim3(blocks), dim3(threads), 0, s, y32, y,
+                              static_cast<long long>(count));
+    if (st != TQ_OK) return st;
   }
   const int st = launch_status();
   if (st == TQ_OK) count_launch(kCntCombine);
