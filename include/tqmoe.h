@@ -109,6 +109,18 @@ int tq_tiles_amortize(int64_t n, int top_k, int E, int tile_m);
  * tile_m 16).  Negative TQ_ERR_INVALID_ARG on invalid arguments. */
 int64_t tq_grouped_min_tokens(int top_k, int E, int tile_m);
 
+/* Native m-tile size of the grouped kernel on sm_103a for a routing shape:
+ * 256 when the expected pairs per woken expert reach 128 (prefill sizes, where
+ * one decode per 256 pairs beats one per 128), else 128 (measured equal to or
+ * faster than smaller tiles at every decode size: the kernel pads a tile's
+ * pairs to the MMA's N, so small tiles save nothing and decode more).  The
+ * whole-product calls below take tile_m = TQ_TILE_NATIVE to use it: their
+ * kernels then run with this tile while the arm selection keeps the pages'
+ * TILE_M (TQ_GATE_TILE_M).  Negative on invalid arguments. */
+#define TQ_TILE_NATIVE 0
+#define TQ_GATE_TILE_M 16
+int tq_native_tile_m(int64_t n, int top_k, int E);
+
 /* Upper bound on the number of m-tiles sum_e ceil(count_e / tile_m) for ANY
  * routing of n*top_k pairs: min(P, floor(P / tile_m) + min(E, P)).  Size the
  * tile map with it.  Negative on invalid arguments. */
@@ -267,6 +279,9 @@ int tq_combine(const float* y32, uint16_t* y, int64_t count, tq_stream_t stream)
  *   It holds counts, offsets, sorted pairs, the tile map, the fp32
  *   accumulator and the pair-sorted activations; its contents are undefined
  *   after the call.
+ * tile_m: 1..256, the m-tile of both the arm selection and the kernel, or
+ *   TQ_TILE_NATIVE (tq_native_tile_m for the kernel, TQ_GATE_TILE_M for the
+ *   selection).
  * arm_used (host, may be NULL): receives TQ_ARM_GEMV or TQ_ARM_GROUPED.
  * The first grouped engagement in a process logs the tile fill and the
  * amortization boundary to stderr once (unless TQ_QUIET=1).

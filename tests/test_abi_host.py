@@ -82,3 +82,20 @@ def test_host_functions_reject_invalid_arguments(tq):
         tq.tq_select_arm(10, 2, 8, 16, pin=7)
     assert np.isnan(tq.tq_pairs_per_woken_expert(4, 9, 8))
     assert tq.tq_moe_workspace_size(16, 2, 8, 256, 128, 16) > 16 * 128 * 4 + 32 * 256 * 2
+
+
+def test_native_tile(tq):
+    """TQ_TILE_NATIVE: 128 at decode sizes, 256 once the expected pairs per
+    woken expert reach 128 (the oracle's closed form decides which); the
+    workspace of tile_m = 0 is that of the native tile."""
+    assert tq.TILE_NATIVE == 0
+    for n, k, E in ((1, 6, 256), (32, 6, 256), (1024, 6, 256), (8192, 6, 256), (5000, 2, 8), (0, 2, 8)):
+        want = 256 if n > 0 and O.pairs_per_woken_expert(n, k, E) >= 128 else 128
+        assert tq.tq_native_tile_m(n, k, E) == want, (n, k, E)
+        assert tq.tq_moe_workspace_size(n, k, E, 4096, 2048, 0) == tq.tq_moe_workspace_size(n, k, E, 4096, 2048, want)
+        assert (tq.tq_moe_mlp_workspace_size(n, k, E, 4096, 2048, 0)
+                == tq.tq_moe_mlp_workspace_size(n, k, E, 4096, 2048, want))
+    assert tq.tq_native_tile_m(32, 6, 256) == 128 and tq.tq_native_tile_m(8192, 6, 256) == 256
+    with pytest.raises(tq.TQError):
+        tq.tq_native_tile_m(4, 9, 8)
+    assert tq.tq_moe_workspace_size(16, 2, 8, 256, 128, 257) == 0

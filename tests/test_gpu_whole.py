@@ -72,3 +72,19 @@ def test_moe_forward_in_cuda_graph(pin):
         eager, _ = tq.tq_moe_forward(src["x"], src["packed"], src["lut"], src["ids"], src["w"], tile_m=16, pin=pin)
         torch.cuda.synchronize()
         assert normwise(y.float().cpu().numpy(), eager.float().cpu().numpy()) <= 1e-2
+
+
+@pytest.mark.parametrize("name", ["tiny_e8_k2_n16", "v4_decode_n32", "v4_prefill_n8192_up"])
+def test_moe_forward_native_tile(name):
+    """tile_m = TQ_TILE_NATIVE: the pages' TILE_M gates the arm, the kernel runs
+    its native tile (256 at the prefill size); output rows match the oracle."""
+    prob = moe_inputs.make_problem(name)
+    d = to_device(prob)
+    s = prob.shape
+    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=tq.TILE_NATIVE,
+                               pin=tq.ARM_AUTO if s.n > 1024 or s.E <= 8 else tq.ARM_GROUPED)
+    check_no_device_error()
+    assert arm == tq.tq_select_arm(s.n, s.top_k, s.E, 16) or s.n <= 1024
+    rows = sample_rows(s.N, 24, seed=3) if s.N > 256 else np.arange(s.N)
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L, rows=rows)
+    assert normwise(y.float().cpu().numpy()[:, rows], ref) <= TOL

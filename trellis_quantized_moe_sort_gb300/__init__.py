@@ -17,7 +17,7 @@ import os
 
 __all__ = [
     "TQError", "lib", "lib_path", "tq_init", "tq_arch_witness", "tq_pairs_per_woken_expert",
-    "tq_tiles_amortize", "tq_grouped_min_tokens", "tq_tile_map_capacity", "tq_select_arm",
+    "tq_tiles_amortize", "tq_grouped_min_tokens", "tq_tile_map_capacity", "tq_native_tile_m", "TILE_NATIVE", "tq_select_arm",
     "tq_route", "tq_router_topk", "tq_route_logits", "tq_build_tile_map", "tq_gather_rows", "tq_prepare", "tq_grouped_gemm", "tq_gemv", "tq_combine",
     "tq_moe_workspace_size", "tq_moe_forward", "tq_moe_forward_static", "tq_device_error", "tq_launch_counts",
     "tq_status_string", "tq_probe_lut_rate", "tq_grouped_gemm_pairs", "tq_swiglu",
@@ -26,6 +26,7 @@ __all__ = [
 ]
 
 ARM_AUTO, ARM_GEMV, ARM_GROUPED, ARM_MEASURED = 0, 1, 2, 3
+TILE_NATIVE = 0          # tile_m of the whole-product calls: the kernel's native m-tile
 _HERE = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_HERE, "libtqmoe.so")
 
@@ -40,6 +41,7 @@ _SIGS = {
     "tq_tiles_amortize": (_c_int, [_c_i64, _c_int, _c_int, _c_int]),
     "tq_grouped_min_tokens": (_c_i64, [_c_int, _c_int, _c_int]),
     "tq_tile_map_capacity": (_c_i64, [_c_i64, _c_int, _c_int, _c_int]),
+    "tq_native_tile_m": (_c_int, [_c_i64, _c_int, _c_int]),
     "tq_select_arm": (_c_int, [_c_i64, _c_int, _c_int, _c_int, _c_int]),
     "tq_route": (_c_int, [_c_p, _c_i64, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p]),
     "tq_build_tile_map": (_c_int, [_c_p, _c_int, _c_int, _c_p, _c_p, _c_i64, _c_p]),
@@ -173,6 +175,13 @@ def tq_grouped_min_tokens(top_k: int, E: int, tile_m: int) -> int:
     if rc < 0:
         raise TQError(int(rc), "tq_grouped_min_tokens")
     return int(rc)
+
+
+def tq_native_tile_m(n: int, top_k: int, E: int) -> int:
+    v = lib().tq_native_tile_m(n, top_k, E)
+    if v < 0:
+        raise TQError(v, "tq_native_tile_m")
+    return int(v)
 
 
 def tq_tile_map_capacity(n: int, top_k: int, E: int, tile_m: int) -> int:

@@ -193,7 +193,7 @@ int tq_grouped_gemm_dense(const uint16_t* x_sorted, const uint16_t* w_dense, con
 }
 
 size_t tq_moe_dequant_workspace_size(int64_t n, int top_k, int E, int K, int N, int tile_m) {
-  const size_t base = tq_moe_workspace_size(n, top_k, E, K, N, tile_m);
+  const size_t base = tq_moe_workspace_size(n, top_k, E, K, N, tile_m);   // resolves TQ_TILE_NATIVE
   if (base == 0) return 0;
   return base + al256(sizeof(uint16_t) * static_cast<size_t>(E) * N * K);
 }
@@ -203,12 +203,16 @@ int tq_moe_forward_dequant(const uint16_t* x, const uint8_t* packed, const uint1
                            int tile_m, void* workspace, size_t workspace_bytes, uint16_t* y, tq_stream_t stream) {
   if (E < 1 || top_k < 1 || top_k > E || E > 1024 || n < 0 || K < 64 || K % 64 != 0 || N < 128 || N % 128 != 0)
     return TQ_ERR_INVALID_ARG;
-  if (L < 2 || L > 16 || (L & 1) || tile_m < 1 || tile_m > 256) return TQ_ERR_INVALID_ARG;
+  const int tile_arg = tile_m;
+  int gate_tile = 0;
+  if (L < 2 || L > 16 || (L & 1) || !resolve_tile(n, top_k, E, tile_arg, &tile_m, &gate_tile))
+    return TQ_ERR_INVALID_ARG;
+  (void)gate_tile;   // the comparator has no arm selection
   if (n * top_k >= (static_cast<int64_t>(1) << 31) || static_cast<int64_t>(E) * N >= (static_cast<int64_t>(1) << 31))
     return TQ_ERR_INVALID_ARG;
   if (n > 0 && (!x || !packed || !lut || !topk_ids || !topk_w || !y)) return TQ_ERR_INVALID_ARG;
   if (n > 0 && (!al16(x) || !al16(packed) || !al16(lut))) return TQ_ERR_INVALID_ARG;
-  const size_t need = tq_moe_dequant_workspace_size(n, top_k, E, K, N, tile_m);
+  const size_t need = tq_moe_dequant_workspace_size(n, top_k, E, K, N, tile_arg);
   if (need == 0) return TQ_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return TQ_ERR_WORKSPACE;

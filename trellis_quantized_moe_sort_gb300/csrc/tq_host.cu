@@ -161,6 +161,19 @@ int sm_count() {
   return v;
 }
 
+bool resolve_tile(int64_t n, int top_k, int E, int tile_m, int* kernel_tile, int* gate_tile) {
+  if (tile_m == TQ_TILE_NATIVE) {
+    const int t = tq_native_tile_m(n, top_k, E);
+    if (t < 0) return false;
+    *kernel_tile = t;
+    *gate_tile = TQ_GATE_TILE_M;
+    return true;
+  }
+  if (tile_m < 1 || tile_m > 256) return false;
+  *kernel_tile = *gate_tile = tile_m;
+  return true;
+}
+
 // Every region is 256-byte aligned and sized as in tq_moe_workspace_size.
 MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K, int N, int64_t cap) {
   const size_t P = static_cast<size_t>(n) * top_k;
@@ -405,8 +418,15 @@ int tq_combine(const float* y32, uint16_t* y, int64_t count, tq_stream_t stream)
   return launch_combine(y32, y, count, s);
 }
 
+int tq_native_tile_m(int64_t n, int top_k, int E) {
+  if (bad_shape(top_k, E) || n < 0) return TQ_ERR_INVALID_ARG;
+  return (n > 0 && tq_pairs_per_woken_expert(n, top_k, E) >= 128.0) ? 256 : 128;
+}
+
 size_t tq_moe_workspace_size(int64_t n, int top_k, int E, int K, int N, int tile_m) {
-  const int64_t cap = tq_tile_map_capacity(n, top_k, E, tile_m);
+  int kt, gt;
+  if (!resolve_tile(n, top_k, E, tile_m, &kt, &gt)) return 0;
+  const int64_t cap = tq_tile_map_capacity(n, top_k, E, kt);
   if (cap < 0 || N < 1 || K < 1) return 0;
   const size_t P = static_cast<size_t>(n) * top_k;
   size_t b = 0;
@@ -439,9 +459,10 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
                    void* workspace, size_t workspace_bytes, uint16_t* y, int* arm_used, tq_stream_t stream) {
   int rc = check_gemm_common(x, packed, lut, L, topk_w, n, top_k, E, K, N, y);
   if (rc != TQ_OK) return rc;
-  if (tile_m < 1 || tile_m > 256 || E > 1024) return TQ_ERR_INVALID_ARG;
+  int gate_tile = 0;
+  if (E > 1024 || !resolve_tile(n, top_k, E, tile_m, &tile_m, &gate_tile)) return TQ_ERR_INVALID_ARG;
   if (n > 0 && !topk_ids) return TQ_ERR_INVALID_ARG;
-  const int arm = tq_select_arm(n, top_k, E, tile_m, env_pin(pin));
+  const int arm = tq_select_arm(n, top_k, E, gate_tile, env_pin(pin));
   if (arm < 0) return arm;
   if (arm == TQ_ARM_GROUPED && N % 128 != 0) return TQ_ERR_INVALID_ARG;
   if (arm == TQ_ARM_GEMV && K > 8192) return TQ_ERR_INVALID_ARG;
@@ -487,9 +508,9 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
       std::fprintf(stderr,
                    "tqmoe: trellis grouped GEMM engaged at %lld tokens x top-%d of %d experts - m-tiles %.0f%% "
                    "full (%.2f pairs per woken expert against TILE_M=%d); the amortization boundary for this "
-                   "routing shape is %lld tokens\n",
-                   static_cast<long long>(n), top_k, E, 100.0 * ppw / tile_m, ppw, tile_m,
-                   static_cast<long long>(tq_grouped_min_tokens(top_k, E, tile_m)));
+                   "routing shape is %lld tokens; kernel m-tile %d\n",
+                   static_cast<long long>(n), top_k, E, 100.0 * ppw / gate_tile, ppw, gate_tile,
+                   static_cast<long long>(tq_grouped_min_tokens(top_k, E, gate_tile)), tile_m);
     });
   } else {
     if (cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(n) * N, s) != cudaSuccess) {

@@ -91,6 +91,11 @@ struct MoeScratch {
   uint8_t* end;
 };
 MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K, int N, int64_t cap);
+
+// tile_m of the whole-product calls: 1..256 for both the arm selection and the
+// kernel, or TQ_TILE_NATIVE (the kernel's native tile, the pages' TILE_M for
+// the selection).  Returns false on an invalid value.
+bool resolve_tile(int64_t n, int top_k, int E, int tile_m, int* kernel_tile, int* gate_tile);
 int launch_swiglu(const float* gate_up, int64_t P, int I, uint16_t* h, cudaStream_t s);
 int launch_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
                 const int32_t* topk_ids, const float* topk_w, int64_t n, int top_k, int E, int K,

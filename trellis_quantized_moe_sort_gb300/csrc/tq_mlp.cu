@@ -94,7 +94,9 @@ int tq_swiglu(const float* gate_up, int64_t P, int I, uint16_t* h, tq_stream_t s
 }
 
 size_t tq_moe_mlp_workspace_size(int64_t n, int top_k, int E, int H, int I, int tile_m) {
-  const int64_t cap = tq_tile_map_capacity(n, top_k, E, tile_m);
+  int kt, gt;
+  if (!resolve_tile(n, top_k, E, tile_m, &kt, &gt)) return 0;
+  const int64_t cap = tq_tile_map_capacity(n, top_k, E, kt);
   if (cap < 0 || H < 1 || I < 1) return 0;
   const size_t P = static_cast<size_t>(n) * top_k;
   size_t b = 0;
@@ -114,7 +116,11 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
                        const uint8_t* packed_down, const uint16_t* lut_down, int L, const int32_t* topk_ids,
                        const float* topk_w, int64_t n, int top_k, int E, int H, int I, int tile_m,
                        void* workspace, size_t workspace_bytes, uint16_t* y, tq_stream_t stream) {
-  if (E < 1 || E > 1024 || top_k < 1 || top_k > E || n < 0 || tile_m < 1 || tile_m > 256) return TQ_ERR_INVALID_ARG;
+  const int tile_arg = tile_m;
+  int gate_tile = 0;
+  if (E < 1 || E > 1024 || top_k < 1 || top_k > E || n < 0) return TQ_ERR_INVALID_ARG;
+  if (!resolve_tile(n, top_k, E, tile_arg, &tile_m, &gate_tile)) return TQ_ERR_INVALID_ARG;
+  (void)gate_tile;   // the MLP runs the grouped arm only
   if (H < 128 || H % 128 != 0 || I < 64 || I % 64 != 0 || (2 * I) % 128 != 0) return TQ_ERR_INVALID_ARG;
   if (L < 2 || L > 16 || (L & 1)) return TQ_ERR_INVALID_ARG;
   if (n * top_k >= (1ll << 31)) return TQ_ERR_INVALID_ARG;
@@ -123,7 +129,7 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
   if (n > 0 && (!aligned16(x) || !aligned16(packed_gu) || !aligned16(lut_gu) || !aligned16(packed_down) ||
                 !aligned16(lut_down)))
     return TQ_ERR_INVALID_ARG;
-  const size_t need = tq_moe_mlp_workspace_size(n, top_k, E, H, I, tile_m);
+  const size_t need = tq_moe_mlp_workspace_size(n, top_k, E, H, I, tile_arg);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return TQ_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
