@@ -46,9 +46,21 @@ dequant_kernel(const uint8_t* __restrict__ packed, const uint16_t* __restrict__ 
   extern __shared__ __align__(16) uint16_t lut_s[];
   constexpr int kEntries = 1 << L;
   constexpr uint32_t kMask = (1u << L) - 1u;
-  for (int i = threadIdx.x; i < kEntries; i += blockDim.x) {
-    const __nv_bfloat16 b = __float2bfloat16_rn(__half2float(__ushort_as_half(__ldg(lut + i))));
-    lut_s[i] = *reinterpret_cast<const uint16_t*>(&b);
+  if constexpr (kEntries >= 8) {
+    // fp16 table in by asynchronous copies, then converted in place
+    stage_to_smem(smem_u32(lut_s), lut, kEntries * 2);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kEntries / 2; i += blockDim.x) {
+      uint32_t* w = reinterpret_cast<uint32_t*>(lut_s) + i;
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(w));
+      const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+      *w = *reinterpret_cast<const uint32_t*>(&b);
+    }
+  } else {
+    for (int i = threadIdx.x; i < kEntries; i += blockDim.x) {
+      const __nv_bfloat16 b = __float2bfloat16_rn(__half2float(__ushort_as_half(__ldg(lut + i))));
+      lut_s[i] = *reinterpret_cast<const uint16_t*>(&b);
+    }
   }
   __syncthreads();
 

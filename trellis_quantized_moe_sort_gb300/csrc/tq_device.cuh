@@ -19,6 +19,17 @@ enum ErrWhere : int {
 // TQ_ERR_DEVICE_TIMEOUT; no correct launch comes near it.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
+// Copies `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// global to shared memory with 16-byte asynchronous copies spread over the
+// block's threads, all in flight at once, and waits for this thread's
+// copies; follow with __syncthreads() before reading what others copied.
+__device__ __forceinline__ void stage_to_smem(uint32_t smem_dst, const void* gsrc, uint32_t bytes) {
+  const char* src = static_cast<const char*>(gsrc);
+  for (uint32_t off = 16u * threadIdx.x; off < bytes; off += 16u * blockDim.x)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst + off), "l"(src + off) : "memory");
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Programmatic dependent launch.  pdl_wait: block until the grid this one
 // depends on (the previous kernel on the stream, when launched with
 // programmatic stream serialization) has finished and its writes are

@@ -42,9 +42,7 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
   constexpr int kEntries = 1 << L;
   constexpr int kLutBytes = (kEntries * 2 + 15) & ~15;
   if constexpr (kEntries >= 8) {
-    const uint4* src = reinterpret_cast<const uint4*>(lut);
-    uint4* dst = reinterpret_cast<uint4*>(lut_s);
-    for (int i = threadIdx.x; i < kEntries / 8; i += THREADS) dst[i] = __ldg(src + i);
+    stage_to_smem(smem_u32(lut_s), lut, kEntries * 2);
   } else {
     for (int i = threadIdx.x; i < kEntries; i += THREADS) lut_s[i] = lut[i];
   }
@@ -53,11 +51,7 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
   // shared memory instead of waiting on global memory.
   const int n_tok = P / top_k;
   uint4* xs = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(lut_s) + kLutBytes);
-  if (x_in_smem) {
-    const uint4* src = reinterpret_cast<const uint4*>(x);
-    const int n16 = n_tok * K / 8;
-    for (int i = threadIdx.x; i < n16; i += THREADS) xs[i] = __ldg(src + i);
-  }
+  if (x_in_smem) stage_to_smem(smem_u32(xs), x, static_cast<uint32_t>(n_tok) * K * 2);
   __syncthreads();
   const uint32_t lut_base = smem_u32(lut_s);
 

@@ -323,10 +323,13 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     constexpr int kEntries = 1 << L;
     uint16_t* lut_dst = reinterpret_cast<uint16_t*>(gbase + p.off_lut);
     if constexpr (kEntries >= 8) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.lut);
+      // fp16 table in by asynchronous copies (all in flight), then converted
+      // in place, 8 entries per step
+      stage_to_smem(lut_s, p.lut, kEntries * 2);
+      __syncthreads();
       uint4* dst = reinterpret_cast<uint4*>(lut_dst);
       for (int i = threadIdx.x; i < kEntries / 8; i += kThreads) {
-        uint4 v = __ldg(src + i);
+        uint4 v = dst[i];
         uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
