@@ -51,7 +51,19 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
   // shared memory instead of waiting on global memory.
   const int n_tok = P / top_k;
   uint4* xs = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(lut_s) + kLutBytes);
-  if (x_in_smem) stage_to_smem(smem_u32(xs), x, static_cast<uint32_t>(n_tok) * K * 2);
+  if (x_in_smem) {
+    // 16-byte piece v of 128-byte chunk c goes to piece v ^ (c & 7) of the chunk
+    const uint32_t xs_base = smem_u32(xs);
+    const int pieces = n_tok * K / 8;
+    for (int q = threadIdx.x; q < pieces; q += THREADS) {
+      const int g = q >> 3, v = q & 7;   // global chunk (8 pieces each; K is a multiple of 64)
+      const int c = g % (K / kChunkSyms);  // chunk within its token: the reader's swizzle key
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(xs_base + 16u * static_cast<uint32_t>(8 * g + (v ^ (c & 7)))),
+                   "l"(reinterpret_cast<const uint4*>(x) + q)
+                   : "memory");
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  }
   __syncthreads();
   const uint32_t lut_base = smem_u32(lut_s);
 
@@ -102,7 +114,10 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
           const size_t off16 = (static_cast<size_t>(tok) * K + static_cast<size_t>(c) * kChunkSyms) / 8;
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
-            const uint4 q = x_in_smem ? xs[off16 + v] : __ldg(reinterpret_cast<const uint4*>(x) + off16 + v);
+            // shared copy: piece v of chunk c sits at piece v ^ (c & 7), so
+            // the 32 lanes (chunks 32 apart) spread over all banks
+            const uint4 q = x_in_smem ? xs[off16 + (v ^ (c & 7))]
+                                      : __ldg(reinterpret_cast<const uint4*>(x) + off16 + v);
             xr[i][4 * v] = q.x;
             xr[i][4 * v + 1] = q.y;
             xr[i][4 * v + 2] = q.z;
