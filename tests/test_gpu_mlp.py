@@ -54,6 +54,21 @@ def test_mlp_v4_n32_sampled_tokens():
     assert normwise(y[tokens].float().cpu().numpy(), ref) <= TOL
 
 
+def test_mlp_prefill_native_tile_sampled_tokens():
+    """8192 tokens, Zipf routing, the native m-tile (256): the per-pair gate|up
+    output is large enough for the blocked row order and the round-robin unit
+    walk; three tokens against the oracle."""
+    prob = moe_inputs.make_mlp_problem("v4_mlp_prefill_n8192")
+    d = _mlp_dev(prob)
+    y = tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"],
+                              tile_m=tq.TILE_NATIVE)
+    check_no_device_error()
+    tokens = [370, 1221, 2109]    # three tokens sharing most of their 9 experts (keeps the oracle short)
+    ref = O.moe_mlp(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed_gu, prob.lut_gu, prob.packed_down,
+                    prob.lut_down, prob.L, tokens=tokens)
+    assert normwise(y[tokens].float().cpu().numpy(), ref) <= TOL
+
+
 def test_grouped_gemm_pairs_all_outputs():
     prob = moe_inputs.make_custom(8, 2, 24, 256, 256, 12, seed=91)
     d = to_device(prob)
