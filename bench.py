@@ -428,12 +428,15 @@ def run_sweep(args):
              "lut": _cuda(torch, prob.lut_bits.view(np.int16))}
         y32 = torch.zeros((s.n, s.N), dtype=torch.float32, device="cuda")
 
-        def timed(fn):
+        def timed(fn, flush_l2=True):
             fn()
             torch.cuda.synchronize()
             ts = []
             for _ in range(args.steps):
-                flush.zero_()
+                if flush_l2:
+                    flush.zero_()
+                else:
+                    fn()   # keeps the GPU busy while the timed launch is enqueued; leaves L2 warm
                 a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
                 fn()
@@ -461,6 +464,16 @@ def run_sweep(args):
                 gather_us = timed(lambda: tq.tq_gather_rows(d["x"], sp, s.top_k, xs))
                 us = timed(lambda: tq.tq_grouped_gemm(xs, d["packed"], d["lut"], sp, d["w"], tiles, nt,
                                                        s.top_k, T, y32))
+                call = lambda: tq.tq_grouped_gemm(xs, d["packed"], d["lut"], sp, d["w"], tiles, nt, s.top_k, T, y32)
+                extra = {"hot_l2_us": round(timed(call, flush_l2=False), 1)}
+                # host cost of one call (Python binding + C ABI + launch), GPU kept busy
+                torch.cuda.synchronize()
+                flush.zero_()
+                h0 = time.perf_counter()
+                for _ in range(20):
+                    call()
+                extra["host_us_per_call"] = round((time.perf_counter() - h0) / 20 * 1e6, 1)
+                torch.cuda.synchronize()
                 staged = ntiles * s.N * s.K // 4
             elif arm == "dequant":
                 # dequantize-materialize comparator: every woken expert decoded
@@ -505,6 +518,10 @@ def run_sweep(args):
             lookups = (ntiles if ntiles is not None else s.pairs) * s.N * s.K
             if arm == "dequant":
                 lookups = woken * s.N * s.K
+            extra["dispatch_T16"] = {1: "gemv", 2: "grouped"}[tq.tq_select_arm(s.n, s.top_k, s.E, 16)]
+            extra["dispatch_measured"] = {1: "gemv", 2: "grouped"}[tq.tq_select_arm(s.n, s.top_k, s.E, 16,
+                                                                                    tq.ARM_MEASURED)]
+            extra["native_tile_m"] = tq.tq_native_tile_m(s.n, s.top_k, s.E)
             print(json.dumps({**extra, 
                 "workload": name, "arm": arm, "tile_m": T, "n": s.n, "pairs": s.pairs, "woken": woken,
                 "m_tiles": ntiles, "us": round(us, 1), "gather_us": gather_us, "pairs_per_s": round(s.pairs / (us * 1e-6), 1),

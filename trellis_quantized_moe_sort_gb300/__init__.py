@@ -116,35 +116,67 @@ def _check(rc: int, what: str):
 
 # ------------------------------------------------------------------ torch glue
 
+_torch_mod = None
+
+
 def _torch():
-    import torch
-    if not torch.cuda.is_available():
-        raise RuntimeError("trellis_quantized_moe_sort_gb300 needs a CUDA device (sm_103a); none found")
-    return torch
+    """torch, once a CUDA device has been seen (checked on the first call only)."""
+    global _torch_mod
+    if _torch_mod is None:
+        import torch
+        if not torch.cuda.is_available():
+            raise RuntimeError("trellis_quantized_moe_sort_gb300 needs a CUDA device (sm_103a); none found")
+        _torch_mod = torch
+    return _torch_mod
 
 
 def _dev_ptr(t, dtypes, name):
-    torch = _torch()
-    if not isinstance(t, torch.Tensor):
-        raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
-    if dtypes and t.dtype not in dtypes:
-        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
-    if not t.is_contiguous():
+    """Device address of a contiguous CUDA tensor of one of `dtypes`."""
+    try:
+        ok = t.is_cuda and (not dtypes or t.dtype in dtypes) and t.is_contiguous()
+    except AttributeError:
+        raise TypeError(f"{name} must be a torch.Tensor") from None
+    if not ok:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if dtypes and t.dtype not in dtypes:
+            raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
         raise ValueError(f"{name} must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
+
+
+def _current_stream_fast():
+    """Raw handle of torch's current stream on the current device."""
+    torch = _torch()
+    return torch.cuda.current_stream().cuda_stream
+
+
+_raw_stream_fn = None
 
 
 def _stream(stream):
+    global _raw_stream_fn
+    if stream is not None:
+        return stream.cuda_stream
     torch = _torch()
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if _raw_stream_fn is None:
+        # the C-level getter of torch's current stream (a plain integer), when
+        # this torch build has it; else the public (slower) route
+        getter = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _raw_stream_fn = ((lambda: getter(torch.cuda.current_device())) if getter is not None
+                          else _current_stream_fast)
+    return _raw_stream_fn()
+
+
+_bits16_types = None
 
 
 def _bits16():
-    torch = _torch()
-    return (torch.bfloat16, torch.float16, torch.int16, torch.uint16)
+    global _bits16_types
+    if _bits16_types is None:
+        torch = _torch()
+        _bits16_types = (torch.bfloat16, torch.float16, torch.int16, torch.uint16)
+    return _bits16_types
 
 
 # ------------------------------------------------------------------ API
