@@ -91,6 +91,7 @@ struct Params {
   int rb_group;     // row blocks per ordering group (row_blocks = plain tile-major order)
   int pair_out;     // 0: y32[token] += w * D (combine); 1: y32[sorted slot] += D (per pair)
   int allow_interleave;  // whole units round-robin over CTAs when there are many (blocked order only)
+  int store_out;         // whole units always, and plain stores: every output element has one writer
   int early_prologue;    // the previous kernel writes nothing the prologue reads (LUT): overlap it
   int n_mma_max;    // largest MMA N (tile_m rounded up to 16)
   int pk_stages;    // packed super-stage buffers
@@ -364,7 +365,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   // This CTA's share of the (unit, super-stage) work; every role walks it in
   // the same order, one segment at a time.
   const long long units = static_cast<long long>(num_tiles) * p.row_blocks;
-  const Walk walk0 = walk_begin(units, n_ss, p.allow_interleave && units >= 16ll * gridDim.x);
+  const Walk walk0 = walk_begin(units, n_ss, p.store_out || (p.allow_interleave && units >= 16ll * gridDim.x));
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ packed-byte producer
@@ -588,9 +589,14 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
             const float wt = __shfl_sync(0xffffffffu, owt[b], src);
             if (out_row >= 0) {
               float* dst = yrow + static_cast<size_t>(out_row) * p.N;
-              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x0 * wt),
-                           "f"(x1 * wt), "f"(x2 * wt), "f"(x3 * wt)
-                           : "memory");
+              if (p.store_out)
+                asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x0 * wt), "f"(x1 * wt),
+                             "f"(x2 * wt), "f"(x3 * wt)
+                             : "memory");
+              else
+                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x0 * wt),
+                             "f"(x1 * wt), "f"(x2 * wt), "f"(x3 * wt)
+                             : "memory");
             }
           }
         }
@@ -726,7 +732,7 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
                    const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                    const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
                    int tile_m, float* y32, int* err, cudaStream_t s, int pair_out, const uint16_t* dense_w,
-                   bool pdl) {
+                   bool pdl, bool store_out) {
   auto encode = encode_fn();
   if (!encode) return TQ_ERR_CUDA;
   const bool dense = dense_w != nullptr;
@@ -754,6 +760,9 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
   // in L2 while six scattered partial sums per element arrive.
   p.pair_out = pair_out;
   p.early_prologue = pdl ? 1 : 0;
+  // Per-pair outputs written once each: whole units (never split between
+  // CTAs) and plain stores, so the caller need not clear the output first.
+  p.store_out = (store_out && pair_out) ? 1 : 0;
   p.rb_group = p.row_blocks;
   const long long out_rows = pair_out ? n * static_cast<long long>(top_k) : n;
   if (out_rows * N * 4 > (24ll << 20)) {

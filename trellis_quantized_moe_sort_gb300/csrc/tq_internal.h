@@ -70,7 +70,7 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
                    const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                    const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
                    int tile_m, float* y32, int* err, cudaStream_t s, int pair_out = 0,
-                   const uint16_t* dense_w = nullptr, bool pdl = false);
+                   const uint16_t* dense_w = nullptr, bool pdl = false, bool store_out = false);
 // Materializes weights: out[i] = bf16(W_{e_i}) [N][K] for slot i < m, e_i =
 // expert_ids[i] (or i when expert_ids is null); a slot whose expert has
 // counts[e_i] == 0 (when counts is given) or e_i < 0 is skipped.

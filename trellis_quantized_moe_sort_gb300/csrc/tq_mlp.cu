@@ -152,10 +152,6 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
   uint16_t* h = reinterpret_cast<uint16_t*>(w);         w += align256(sizeof(uint16_t) * P * I);
   float* y32 = reinterpret_cast<float*>(w);
 
-  if (cudaMemsetAsync(gate_up, 0, sizeof(float) * P * 2 * I, s) != cudaSuccess) {
-    cudaGetLastError();
-    return TQ_ERR_CUDA;
-  }
   rc = launch_route_tile_map(topk_ids, static_cast<int>(P), E, tile_m, counts, offsets, sorted_pairs, tiles,
                              num_tiles, cap, err, s);
   if (rc == TQ_OK)
@@ -163,7 +159,8 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
                             static_cast<int64_t>(n) * H, err, s);
   if (rc == TQ_OK)
     rc = launch_grouped(x_sorted, packed_gu, lut_gu, L, sorted_pairs, nullptr, tiles, num_tiles, cap, n, top_k, E,
-                        H, 2 * I, tile_m, gate_up, err, s, /*pair_out=*/1);
+                        H, 2 * I, tile_m, gate_up, err, s, /*pair_out=*/1, nullptr, false,
+                        /*store_out=*/true);   // every gate|up element written once: no clear needed
   if (rc == TQ_OK) rc = launch_swiglu(gate_up, static_cast<int64_t>(P), I, h, s);
   if (rc == TQ_OK)
     rc = launch_grouped(h, packed_down, lut_down, L, sorted_pairs, topk_w, tiles, num_tiles, cap, n, top_k, E, I,
