@@ -37,10 +37,16 @@
  *    allocates device memory or keeps a pointer after returning (the one fixed
  *    device array the library holds is described at tq_moe_forward_static).
  *  - Calls taking a stream enqueue work on it and return without waiting;
- *    they never synchronize the device.  Status codes report argument and
- *    launch errors only; device-side faults of the data (an expert id out of
- *    range, a tile map over capacity, a wait that timed out) are recorded in a
- *    device error word read by tq_device_error().
+ *    they never synchronize the device.  The route, tile map, gather,
+ *    grouped GEMM and combine kernels are launched as programmatic dependents
+ *    of the previous kernel on the stream (they may start while it drains)
+ *    and wait for it to finish before touching memory, so stream order holds
+ *    as for ordinary launches.  (Inside tq_moe_forward the grouped kernel
+ *    reads its LUT before that wait; the kernel before it there is the
+ *    library's own gather, which does not write the LUT.)  Status codes
+ *    report argument and launch errors only; device-side faults of the data
+ *    (an expert id out of range, a tile map over capacity, a wait that timed
+ *    out) are recorded in a device error word read by tq_device_error().
  *  - Return value: TQ_OK (0) or a negative TQ_ERR_* code.  A failed call has
  *    launched nothing or reports the launch failure; outputs are then
  *    undefined and must not be read as results.
