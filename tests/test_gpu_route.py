@@ -140,3 +140,36 @@ def test_prepare_equals_separate_calls():
         ntiles = int(nt1.item())
         assert torch.equal(t1[:ntiles], t2[:ntiles])
         assert torch.count_nonzero(y32).item() == 0
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("tile_m", [1, 16, 256])
+def test_prepare_bitexact_against_oracle(name, tile_m):
+    """The fused route + tile map launch and the gather of tq_prepare against
+    the oracle's route and tile map, bit for bit, on every routing case."""
+    ids, E = CASES[name]
+    n, k = ids.shape
+    K = 64
+    rng = np.random.Generator(np.random.PCG64(17))
+    x_bits = moe_inputs.fp32_to_bf16_bits(rng.standard_normal((n, K), dtype=np.float32))
+    d_ids = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32)).cuda()
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda()
+    cap = tq.tq_tile_map_capacity(n, k, E, tile_m)
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    sp = torch.empty(max(n * k, 1), dtype=torch.int32, device="cuda")
+    tiles = torch.empty((max(cap, 1), 3), dtype=torch.int32, device="cuda")
+    nt = torch.empty(1, dtype=torch.int32, device="cuda")
+    xs = torch.empty((max(n * k, 1), K), dtype=torch.int16, device="cuda")
+    tq.tq_prepare(d_ids, x, E, tile_m, max(cap, 1), counts, offsets, sp[:n * k], tiles, nt, xs[:n * k])
+    check_no_device_error()
+    c, o, s = O.route(ids, E)
+    assert np.array_equal(counts.cpu().numpy(), c)
+    assert np.array_equal(offsets.cpu().numpy(), o)
+    assert np.array_equal(sp[:n * k].cpu().numpy(), s)
+    want = O.tile_map(o, tile_m)
+    got_n = int(nt.item())
+    assert got_n == len(want)
+    assert np.array_equal(tiles[:got_n].cpu().numpy(), np.asarray(want, dtype=np.int32).reshape(-1, 3))
+    if n * k:
+        np.testing.assert_array_equal(xs[:n * k].cpu().numpy().view(np.uint16), x_bits[s // k])
