@@ -15,8 +15,10 @@ from __future__ import annotations
 
 import os
 
-os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the CPU baseline runs on one core
-os.environ.setdefault("OMP_NUM_THREADS", "1")
+# the CPU baseline (the numpy oracle) runs on exactly one core: pin every BLAS
+# and OpenMP pool before numpy loads, so its reported "cores": 1 holds
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+    os.environ[_v] = "1"
 os.environ.setdefault("MKL_NUM_THREADS", "1")
 
 import argparse
