@@ -19,7 +19,6 @@ import os
 # and OpenMP pool before numpy loads, so its reported "cores": 1 holds
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
     os.environ[_v] = "1"
-os.environ.setdefault("MKL_NUM_THREADS", "1")
 
 import argparse
 import json
