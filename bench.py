@@ -636,34 +636,43 @@ def run_mlp_sweep(args):
         ws = torch.empty(tq.tq_moe_mlp_workspace_size(prob.n, prob.top_k, prob.E, prob.H, prob.I, T),
                          dtype=torch.uint8, device="cuda")
         y = torch.empty((prob.n, prob.H), dtype=torch.bfloat16, device="cuda")
-        call = lambda: tq.tq_moe_mlp_forward(x, pgu, lgu, pd, ld, ids, w, tile_m=T, workspace=ws, y=y)
-        call()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(args.steps):
-            flush.zero_()
-            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            call()
-            b_.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b_) * 1e3)
-        code, where = tq.tq_device_error()
-        if code:
-            raise RuntimeError(f"device error {code} at {where} ({name})")
-        counts = np.bincount(prob.topk_ids.reshape(-1), minlength=prob.E)
-        tiles = int(np.sum(-(-counts // T)))
-        lookups = tiles * (2 * prob.I * prob.H + prob.H * prob.I)
-        us = float(np.median(ts))
-        ceiling = lookups / (152 * rate * 2.07e9) * 1e6
-        flops = 2 * prob.n * prob.top_k * 3 * prob.H * prob.I
-        print(json.dumps({"workload": name, "tile_m": T, "n": prob.n, "pairs": prob.n * prob.top_k, "m_tiles": tiles,
-                          "us_per_call": round(us, 1), "tokens_per_s": round(prob.n / (us * 1e-6), 1),
-                          "lookups": lookups, "decode_ceiling_us": round(ceiling, 1),
-                          "decode_frac": round(ceiling / us, 3),
-                          "tensor_roofline_us": round(flops / (measured_peaks()[2] * 1e12) * 1e6, 1)}), flush=True)
+        for pin in ([tq.ARM_GROUPED, tq.ARM_GEMV] if prob.n <= 128 else [tq.ARM_GROUPED]):
+            _mlp_time(args, tq, torch, flush, rate, name, prob, T, pin,
+                      lambda: tq.tq_moe_mlp_forward(x, pgu, lgu, pd, ld, ids, w, tile_m=T, pin=pin, workspace=ws,
+                                                    y=y))
         del x, pgu, pd, ws, y
         torch.cuda.empty_cache()
+
+
+def _mlp_time(args, tq, torch, flush, rate, name, prob, T, pin, call):
+    """One line of --mlp-sweep: the call's median time after an L2 flush."""
+    call()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b_.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b_) * 1e3)
+    code, where = tq.tq_device_error()
+    if code:
+        raise RuntimeError(f"device error {code} at {where} ({name})")
+    counts = np.bincount(prob.topk_ids.reshape(-1), minlength=prob.E)
+    tiles = int(np.sum(-(-counts // T)))
+    units = tiles if pin == tq.ARM_GROUPED else prob.n * prob.top_k   # decodes per matrix
+    lookups = units * (2 * prob.I * prob.H + prob.H * prob.I)
+    us = float(np.median(ts))
+    ceiling = lookups / (152 * rate * 2.07e9) * 1e6
+    flops = 2 * prob.n * prob.top_k * 3 * prob.H * prob.I
+    print(json.dumps({"workload": name, "arm": {tq.ARM_GROUPED: "grouped", tq.ARM_GEMV: "gemv"}[pin],
+                      "tile_m": T, "n": prob.n, "pairs": prob.n * prob.top_k, "m_tiles": tiles,
+                      "us_per_call": round(us, 1), "tokens_per_s": round(prob.n / (us * 1e-6), 1),
+                      "lookups": lookups, "decode_ceiling_us": round(ceiling, 1),
+                      "decode_frac": round(ceiling / us, 3),
+                      "tensor_roofline_us": round(flops / (measured_peaks()[2] * 1e12) * 1e6, 1)}), flush=True)
 
 
 def main(argv=None):

@@ -343,9 +343,13 @@ int tq_moe_forward_static(const uint16_t* x, const uint8_t* packed, const uint16
  * tq_swiglu: h[s][i] = bf16(silu(g) * u), g = gate_up[s][i],
  *   u = gate_up[s][I + i]; gate_up (device) fp32 [P][2I], h (device) bf16
  *   [P][I]; I % 4 == 0.
- * tq_moe_mlp_forward: route, tile map, gather, gate|up (per pair), SwiGLU,
- *   down (combined per token with the router weights), bf16 y [n][H]; the
- *   grouped arm only.  H % 128 == 0, I % 64 == 0.  workspace (device) >=
+ * tq_moe_mlp_forward: the arm chosen as in tq_moe_forward (tq_select_arm with
+ *   `pin`, the gate's TILE_M from `tile_m`; arm_used (host, may be NULL)
+ *   receives it).  Grouped arm: route + tile map, gather, gate|up (per pair),
+ *   SwiGLU, down (combined per token with the router weights).  GEMV arm:
+ *   gate|up by per-pair GEMVs, SwiGLU, down by per-pair GEMVs on h combined
+ *   per token.  Output bf16 y [n][H].  H % 128 == 0, I % 64 == 0 (and
+ *   H, I <= 8192 for the GEMV arm).  workspace (device) >=
  *   tq_moe_mlp_workspace_size(...) bytes, 256-byte aligned.
  * ------------------------------------------------------------------------- */
 int tq_grouped_gemm_pairs(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
@@ -357,8 +361,9 @@ size_t tq_moe_mlp_workspace_size(int64_t n, int top_k, int E, int H, int I, int 
 int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16_t* lut_gu,
                        const uint8_t* packed_down, const uint16_t* lut_down, int L,
                        const int32_t* topk_ids, const float* topk_w,
-                       int64_t n, int top_k, int E, int H, int I, int tile_m,
-                       void* workspace, size_t workspace_bytes, uint16_t* y, tq_stream_t stream);
+                       int64_t n, int top_k, int E, int H, int I, int tile_m, int pin,
+                       void* workspace, size_t workspace_bytes, uint16_t* y, int* arm_used,
+                       tq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Dequantize-materialize comparator  ([P1] "Tests": the dequantize path that

@@ -202,6 +202,8 @@ MLP_WORKLOADS = {
     "v4_mlp_n32": (256, 6, 32, 4096, 2048, 16, "uniform"),
     "v4_mlp_n128": (256, 6, 128, 4096, 2048, 16, "uniform"),
     "v4_mlp_prefill_n8192": (256, 6, 8192, 4096, 2048, 16, "zipf"),
+    # one token (batch-1 decode), appended last so earlier workloads keep their seeds
+    "v4_mlp_n1": (256, 6, 1, 4096, 2048, 16, "uniform"),
 }
 
 

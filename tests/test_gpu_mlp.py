@@ -32,22 +32,31 @@ def _mlp_dev(prob):
                     pd=c(prob.packed_down), ld=c(prob.lut_down.view(np.int16)))
 
 
-@pytest.mark.parametrize("tile_m", [16, 64])
-def test_mlp_tiny_all_outputs(tile_m):
+@pytest.mark.parametrize("tile_m,pin", [(16, tq.ARM_GROUPED), (64, tq.ARM_GROUPED), (16, tq.ARM_GEMV)])
+def test_mlp_tiny_all_outputs(tile_m, pin):
     prob = moe_inputs.make_mlp_problem("tiny_mlp_e8_k2_n16")
     d = _mlp_dev(prob)
-    y = tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"], tile_m=tile_m)
+    before = tq.tq_launch_counts()
+    y, arm = tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"], tile_m=tile_m,
+                                   pin=pin)
     check_no_device_error()
+    after = tq.tq_launch_counts()
+    assert arm == pin
+    ran = "grouped" if pin == tq.ARM_GROUPED else "gemv"
+    assert after[ran] == before[ran] + 2     # gate|up and down
     ref = O.moe_mlp(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed_gu, prob.lut_gu, prob.packed_down,
                     prob.lut_down, prob.L)
     assert normwise(y.float().cpu().numpy(), ref) <= TOL
 
 
-def test_mlp_v4_n32_sampled_tokens():
+@pytest.mark.parametrize("pin", [tq.ARM_GROUPED, tq.ARM_GEMV])
+def test_mlp_v4_n32_sampled_tokens(pin):
     prob = moe_inputs.make_mlp_problem("v4_mlp_n32")
     d = _mlp_dev(prob)
-    y = tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"], tile_m=16)
+    y, arm = tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"], tile_m=16,
+                                   pin=pin)
     check_no_device_error()
+    assert arm == pin
     tokens = [0, 17, 31]
     ref = O.moe_mlp(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed_gu, prob.lut_gu, prob.packed_down,
                     prob.lut_down, prob.L, tokens=tokens)
@@ -60,8 +69,9 @@ def test_mlp_prefill_native_tile_sampled_tokens():
     walk; three tokens against the oracle."""
     prob = moe_inputs.make_mlp_problem("v4_mlp_prefill_n8192")
     d = _mlp_dev(prob)
-    y = tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"],
-                              tile_m=tq.TILE_NATIVE)
+    y, arm = tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"],
+                                   tile_m=tq.TILE_NATIVE)
+    assert arm == tq.ARM_GROUPED     # 8192 tokens: the first page's predicate picks the grouped arm
     check_no_device_error()
     tokens = [370, 1221, 2109]    # three tokens sharing most of their 9 experts (keeps the oracle short)
     ref = O.moe_mlp(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed_gu, prob.lut_gu, prob.packed_down,

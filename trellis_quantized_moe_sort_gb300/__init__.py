@@ -67,7 +67,7 @@ _SIGS = {
     "tq_swiglu": (_c_int, [_c_p, _c_i64, _c_int, _c_p, _c_p]),
     "tq_moe_mlp_workspace_size": (_c_sz, [_c_i64, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "tq_moe_mlp_forward": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int, _c_int,
-                                    _c_int, _c_int, _c_p, _c_sz, _c_p, _c_p]),
+                                    _c_int, _c_int, _c_int, _c_p, _c_sz, _c_p, ctypes.POINTER(_c_int), _c_p]),
     "tq_dequantize": (_c_int, [_c_p, _c_p, _c_int, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p]),
     "tq_grouped_gemm_dense": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_int, _c_int, _c_int,
                                        _c_int, _c_int, _c_p, _c_p]),
@@ -443,8 +443,8 @@ def tq_moe_mlp_workspace_size(n: int, top_k: int, E: int, H: int, I: int, tile_m
 
 
 def tq_moe_mlp_forward(x, packed_gu, lut_gu, packed_down, lut_down, topk_ids, topk_w, tile_m: int = 16,
-                       workspace=None, y=None, stream=None):
-    """Whole SwiGLU expert MLP -> y bf16 [n, H]."""
+                       pin: int = ARM_AUTO, workspace=None, y=None, stream=None):
+    """Whole SwiGLU expert MLP -> (y bf16 [n, H], arm used)."""
     torch = _torch()
     n, H = x.shape
     E, I2, hb = packed_gu.shape
@@ -458,15 +458,17 @@ def tq_moe_mlp_forward(x, packed_gu, lut_gu, packed_down, lut_down, topk_ids, to
     need = tq_moe_mlp_workspace_size(n, top_k, E, H, I, tile_m)
     workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device) if workspace is None else workspace
     y = torch.empty((n, H), dtype=torch.bfloat16, device=x.device) if y is None else y
+    arm = ctypes.c_int(-1)
     _check(lib().tq_moe_mlp_forward(_dev_ptr(x, _bits16(), "x"), _dev_ptr(packed_gu, (torch.uint8,), "packed_gu"),
                                     _dev_ptr(lut_gu, _bits16(), "lut_gu"),
                                     _dev_ptr(packed_down, (torch.uint8,), "packed_down"),
                                     _dev_ptr(lut_down, _bits16(), "lut_down"), L,
                                     _dev_ptr(topk_ids, (torch.int32,), "topk_ids"),
                                     _dev_ptr(topk_w, (torch.float32,), "topk_w"), n, top_k, E, H, I, tile_m,
-                                    _dev_ptr(workspace, (torch.uint8,), "workspace"), workspace.numel(),
-                                    _dev_ptr(y, _bits16(), "y"), _stream(stream)), "tq_moe_mlp_forward")
-    return y
+                                    pin, _dev_ptr(workspace, (torch.uint8,), "workspace"), workspace.numel(),
+                                    _dev_ptr(y, _bits16(), "y"), ctypes.byref(arm), _stream(stream)),
+           "tq_moe_mlp_forward")
+    return y, arm.value
 
 
 def tq_swiglu(gate_up, h=None, stream=None):

@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
             const uint16_t* __restrict__ lut, const int32_t* __restrict__ topk_ids,
             const float* __restrict__ topk_w, int P, int top_k, int E, int K, int N, int x_in_smem,
-            float* __restrict__ y32, int* err) {
+            int pair_in, int pair_out, float* __restrict__ y32, int* err) {
   extern __shared__ __align__(16) uint16_t lut_s[];
   constexpr int kEntries = 1 << L;
   constexpr int kLutBytes = (kEntries * 2 + 15) & ~15;
@@ -50,11 +50,12 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
   // LUT), so a warp that moves to another pair refills its registers from
   // shared memory instead of waiting on global memory.
   const int n_tok = P / top_k;
+  const int x_rows = pair_in ? P : n_tok;   // x is per pair (sorted by pair id) or per token
   uint4* xs = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(lut_s) + kLutBytes);
   if (x_in_smem) {
     // 16-byte piece v of 128-byte chunk c goes to piece v ^ (c & 7) of the chunk
     const uint32_t xs_base = smem_u32(xs);
-    const int pieces = n_tok * K / 8;
+    const int pieces = x_rows * K / 8;
     for (int q = threadIdx.x; q < pieces; q += THREADS) {
       const int g = q >> 3, v = q & 7;   // global chunk (8 pieces each; K is a multiple of 64)
       const int c = g % (K / kChunkSyms);  // chunk within its token: the reader's swizzle key
@@ -101,11 +102,11 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
     const int r = static_cast<int>(it - static_cast<long long>(pair) * N);
     if (pair != cur_pair) {
       cur_pair = pair;
-      tok = pair / top_k;
+      tok = pair_in ? pair : pair / top_k;   // the row of x this pair multiplies
       const int e = __ldg(topk_ids + pair);
       pair_ok = e >= 0 && e < E;
       if (!pair_ok && lane == 0 && (r == 0 || it == i0)) record_error(err, TQ_ERR_INVALID_ARG, kWhereRoute);
-      wt = __ldg(topk_w + pair);
+      wt = pair_out ? 1.f : __ldg(topk_w + pair);   // per-pair outputs carry no router weight
       // activations of this token: chunk c = lane + 32 i, 64 bf16 = 32 words
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
@@ -160,7 +161,12 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) atomicAdd(y32 + static_cast<size_t>(tok) * N + r, acc * wt);
+    if (lane == 0) {
+      if (pair_out)
+        y32[static_cast<size_t>(pair) * N + r] = acc;   // one writer per (pair, row)
+      else
+        atomicAdd(y32 + static_cast<size_t>(pair / top_k) * N + r, acc * wt);
+    }
   };
 
   // The next row's bytes are in flight while this row decodes (two register
@@ -179,11 +185,11 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
 template <int L, int CPL>
 int launch_one(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, const int32_t* ids,
                const float* w, int P, int top_k, int E, int K, int N, float* y32, int* err,
-               cudaStream_t s) {
+               cudaStream_t s, int pair_in, int pair_out) {
   constexpr int kThreads = (CPL >= 4) ? 256 : 512;
   auto kfn = gemv_kernel<L, CPL, kThreads>;
   const size_t lut_bytes = ((sizeof(uint16_t) << L) + 15) & ~static_cast<size_t>(15);
-  const size_t x_bytes = static_cast<size_t>(P / top_k) * K * 2;
+  const size_t x_bytes = static_cast<size_t>(pair_in ? P : P / top_k) * K * 2;
   // activations go to shared memory when they fit beside the LUT (small batches)
   const int x_in_smem = (lut_bytes + x_bytes <= 200u * 1024u) ? 1 : 0;
   const size_t smem = std::max<size_t>(16, lut_bytes + (x_in_smem ? x_bytes : 0));
@@ -195,37 +201,38 @@ int launch_one(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, co
   const int sms = sm_count();
   const long long items = static_cast<long long>(P) * N;
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(sms, (items + kThreads / 32 - 1) / (kThreads / 32))));
-  kfn<<<grid, kThreads, smem, s>>>(x, packed, lut, ids, w, P, top_k, E, K, N, x_in_smem, y32, err);
+  kfn<<<grid, kThreads, smem, s>>>(x, packed, lut, ids, w, P, top_k, E, K, N, x_in_smem, pair_in, pair_out, y32,
+                                   err);
   return launch_status();
 }
 
 template <int L>
 int launch_L(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, const int32_t* ids,
              const float* w, int P, int top_k, int E, int K, int N, float* y32, int* err,
-             cudaStream_t s) {
+             cudaStream_t s, int pi, int po) {
   const int nchunks = K / kChunkSyms;
-  if (nchunks <= 32) return launch_one<L, 1>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s);
-  if (nchunks <= 64) return launch_one<L, 2>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s);
-  return launch_one<L, 4>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s);
+  if (nchunks <= 32) return launch_one<L, 1>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s, pi, po);
+  if (nchunks <= 64) return launch_one<L, 2>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s, pi, po);
+  return launch_one<L, 4>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s, pi, po);
 }
 
 }  // namespace
 
 int launch_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
                 const int32_t* topk_ids, const float* topk_w, int64_t n, int top_k, int E, int K,
-                int N, float* y32, int* err, cudaStream_t s) {
+                int N, float* y32, int* err, cudaStream_t s, int pair_in, int pair_out) {
   const int P = static_cast<int>(n * top_k);
   if (P == 0) return TQ_OK;
   int st;
   switch (L) {
-    case 2: st = launch_L<2>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
-    case 4: st = launch_L<4>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
-    case 6: st = launch_L<6>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
-    case 8: st = launch_L<8>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
-    case 10: st = launch_L<10>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
-    case 12: st = launch_L<12>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
-    case 14: st = launch_L<14>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
-    case 16: st = launch_L<16>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s); break;
+    case 2: st = launch_L<2>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
+    case 4: st = launch_L<4>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
+    case 6: st = launch_L<6>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
+    case 8: st = launch_L<8>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
+    case 10: st = launch_L<10>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
+    case 12: st = launch_L<12>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
+    case 14: st = launch_L<14>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
+    case 16: st = launch_L<16>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
     default: return TQ_ERR_INVALID_ARG;
   }
   if (st == TQ_OK) count_launch(kCntGemv);

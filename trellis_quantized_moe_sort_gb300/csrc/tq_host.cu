@@ -190,6 +190,20 @@ MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K
   return m;
 }
 
+int env_pin(int pin) {
+  if (pin != TQ_ARM_AUTO) return pin;
+  const char* v = std::getenv("TQ_FORCE_ARM");
+  if (!v || !*v || !std::strcmp(v, "auto")) return TQ_ARM_AUTO;
+  if (!std::strcmp(v, "gemv")) return TQ_ARM_GEMV;
+  if (!std::strcmp(v, "grouped")) return TQ_ARM_GROUPED;
+  if (!std::strcmp(v, "measured")) return TQ_ARM_MEASURED;
+  static std::once_flag warned;
+  std::call_once(warned, [v] {
+    std::fprintf(stderr, "tqmoe: unknown TQ_FORCE_ARM=%s (expected auto|gemv|grouped|measured); keeping auto\n", v);
+  });
+  return TQ_ARM_AUTO;
+}
+
 }  // namespace tq
 
 using namespace tq;
@@ -440,19 +454,6 @@ size_t tq_moe_workspace_size(int64_t n, int top_k, int E, int K, int N, int tile
   return b;
 }
 
-static int env_pin(int pin) {
-  if (pin != TQ_ARM_AUTO) return pin;
-  const char* v = std::getenv("TQ_FORCE_ARM");
-  if (!v || !*v || !std::strcmp(v, "auto")) return TQ_ARM_AUTO;
-  if (!std::strcmp(v, "gemv")) return TQ_ARM_GEMV;
-  if (!std::strcmp(v, "grouped")) return TQ_ARM_GROUPED;
-  if (!std::strcmp(v, "measured")) return TQ_ARM_MEASURED;
-  static std::once_flag warned;
-  std::call_once(warned, [v] {
-    std::fprintf(stderr, "tqmoe: unknown TQ_FORCE_ARM=%s (expected auto|gemv|grouped|measured); keeping auto\n", v);
-  });
-  return TQ_ARM_AUTO;
-}
 
 int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L, const int32_t* topk_ids,
                    const float* topk_w, int64_t n, int top_k, int E, int K, int N, int tile_m, int pin,

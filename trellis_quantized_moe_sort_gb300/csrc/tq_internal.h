@@ -97,8 +97,13 @@ MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K
 // the selection).  Returns false on an invalid value.
 bool resolve_tile(int64_t n, int top_k, int E, int tile_m, int* kernel_tile, int* gate_tile);
 int launch_swiglu(const float* gate_up, int64_t P, int I, uint16_t* h, cudaStream_t s);
+// pair_in: x holds one row per pair (x[pair]) instead of per token;
+// pair_out: out[pair][row] = the row's dot product (plain store, no router
+// weight) instead of y32[token][row] += w * dot.
 int launch_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
                 const int32_t* topk_ids, const float* topk_w, int64_t n, int top_k, int E, int K,
-                int N, float* y32, int* err, cudaStream_t s);
+                int N, float* y32, int* err, cudaStream_t s, int pair_in = 0, int pair_out = 0);
+// TQ_FORCE_ARM (auto|gemv|grouped|measured) applied to an automatic pin.
+int env_pin(int pin);
 
 }  // namespace tq

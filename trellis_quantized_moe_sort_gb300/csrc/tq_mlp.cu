@@ -114,13 +114,14 @@ size_t tq_moe_mlp_workspace_size(int64_t n, int top_k, int E, int H, int I, int 
 
 int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16_t* lut_gu,
                        const uint8_t* packed_down, const uint16_t* lut_down, int L, const int32_t* topk_ids,
-                       const float* topk_w, int64_t n, int top_k, int E, int H, int I, int tile_m,
-                       void* workspace, size_t workspace_bytes, uint16_t* y, tq_stream_t stream) {
+                       const float* topk_w, int64_t n, int top_k, int E, int H, int I, int tile_m, int pin,
+                       void* workspace, size_t workspace_bytes, uint16_t* y, int* arm_used, tq_stream_t stream) {
   const int tile_arg = tile_m;
   int gate_tile = 0;
   if (E < 1 || E > 1024 || top_k < 1 || top_k > E || n < 0) return TQ_ERR_INVALID_ARG;
   if (!resolve_tile(n, top_k, E, tile_arg, &tile_m, &gate_tile)) return TQ_ERR_INVALID_ARG;
-  (void)gate_tile;   // the MLP runs the grouped arm only
+  const int arm = tq_select_arm(n, top_k, E, gate_tile, env_pin(pin));
+  if (arm < 0) return arm;
   if (H < 128 || H % 128 != 0 || I < 64 || I % 64 != 0 || (2 * I) % 128 != 0) return TQ_ERR_INVALID_ARG;
   if (L < 2 || L > 16 || (L & 1)) return TQ_ERR_INVALID_ARG;
   if (n * top_k >= (1ll << 31)) return TQ_ERR_INVALID_ARG;
@@ -132,9 +133,11 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
   const size_t need = tq_moe_mlp_workspace_size(n, top_k, E, H, I, tile_arg);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return TQ_ERR_WORKSPACE;
+  if (arm == TQ_ARM_GEMV && (H > 8192 || I > 8192)) return TQ_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int rc = require_sm103(s);
   if (rc != TQ_OK) return rc;
+  if (arm_used) *arm_used = arm;
   if (n == 0) return TQ_OK;
   int* err = error_word(&rc);
   if (!err) return rc;
@@ -152,6 +155,22 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
   uint16_t* h = reinterpret_cast<uint16_t*>(w);         w += align256(sizeof(uint16_t) * P * I);
   float* y32 = reinterpret_cast<float*>(w);
 
+  if (arm == TQ_ARM_GEMV) {
+    // per-pair GEMVs: gate|up per pair (plain stores), SwiGLU, down per pair
+    // with the router weights into y32 (no routing sort, no tile map)
+    if (cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(n) * H, s) != cudaSuccess) {
+      cudaGetLastError();
+      return TQ_ERR_CUDA;
+    }
+    rc = launch_gemv(x, packed_gu, lut_gu, L, topk_ids, nullptr, n, top_k, E, H, 2 * I, gate_up, err, s,
+                     /*pair_in=*/0, /*pair_out=*/1);
+    if (rc == TQ_OK) rc = launch_swiglu(gate_up, static_cast<int64_t>(P), I, h, s);
+    if (rc == TQ_OK)
+      rc = launch_gemv(h, packed_down, lut_down, L, topk_ids, topk_w, n, top_k, E, I, H, y32, err, s,
+                       /*pair_in=*/1, /*pair_out=*/0);
+    if (rc == TQ_OK) rc = launch_combine(y32, y, static_cast<int64_t>(n) * H, s);
+    return rc;
+  }
   rc = launch_route_tile_map(topk_ids, static_cast<int>(P), E, tile_m, counts, offsets, sorted_pairs, tiles,
                              num_tiles, cap, err, s);
   if (rc == TQ_OK)
