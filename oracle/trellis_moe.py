@@ -15,7 +15,7 @@ states the passage it follows.  Page titles used in the citations:
   "The two changes" (packed 2-bit bytes cross HBM; decode fused into the
   multiply).
 
-Readings where the pages leave a step open (the same list is in the design doc):
+Readings where the pages leave a step open:
 
 R1  Bitstream.  Each (expert e, output row r) owns one stream of K 2-bit
     symbols; symbol j is bits [2(j%4), 2(j%4)+2) of byte j//4 of the row
