@@ -185,18 +185,24 @@ def run_ours(args, rank, world, dist):
     num_tiles = torch.empty(1, dtype=torch.int32, device="cuda")
     y32 = torch.empty((n, N), dtype=torch.float32, device="cuda")
     y = torch.empty((n, N), dtype=torch.bfloat16, device="cuda")
-    x_sorted = torch.empty((P, K), dtype=torch.int16, device="cuda")
     stream = torch.cuda.current_stream()
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
 
+    # the activation layout tq_moe_forward uses for this m-tile: token rows
+    # gathered by the kernel, or a pair-sorted copy made by the prepare launch
+    lay = tq.X_TOKENS if T <= tq.GATHER_MAX_TILE_M else tq.X_PAIR_SORTED
+    x_sorted = None if lay == tq.X_TOKENS else torch.empty((P, K), dtype=torch.int16, device="cuda")
+
     def step(i, timed_slot=None):
         s = sets[i % args.weight_sets]
-        # route + tile map (one launch), gather clearing y32 (one launch)
+        # route + tile map clearing y32 (one launch), and for large m-tiles the
+        # pair-sorted copy of x (a second launch)
         tq.tq_prepare(s["ids"], s["x"], E, T, cap, counts, offsets, sorted_pairs, tiles, num_tiles, x_sorted, y32)
         if timed_slot is not None:
             gev[timed_slot][0].record(stream)
-        tq.tq_grouped_gemm(x_sorted, s["packed"], s["lut"], sorted_pairs, s["w"], tiles, num_tiles, k, T, y32)
+        tq.tq_grouped_gemm(s["x"] if x_sorted is None else x_sorted, s["packed"], s["lut"], sorted_pairs, s["w"],
+                           tiles, num_tiles, k, T, y32, x_layout=lay)
         if timed_slot is not None:
             gev[timed_slot][1].record(stream)
         tq.tq_combine(y32, y)
@@ -447,26 +453,33 @@ def run_sweep(args):
             return float(np.median(ts))
 
         tiles_list = [int(t) for t in args.sweep_tiles.split(",")]
-        arms = [("grouped", T) for T in tiles_list]
+        auto_layout = lambda T: tq.X_TOKENS if T <= tq.GATHER_MAX_TILE_M else tq.X_PAIR_SORTED
+        layouts = (lambda T: (tq.X_TOKENS, tq.X_PAIR_SORTED)) if args.sweep_both_layouts else \
+            (lambda T: (auto_layout(T),))
+        arms = [("grouped", T, lay) for T in tiles_list for lay in layouts(T)]
         if s.n <= 1024 and not args.sweep_no_gemv:
-            arms.append(("gemv", None))
+            arms.append(("gemv", None, None))
         if args.sweep_dequant:
-            arms += [("dequant", T) for T in tiles_list]
+            arms += [("dequant", T, auto_layout(T)) for T in tiles_list]
         w_dense = None
-        for arm, T in arms:
+        for arm, T, lay in arms:
             extra = {}
             if arm == "grouped":
                 _, offsets, sp = tq.tq_route(d["ids"], s.E)
                 cap = tq.tq_tile_map_capacity(s.n, s.top_k, s.E, T)
                 tiles, nt = tq.tq_build_tile_map(offsets, T, cap)
-                xs = tq.tq_gather_rows(d["x"], sp, s.top_k)
+                xin = d["x"]
+                if lay == tq.X_PAIR_SORTED:
+                    # the pair-sorted copy (one pass) the kernel then reads with box copies
+                    xin = tq.tq_gather_rows(d["x"], sp, s.top_k)
+                    extra["gather_us"] = round(timed(lambda: tq.tq_gather_rows(d["x"], sp, s.top_k, xin)), 1)
                 torch.cuda.synchronize()
                 ntiles = int(nt.item())
-                gather_us = timed(lambda: tq.tq_gather_rows(d["x"], sp, s.top_k, xs))
-                us = timed(lambda: tq.tq_grouped_gemm(xs, d["packed"], d["lut"], sp, d["w"], tiles, nt,
-                                                       s.top_k, T, y32))
-                call = lambda: tq.tq_grouped_gemm(xs, d["packed"], d["lut"], sp, d["w"], tiles, nt, s.top_k, T, y32)
-                extra = {"hot_l2_us": round(timed(call, flush_l2=False), 1)}
+                call = lambda: tq.tq_grouped_gemm(xin, d["packed"], d["lut"], sp, d["w"], tiles, nt, s.top_k, T, y32,
+                                                  x_layout=lay)
+                us = timed(call)
+                extra["x_layout"] = "tokens" if lay == tq.X_TOKENS else "pair_sorted"
+                extra["hot_l2_us"] = round(timed(call, flush_l2=False), 1)
                 # host cost of one call (Python binding + C ABI + launch), GPU kept busy
                 torch.cuda.synchronize()
                 flush.zero_()
@@ -483,7 +496,7 @@ def run_sweep(args):
                 _, offsets, sp = tq.tq_route(d["ids"], s.E)
                 cap = tq.tq_tile_map_capacity(s.n, s.top_k, s.E, T)
                 tiles, nt = tq.tq_build_tile_map(offsets, T, cap)
-                xs = tq.tq_gather_rows(d["x"], sp, s.top_k)
+                xin = d["x"] if lay == tq.X_TOKENS else tq.tq_gather_rows(d["x"], sp, s.top_k)
                 woken_ids = np.unique(prob.topk_ids)
                 ids = np.full(s.E, -1, dtype=np.int32)
                 ids[woken_ids] = woken_ids
@@ -492,9 +505,9 @@ def run_sweep(args):
                     w_dense = torch.empty((s.E, s.N, s.K), dtype=torch.bfloat16, device="cuda")
                 torch.cuda.synchronize()
                 ntiles = int(nt.item())
-                gather_us = timed(lambda: tq.tq_gather_rows(d["x"], sp, s.top_k, xs))
                 deq_us = timed(lambda: tq.tq_dequantize(d["packed"], d["lut"], expert_ids=ids_d, w_out=w_dense))
-                gemm_us = timed(lambda: tq.tq_grouped_gemm_dense(xs, w_dense, sp, d["w"], tiles, nt, s.top_k, T, y32))
+                gemm_us = timed(lambda: tq.tq_grouped_gemm_dense(xin, w_dense, sp, d["w"], tiles, nt, s.top_k, T,
+                                                                 y32, x_layout=lay))
                 us = deq_us + gemm_us
                 staged = ntiles * s.N * s.K // 4
                 mat = len(woken_ids) * s.N * s.K * 2
@@ -505,7 +518,6 @@ def run_sweep(args):
             else:
                 us = timed(lambda: tq.tq_gemv(d["x"], d["packed"], d["lut"], d["ids"], d["w"], y32))
                 ntiles = None
-                gather_us = None
                 staged = s.pairs * s.N * s.K // 4
             code, where = tq.tq_device_error()
             if code:
@@ -525,7 +537,7 @@ def run_sweep(args):
             extra["native_tile_m"] = tq.tq_native_tile_m(s.n, s.top_k, s.E)
             print(json.dumps({**extra, 
                 "workload": name, "arm": arm, "tile_m": T, "n": s.n, "pairs": s.pairs, "woken": woken,
-                "m_tiles": ntiles, "us": round(us, 1), "gather_us": gather_us, "pairs_per_s": round(s.pairs / (us * 1e-6), 1),
+                "m_tiles": ntiles, "us": round(us, 1), "pairs_per_s": round(s.pairs / (us * 1e-6), 1),
                 "staged_packed_GBps": round(staged / (us * 1e-6) / 1e9, 1),
                 "roofline_us": round(max(t_hbm, t_tc), 1), "bound": "hbm" if t_hbm >= t_tc else "tensor",
                 "frac": round(max(t_hbm, t_tc) / us, 4),
@@ -595,15 +607,13 @@ def run_gate_study(args):
             _, offsets, sp = tq.tq_route(ids, s.E)
             cap = tq.tq_tile_map_capacity(n, s.top_k, s.E, T)
             tiles, nt = tq.tq_build_tile_map(offsets, T, cap)
-            xs = tq.tq_gather_rows(x, sp, s.top_k)
 
             counts = torch.empty(s.E, dtype=torch.int32, device="cuda")
 
-            def whole():  # route + tile map + gather + grouped GEMM (the arm's full device work)
+            def whole():  # route + tile map + grouped GEMM (the arm's full device work)
                 tq.tq_route(ids, s.E, counts, offsets, sp)
                 tq.tq_build_tile_map(offsets, T, cap, tiles, nt)
-                tq.tq_gather_rows(x, sp, s.top_k, xs)
-                tq.tq_grouped_gemm(xs, packed, lut, sp, w, tiles, nt, s.top_k, T, y32)
+                tq.tq_grouped_gemm(x, packed, lut, sp, w, tiles, nt, s.top_k, T, y32)
             row[f"grouped_T{T}_us"] = round(timed(whole), 1)
         code, where = tq.tq_device_error()
         if code:
@@ -692,6 +702,9 @@ def main(argv=None):
     ap.add_argument("--sweep-workloads", default="", help="comma-separated subset for --sweep")
     ap.add_argument("--sweep-tiles", default="16,128", help="TILE_M values for --sweep")
     ap.add_argument("--sweep-no-gemv", action="store_true", help="skip the GEMV arm in --sweep")
+    ap.add_argument("--sweep-both-layouts", action="store_true",
+                    help="time the grouped kernel on token rows (gathered in the kernel) and on the pair-sorted "
+                         "copy at every TILE_M (default: the layout the whole-product calls use)")
     ap.add_argument("--sweep-dequant", action="store_true",
                     help="add the dequantize-materialize comparator (dense bf16 experts + the same grouped GEMM) to --sweep")
     ap.add_argument("--gate-study", action="store_true", help="both arms across token counts (V4 up shape)")

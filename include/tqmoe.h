@@ -115,14 +115,17 @@ int tq_tiles_amortize(int64_t n, int top_k, int E, int tile_m);
  * tile_m 16).  Negative TQ_ERR_INVALID_ARG on invalid arguments. */
 int64_t tq_grouped_min_tokens(int top_k, int E, int tile_m);
 
-/* Native m-tile size of the grouped kernel on sm_103a for a routing shape:
- * 256 when the expected pairs per woken expert reach 128 (prefill sizes, where
- * one decode per 256 pairs beats one per 128), else 128 (measured equal to or
- * faster than smaller tiles at every decode size: the kernel pads a tile's
- * pairs to the MMA's N, so small tiles save nothing and decode more).  The
- * whole-product calls below take tile_m = TQ_TILE_NATIVE to use it: their
- * kernels then run with this tile while the arm selection keeps the pages'
- * TILE_M (TQ_GATE_TILE_M).  Negative on invalid arguments. */
+/* Native m-tile size of the grouped kernel on sm_103a for a routing shape,
+ * by the expected pairs per woken expert (ppw, tq_pairs_per_woken_expert):
+ * 256 when ppw >= 128 (prefill sizes, where one decode per 256 pairs beats
+ * one per 128); 16 when ppw <= 4 (almost no expert has more than 16 pairs,
+ * so the m-tiles are the woken experts either way, and at 16 the kernel
+ * gathers the token rows itself, saving the pair-sorted copy); else 128
+ * (fewer m-tiles, hence fewer decodes, than 16 once experts share more
+ * pairs).  Measured on GB300 at 32, 128, 512, 1024 and 8192 tokens of top-6
+ * of 256.  The whole-product calls below take tile_m = TQ_TILE_NATIVE to use
+ * it: their kernels then run with this tile while the arm selection keeps the
+ * pages' TILE_M (TQ_GATE_TILE_M).  Negative on invalid arguments. */
 #define TQ_TILE_NATIVE 0
 #define TQ_GATE_TILE_M 16
 int tq_native_tile_m(int64_t n, int top_k, int E);
@@ -205,7 +208,8 @@ int tq_build_tile_map(const int32_t* offsets, int E, int tile_m,
 
 /* ---------------------------------------------------------------------------
  * Activation gather: x_sorted[s][:] = x[sorted_pairs[s] / top_k][:] for every
- * sorted slot s < n*top_k, so that the rows of an m-tile are consecutive.
+ * sorted slot s < n*top_k, so that the rows of an m-tile are consecutive
+ * (TQ_X_PAIR_SORTED input of tq_grouped_gemm; tq_grouped_gemm_pairs input).
  * x (device) bf16 [n][K]; x_sorted (device) bf16 [n*top_k][K]; both 16-byte
  * aligned; K % 8 == 0.  A pair id out of range gives a zero row and sets
  * TQ_ERR_INVALID_ARG in the device error word.
@@ -214,14 +218,15 @@ int tq_gather_rows(const uint16_t* x, const int32_t* sorted_pairs, int64_t n, in
                    uint16_t* x_sorted, tq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
- * Everything the grouped GEMM needs, in two launches: tq_route and
- * tq_build_tile_map fused into one single-block kernel (the tile map takes
- * each expert's slot range from the sort's registers), then tq_gather_rows,
- * which also clears y32[0 .. y32_count) (the fp32 accumulator; 16-byte
- * aligned and y32_count % 4 == 0 for the fused clear, otherwise it is
- * cleared by a separate memset).  Results are those of the three calls.
- * Arguments as in tq_route, tq_build_tile_map and tq_gather_rows; y32 may be
- * NULL when y32_count == 0.
+ * Everything the grouped GEMM needs, in one launch: tq_route and
+ * tq_build_tile_map fused (one block sorts; the tile map takes each expert's
+ * slot range from the sort's registers) while the launch's other blocks
+ * clear y32[0 .. y32_count) (the fp32 accumulator; 16-byte aligned and
+ * y32_count % 4 == 0 for the fused clear, otherwise it is cleared by a
+ * separate memset).  x_sorted may be NULL: when given, tq_gather_rows also
+ * runs (a second launch; x is unused otherwise).  Results are those of the separate calls.  Arguments as in
+ * tq_route, tq_build_tile_map and tq_gather_rows; y32 may be NULL when
+ * y32_count == 0.
  * ------------------------------------------------------------------------- */
 int tq_prepare(const int32_t* topk_ids, const uint16_t* x, int64_t n, int top_k, int E, int K, int tile_m,
                int32_t* counts, int32_t* offsets, int32_t* sorted_pairs, int32_t* tiles, int32_t* num_tiles,
@@ -233,12 +238,20 @@ int tq_prepare(const int32_t* topk_ids, const uint16_t* x, int64_t n, int top_k,
  *
  * For every m-tile and every 128-row block of N: TMA stages the expert's
  * packed rows once, warps decode runs of 32 symbols (seeded by the window
- * identity, then stepped) into a bf16 weight tile in tensor memory, tcgen05
- * MMAs contract it with the tile's gathered activations (fp32 accumulate),
- * and the epilogue scales by the router weight and adds into y32.
+ * identity, then stepped) into a bf16 weight tile in tensor memory, TMA
+ * copies the tile's activation rows into shared memory, tcgen05 MMAs
+ * contract the two (fp32 accumulate), and the epilogue scales by the router
+ * weight and adds into y32.
  *
- * x_sorted   (device) bf16 [n*top_k][K], the pair-sorted activations from
- *            tq_gather_rows with the same sorted_pairs; 16-byte aligned.
+ * x_layout   TQ_X_TOKENS: x (device) bf16 [n][K], the token activations; the
+ *            kernel gathers row sorted_pairs[slot] / top_k of each m-tile
+ *            slot, four rows per copy.  TQ_X_PAIR_SORTED: x (device) bf16
+ *            [n*top_k][K] from tq_gather_rows (row = sorted slot), one box
+ *            copy per m-tile and k-step.  Results are identical; the row
+ *            gathers cost one copy per four pairs, so for m-tiles above
+ *            TQ_GATHER_MAX_TILE_M the separate tq_gather_rows pass is faster
+ *            (the whole-product calls choose by that rule).
+ * x          16-byte aligned.
  * packed     (device) uint8 [E][N][K/4]; 16-byte aligned.
  * lut        (device) fp16 [2^L] (converted to bf16, nearest-even, on chip).
  * sorted_pairs, tiles, num_tiles: from tq_route / tq_build_tile_map with the
@@ -250,7 +263,10 @@ int tq_prepare(const int32_t* topk_ids, const uint16_t* x, int64_t n, int top_k,
  * Requires: K % 64 == 0, N % 128 == 0, L even in [2, 16], 1 <= tile_m <= 256,
  * 1 <= top_k <= E.  Device: compute capability 10.3.
  * ------------------------------------------------------------------------- */
-int tq_grouped_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
+#define TQ_X_TOKENS 0
+#define TQ_X_PAIR_SORTED 1
+#define TQ_GATHER_MAX_TILE_M 16
+int tq_grouped_gemm(const uint16_t* x, int x_layout, const uint8_t* packed, const uint16_t* lut, int L,
                     const int32_t* sorted_pairs, const float* topk_w,
                     const int32_t* tiles, const int32_t* num_tiles, int64_t cap,
                     int64_t n, int top_k, int E, int K, int N, int tile_m,
@@ -283,8 +299,8 @@ int tq_combine(const float* y32, uint16_t* y, int64_t count, tq_stream_t stream)
  * workspace (device): caller-owned scratch of at least
  *   tq_moe_workspace_size(n, top_k, E, K, N, tile_m) bytes, 256-byte aligned.
  *   It holds counts, offsets, sorted pairs, the tile map, the fp32
- *   accumulator and the pair-sorted activations; its contents are undefined
- *   after the call.
+ *   accumulator and, for a kernel m-tile above TQ_GATHER_MAX_TILE_M, the
+ *   pair-sorted activations; its contents are undefined after the call.
  * tile_m: 1..256, the m-tile of both the arm selection and the kernel, or
  *   TQ_TILE_NATIVE (tq_native_tile_m for the kernel, TQ_GATE_TILE_M for the
  *   selection).
@@ -312,7 +328,7 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
  * TQ_STATIC_SCRATCH_BYTES (16 MiB) that every GPU loading this library holds
  * until the process exits; a shape whose tq_moe_workspace_size() exceeds it
  * is rejected with TQ_ERR_WORKSPACE before anything is launched (at
- * K = 4096, N = 2048, top-6 that is about n > 290 tokens).  The call allocates nothing (no cudaMalloc,
+ * K = 4096, N = 2048, top-6 that is n > 2040 tokens).  The call allocates nothing (no cudaMalloc,
  * no cudaFree, no allocating library routine).
  *
  * The first call on a device looks up the array's device address with that
@@ -345,8 +361,10 @@ int tq_moe_forward_static(const uint16_t* x, const uint8_t* packed, const uint16
  *   [P][I]; I % 4 == 0.
  * tq_moe_mlp_forward: the arm chosen as in tq_moe_forward (tq_select_arm with
  *   `pin`, the gate's TILE_M from `tile_m`; arm_used (host, may be NULL)
- *   receives it).  Grouped arm: route + tile map, gather, gate|up (per pair),
- *   SwiGLU, down (combined per token with the router weights).  GEMV arm:
+ *   receives it).  Grouped arm: route + tile map, gate|up (per pair; token
+ *   rows gathered in the kernel, or by tq_gather_rows above
+ *   TQ_GATHER_MAX_TILE_M), SwiGLU, down (combined per token with the router
+ *   weights).  GEMV arm:
  *   gate|up by per-pair GEMVs, SwiGLU, down by per-pair GEMVs on h combined
  *   per token.  Output bf16 y [n][H].  H % 128 == 0, I % 64 == 0 (and
  *   H, I <= 8192 for the GEMV arm).  workspace (device) >=
@@ -383,8 +401,9 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
  *   4096 x 2048).
  * tq_grouped_gemm_dense: tq_grouped_gemm with dense bf16 weights
  *   w_dense (device) [E][N][K] (16-byte aligned) in place of packed + lut;
- *   same m-tiles, MMA and epilogue (y32 += w * W_e x).
- * tq_moe_forward_dequant: zero y32, route, tile map, gather, dequantize every
+ *   same m-tiles, activation layouts (x, x_layout), MMA and epilogue
+ *   (y32 += w * W_e x).
+ * tq_moe_forward_dequant: zero y32, route, tile map, dequantize every
  *   expert with at least one pair into slot e of an [E][N][K] bf16 buffer in
  *   the workspace, tq_grouped_gemm_dense, combine to bf16 y [n][N].
  *   workspace (device) >= tq_moe_dequant_workspace_size(...) bytes (the
@@ -393,7 +412,7 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
  * ------------------------------------------------------------------------- */
 int tq_dequantize(const uint8_t* packed, const uint16_t* lut, int L, const int32_t* expert_ids, int m,
                   int E, int N, int K, uint16_t* w_out, tq_stream_t stream);
-int tq_grouped_gemm_dense(const uint16_t* x_sorted, const uint16_t* w_dense, const int32_t* sorted_pairs,
+int tq_grouped_gemm_dense(const uint16_t* x, int x_layout, const uint16_t* w_dense, const int32_t* sorted_pairs,
                           const float* topk_w, const int32_t* tiles, const int32_t* num_tiles, int64_t cap,
                           int64_t n, int top_k, int E, int K, int N, int tile_m, float* y32,
                           tq_stream_t stream);

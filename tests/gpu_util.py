@@ -26,14 +26,16 @@ def check_no_device_error():
     assert (code, where) == (0, 0), f"device error word: code={code} where={where}"
 
 
-def grouped_y32(prob, d, tile_m):
+def grouped_y32(prob, d, tile_m, x_layout=tq.X_TOKENS):
+    """The grouped GEMM's fp32 output; x_layout picks token rows (gathered in
+    the kernel) or the pair-sorted copy from tq_gather_rows."""
     s = prob.shape
     counts, offsets, sp = tq.tq_route(d["ids"], s.E)
     cap = tq.tq_tile_map_capacity(s.n, s.top_k, s.E, tile_m)
     tiles, nt = tq.tq_build_tile_map(offsets, tile_m, cap)
-    xs = tq.tq_gather_rows(d["x"], sp, s.top_k)
     y32 = torch.zeros((s.n, s.N), dtype=torch.float32, device="cuda")
-    tq.tq_grouped_gemm(xs, d["packed"], d["lut"], sp, d["w"], tiles, nt, s.top_k, tile_m, y32)
+    x = d["x"] if x_layout == tq.X_TOKENS else tq.tq_gather_rows(d["x"], sp, s.top_k)
+    tq.tq_grouped_gemm(x, d["packed"], d["lut"], sp, d["w"], tiles, nt, s.top_k, tile_m, y32, x_layout=x_layout)
     check_no_device_error()
     return y32
 

@@ -81,21 +81,35 @@ def test_host_functions_reject_invalid_arguments(tq):
     with pytest.raises(tq.TQError):
         tq.tq_select_arm(10, 2, 8, 16, pin=7)
     assert np.isnan(tq.tq_pairs_per_woken_expert(4, 9, 8))
-    assert tq.tq_moe_workspace_size(16, 2, 8, 256, 128, 16) > 16 * 128 * 4 + 32 * 256 * 2
+    # counts, offsets, sorted pairs, tile map, tile count, fp32 accumulator
+    # (each region 256-byte aligned); no copy of the activations
+    a256 = lambda b: (b + 255) // 256 * 256
+    cap = tq.tq_tile_map_capacity(16, 2, 8, 16)
+    assert tq.tq_moe_workspace_size(16, 2, 8, 256, 128, 16) == (
+        a256(8 * 4) + a256(9 * 4) + a256(32 * 4) + a256(3 * cap * 4) + a256(4) + a256(16 * 128 * 4))
+    # above the in-kernel gather's m-tile, the pair-sorted activations too
+    T = tq.GATHER_MAX_TILE_M + 1
+    cap = tq.tq_tile_map_capacity(16, 2, 8, T)
+    assert tq.tq_moe_workspace_size(16, 2, 8, 256, 128, T) == (
+        a256(8 * 4) + a256(9 * 4) + a256(32 * 4) + a256(3 * cap * 4) + a256(4) + a256(16 * 128 * 4)
+        + a256(32 * 256 * 2))
 
 
 def test_native_tile(tq):
-    """TQ_TILE_NATIVE: 128 at decode sizes, 256 once the expected pairs per
-    woken expert reach 128 (the oracle's closed form decides which); the
-    workspace of tile_m = 0 is that of the native tile."""
+    """TQ_TILE_NATIVE: 16 while the expected pairs per woken expert stay at
+    most 4, 128 above, 256 once they reach 128 (the oracle's closed form
+    decides which); the workspace of tile_m = 0 is that of the native tile."""
     assert tq.TILE_NATIVE == 0
-    for n, k, E in ((1, 6, 256), (32, 6, 256), (1024, 6, 256), (8192, 6, 256), (5000, 2, 8), (0, 2, 8)):
-        want = 256 if n > 0 and O.pairs_per_woken_expert(n, k, E) >= 128 else 128
+    for n, k, E in ((1, 6, 256), (32, 6, 256), (128, 6, 256), (512, 6, 256), (1024, 6, 256), (8192, 6, 256),
+                    (5000, 2, 8), (0, 2, 8)):
+        ppw = O.pairs_per_woken_expert(n, k, E) if n > 0 else 0.0
+        want = 256 if ppw >= 128 else (128 if ppw > 4 else 16)
         assert tq.tq_native_tile_m(n, k, E) == want, (n, k, E)
         assert tq.tq_moe_workspace_size(n, k, E, 4096, 2048, 0) == tq.tq_moe_workspace_size(n, k, E, 4096, 2048, want)
         assert (tq.tq_moe_mlp_workspace_size(n, k, E, 4096, 2048, 0)
                 == tq.tq_moe_mlp_workspace_size(n, k, E, 4096, 2048, want))
-    assert tq.tq_native_tile_m(32, 6, 256) == 128 and tq.tq_native_tile_m(8192, 6, 256) == 256
+    assert tq.tq_native_tile_m(32, 6, 256) == 16 and tq.tq_native_tile_m(512, 6, 256) == 128
+    assert tq.tq_native_tile_m(8192, 6, 256) == 256
     with pytest.raises(tq.TQError):
         tq.tq_native_tile_m(4, 9, 8)
     assert tq.tq_moe_workspace_size(16, 2, 8, 256, 128, 257) == 0

@@ -142,10 +142,9 @@ def test_dense_gemm_equals_fused_on_materialized_weights():
     counts, offsets, sp = tq.tq_route(d["ids"], s.E)
     cap = tq.tq_tile_map_capacity(s.n, s.top_k, s.E, T)
     tiles, nt = tq.tq_build_tile_map(offsets, T, cap)
-    xs = tq.tq_gather_rows(d["x"], sp, s.top_k)
     w_dense = tq.tq_dequantize(d["packed"], d["lut"])
     y32 = torch.zeros((s.n, s.N), dtype=torch.float32, device="cuda")
-    tq.tq_grouped_gemm_dense(xs, w_dense, sp, d["w"], tiles, nt, s.top_k, T, y32)
+    tq.tq_grouped_gemm_dense(d["x"], w_dense, sp, d["w"], tiles, nt, s.top_k, T, y32)
     check_no_device_error()
     assert normwise(y32.cpu().numpy(), fused.cpu().numpy()) <= 1e-5
 

@@ -51,11 +51,12 @@ def _small(name):
     return moe_inputs.make_custom(E, k, n, K, N, L, seed=zlib.crc32(name.encode()) % 1000, routing=routing), T
 
 
+@pytest.mark.parametrize("lay", [tq.X_TOKENS, tq.X_PAIR_SORTED])
 @pytest.mark.parametrize("name", sorted(SMALL))
-def test_grouped_small_all_outputs(name):
+def test_grouped_small_all_outputs(name, lay):
     prob, T = _small(name)
     d = to_device(prob)
-    y = grouped_y32(prob, d, T).cpu().numpy()
+    y = grouped_y32(prob, d, T, lay).cpu().numpy()
     ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, prob.shape.L)
     err = normwise(y, ref)
     assert err <= TOL, err
@@ -77,10 +78,9 @@ def test_grouped_accumulates_into_y32():
     _, offsets, sp = tq.tq_route(d["ids"], s.E)
     cap = tq.tq_tile_map_capacity(s.n, s.top_k, s.E, T)
     tiles, nt = tq.tq_build_tile_map(offsets, T, cap)
-    xs = tq.tq_gather_rows(d["x"], sp, s.top_k)
     y32 = torch.ones((s.n, s.N), dtype=torch.float32, device="cuda")
     for _ in range(2):
-        tq.tq_grouped_gemm(xs, d["packed"], d["lut"], sp, d["w"], tiles, nt, s.top_k, T, y32)
+        tq.tq_grouped_gemm(d["x"], d["packed"], d["lut"], sp, d["w"], tiles, nt, s.top_k, T, y32)
     check_no_device_error()
     ref = 1.0 + 2.0 * O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed,
                                     prob.lut_bits, s.L)
@@ -125,9 +125,11 @@ def test_full_size_sampled_rows(name, full_problems):
     s = prob.shape
     rows = sample_rows(s.N, 48, seed=len(name))
     ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L, rows=rows)
-    for T in (16, 128):
-        y = grouped_y32(prob, d, T)[:, torch.from_numpy(rows).cuda()].cpu().numpy()
-        assert normwise(y, ref) <= TOL, (T, normwise(y, ref))
+    # token rows gathered by the kernel and the pair-sorted copy (each at the
+    # m-tile the whole-product calls use it with, and token rows at 128 too)
+    for T, lay in ((16, tq.X_TOKENS), (128, tq.X_PAIR_SORTED), (128, tq.X_TOKENS)):
+        y = grouped_y32(prob, d, T, lay)[:, torch.from_numpy(rows).cuda()].cpu().numpy()
+        assert normwise(y, ref) <= TOL, (T, lay, normwise(y, ref))
     if s.n <= 1024:
         y = gemv_y32(prob, d)[:, torch.from_numpy(rows).cuda()].cpu().numpy()
         assert normwise(y, ref) <= TOL_GEMV
@@ -149,6 +151,10 @@ def test_moe_forward_gate_and_arms():
         ran = "grouped" if arm == 2 else "gemv"
         other = "gemv" if arm == 2 else "grouped"
         assert after[ran] == before[ran] + 1 and after[other] == before[other]
+        # the grouped arm: one routing launch, the kernel gathers activations itself
+        assert after["gather"] == before["gather"]
+        if arm == 2:
+            assert after["route_tile_map"] == before["route_tile_map"] + 1
         ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, 12)
         got = y.float().cpu().numpy()
         assert normwise(got, ref) <= TOL

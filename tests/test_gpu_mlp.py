@@ -44,6 +44,10 @@ def test_mlp_tiny_all_outputs(tile_m, pin):
     assert arm == pin
     ran = "grouped" if pin == tq.ARM_GROUPED else "gemv"
     assert after[ran] == before[ran] + 2     # gate|up and down
+    # the gate|up input: token rows gathered in the kernel, or a pair-sorted
+    # copy (one gather launch) above the in-kernel gather's m-tile
+    gathers = 1 if pin == tq.ARM_GROUPED and tile_m > tq.GATHER_MAX_TILE_M else 0
+    assert after["gather"] == before["gather"] + gathers
     ref = O.moe_mlp(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed_gu, prob.lut_gu, prob.packed_down,
                     prob.lut_down, prob.L)
     assert normwise(y.float().cpu().numpy(), ref) <= TOL

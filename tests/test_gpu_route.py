@@ -112,9 +112,10 @@ def test_combine_bitexact():
 
 
 def test_prepare_equals_separate_calls():
-    """tq_prepare (route + tile map in one launch, gather clearing y32) gives
-    bit for bit what tq_route, tq_build_tile_map and tq_gather_rows give, and
-    leaves y32 zero."""
+    """tq_prepare (route + tile map in one launch whose other blocks clear
+    y32, then the gather when x_sorted is given) gives bit for bit what
+    tq_route, tq_build_tile_map and tq_gather_rows give, and leaves y32 zero
+    (64 MiB of it at the prefill size)."""
     import moe_inputs
     for name, T in (("v4_decode_n32", 16), ("v4_prefill_n8192_up", 256)):
         prob = moe_inputs.make_problem(name, with_packed=False)
@@ -139,6 +140,18 @@ def test_prepare_equals_separate_calls():
             assert torch.equal(a, b)
         ntiles = int(nt1.item())
         assert torch.equal(t1[:ntiles], t2[:ntiles])
+        assert torch.count_nonzero(y32).item() == 0
+        # without x_sorted: one launch, the same routing, y32 cleared
+        y32.fill_(5.0)
+        sp2.fill_(-1)
+        before = tq.tq_launch_counts()
+        tq.tq_prepare(ids, x, s.E, T, cap, c2, o2, sp2, t2, nt2, None, y32)
+        torch.cuda.synchronize()
+        after = tq.tq_launch_counts()
+        assert after["route_tile_map"] == before["route_tile_map"] + 1
+        assert after["gather"] == before["gather"]
+        assert tq.tq_device_error() == (0, 0)
+        assert torch.equal(sp1, sp2) and torch.equal(t1[:ntiles], t2[:ntiles])
         assert torch.count_nonzero(y32).item() == 0
 
 

@@ -47,7 +47,7 @@ def test_lut_probe_rate_is_sane():
 @pytest.mark.parametrize("pin", [tq.ARM_GROUPED, tq.ARM_GEMV])
 def test_moe_forward_in_cuda_graph(pin):
     """tq_moe_forward captured in a CUDA graph (its grouped kernel is a
-    programmatic dependent of the gather) replays to the eager result, on new
+    programmatic dependent of the routing launch) replays to the eager result, on new
     inputs copied into the captured buffers, within the fp32 summation-order
     noise of the atomics."""
     s = moe_inputs.shape("v4_decode_n32")

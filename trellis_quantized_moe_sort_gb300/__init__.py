@@ -23,10 +23,13 @@ __all__ = [
     "tq_status_string", "tq_probe_lut_rate", "tq_grouped_gemm_pairs", "tq_swiglu",
     "tq_moe_mlp_workspace_size", "tq_moe_mlp_forward", "tq_dequantize", "tq_grouped_gemm_dense",
     "tq_moe_dequant_workspace_size", "tq_moe_forward_dequant", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "ARM_MEASURED", "EXPORTED_SYMBOLS",
+    "X_TOKENS", "X_PAIR_SORTED", "GATHER_MAX_TILE_M",
 ]
 
 ARM_AUTO, ARM_GEMV, ARM_GROUPED, ARM_MEASURED = 0, 1, 2, 3
 TILE_NATIVE = 0          # tile_m of the whole-product calls: the kernel's native m-tile
+X_TOKENS, X_PAIR_SORTED = 0, 1   # activation layouts of tq_grouped_gemm / tq_grouped_gemm_dense
+GATHER_MAX_TILE_M = 16   # the whole-product calls gather rows in the kernel up to this m-tile
 _HERE = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_HERE, "libtqmoe.so")
 
@@ -47,7 +50,7 @@ _SIGS = {
     "tq_build_tile_map": (_c_int, [_c_p, _c_int, _c_int, _c_p, _c_p, _c_i64, _c_p]),
     "tq_router_topk": (_c_int, [_c_p, _c_i64, _c_int, _c_int, _c_p, _c_p, _c_p]),
     "tq_route_logits": (_c_int, [_c_p, _c_i64, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
-    "tq_grouped_gemm": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64,
+    "tq_grouped_gemm": (_c_int, [_c_p, _c_int, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64,
                                  _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p]),
     "tq_gemv": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int, _c_int,
                          _c_int, _c_p, _c_p]),
@@ -69,7 +72,8 @@ _SIGS = {
     "tq_moe_mlp_forward": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int, _c_int,
                                     _c_int, _c_int, _c_int, _c_p, _c_sz, _c_p, ctypes.POINTER(_c_int), _c_p]),
     "tq_dequantize": (_c_int, [_c_p, _c_p, _c_int, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p]),
-    "tq_grouped_gemm_dense": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_int, _c_int, _c_int,
+    "tq_grouped_gemm_dense": (_c_int, [_c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_int, _c_int,
+                                       _c_int,
                                        _c_int, _c_int, _c_p, _c_p]),
     "tq_moe_dequant_workspace_size": (_c_sz, [_c_i64, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "tq_moe_forward_dequant": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int, _c_int,
@@ -314,37 +318,49 @@ def tq_gather_rows(x, sorted_pairs, top_k: int, x_sorted=None, stream=None):
 
 
 def tq_prepare(topk_ids, x, E: int, tile_m: int, cap: int, counts, offsets, sorted_pairs, tiles, num_tiles,
-               x_sorted, y32=None, stream=None) -> None:
-    """Route + tile map (one launch) and the activation gather, clearing y32
-    (fp32) in the same launch when it is given."""
+               x_sorted=None, y32=None, stream=None) -> None:
+    """Route + tile map in one launch, clearing y32 (fp32) in the same launch
+    when it is given; with x_sorted, also the pair-sorted copy of x (what
+    tq_grouped_gemm_pairs reads; tq_grouped_gemm gathers the rows itself)."""
     torch = _torch()
     n, top_k = topk_ids.shape
     K = x.shape[1]
     y32_ptr = None if y32 is None else _dev_ptr(y32, (torch.float32,), "y32")
+    xs_ptr = None if x_sorted is None else _dev_ptr(x_sorted, _bits16(), "x_sorted")
     _check(lib().tq_prepare(_dev_ptr(topk_ids, (torch.int32,), "topk_ids"), _dev_ptr(x, _bits16(), "x"), n, top_k,
                             E, K, tile_m, _dev_ptr(counts, (torch.int32,), "counts"),
                             _dev_ptr(offsets, (torch.int32,), "offsets"),
                             _dev_ptr(sorted_pairs, (torch.int32,), "sorted_pairs"),
                             _dev_ptr(tiles, (torch.int32,), "tiles"), _dev_ptr(num_tiles, (torch.int32,), "num_tiles"),
-                            cap, _dev_ptr(x_sorted, _bits16(), "x_sorted"), y32_ptr,
-                            0 if y32 is None else y32.numel(), _stream(stream)), "tq_prepare")
+                            cap, xs_ptr, y32_ptr, 0 if y32 is None else y32.numel(), _stream(stream)), "tq_prepare")
 
 
-def tq_grouped_gemm(x_sorted, packed, lut, sorted_pairs, topk_w, tiles, num_tiles, top_k: int, tile_m: int,
-                    y32, stream=None) -> None:
+def _x_rows(x, x_layout: int, top_k: int) -> int:
+    """Tokens n of an activation tensor in either layout."""
+    if x_layout == X_TOKENS:
+        return x.shape[0]
+    if x_layout != X_PAIR_SORTED:
+        raise ValueError(f"x_layout must be X_TOKENS or X_PAIR_SORTED, not {x_layout}")
+    if x.shape[0] % top_k:
+        raise ValueError("pair-sorted x must have n*top_k rows")
+    return x.shape[0] // top_k
+
+
+def tq_grouped_gemm(x, packed, lut, sorted_pairs, topk_w, tiles, num_tiles, top_k: int, tile_m: int,
+                    y32, x_layout: int = X_TOKENS, stream=None) -> None:
     """y32 += grouped product (y32 fp32 [n, N], zero it for a plain product).
-    x_sorted: pair-sorted activations [n*top_k, K] from tq_gather_rows."""
+    x: the token activations [n, K] (X_TOKENS: the kernel gathers each m-tile's
+    rows through sorted_pairs) or their pair-sorted copy [n*top_k, K] from
+    tq_gather_rows (X_PAIR_SORTED)."""
     torch = _torch()
-    P, K = x_sorted.shape
+    n = _x_rows(x, x_layout, top_k)
+    K = x.shape[1]
     E, N, kb = packed.shape
     if kb * 4 != K:
         raise ValueError(f"packed has {kb} bytes per row, expected K/4 = {K // 4}")
-    if P % top_k:
-        raise ValueError("x_sorted must have n*top_k rows")
-    n = P // top_k
     L = lut.numel().bit_length() - 1
     cap = tiles.shape[0]
-    _check(lib().tq_grouped_gemm(_dev_ptr(x_sorted, _bits16(), "x_sorted"), _dev_ptr(packed, (torch.uint8,), "packed"),
+    _check(lib().tq_grouped_gemm(_dev_ptr(x, _bits16(), "x"), x_layout, _dev_ptr(packed, (torch.uint8,), "packed"),
                                  _dev_ptr(lut, _bits16(), "lut"), L,
                                  _dev_ptr(sorted_pairs, (torch.int32,), "sorted_pairs"),
                                  _dev_ptr(topk_w, (torch.float32,), "topk_w"),
@@ -498,21 +514,22 @@ def tq_dequantize(packed, lut, expert_ids=None, w_out=None, stream=None):
     return w_out
 
 
-def tq_grouped_gemm_dense(x_sorted, w_dense, sorted_pairs, topk_w, tiles, num_tiles, top_k: int, tile_m: int,
-                          y32, stream=None) -> None:
-    """y32 += grouped product with dense bf16 weights w_dense [E, N, K]."""
+def tq_grouped_gemm_dense(x, w_dense, sorted_pairs, topk_w, tiles, num_tiles, top_k: int, tile_m: int,
+                          y32, x_layout: int = X_TOKENS, stream=None) -> None:
+    """y32 += grouped product with dense bf16 weights w_dense [E, N, K];
+    x and x_layout as in tq_grouped_gemm."""
     torch = _torch()
-    P, K = x_sorted.shape
+    n = _x_rows(x, x_layout, top_k)
+    K = x.shape[1]
     E, N, K2 = w_dense.shape
     if K2 != K:
-        raise ValueError(f"w_dense has K = {K2}, x_sorted has {K}")
-    if P % top_k:
-        raise ValueError("x_sorted must have n*top_k rows")
-    _check(lib().tq_grouped_gemm_dense(_dev_ptr(x_sorted, _bits16(), "x_sorted"), _dev_ptr(w_dense, _bits16(), "w_dense"),
+        raise ValueError(f"w_dense has K = {K2}, x has {K}")
+    _check(lib().tq_grouped_gemm_dense(_dev_ptr(x, _bits16(), "x"), x_layout,
+                                       _dev_ptr(w_dense, _bits16(), "w_dense"),
                                        _dev_ptr(sorted_pairs, (torch.int32,), "sorted_pairs"),
                                        _dev_ptr(topk_w, (torch.float32,), "topk_w"),
                                        _dev_ptr(tiles, (torch.int32,), "tiles"),
-                                       _dev_ptr(num_tiles, (torch.int32,), "num_tiles"), tiles.shape[0], P // top_k,
+                                       _dev_ptr(num_tiles, (torch.int32,), "num_tiles"), tiles.shape[0], n,
                                        top_k, E, K, N, tile_m, _dev_ptr(y32, (torch.float32,), "y32"),
                                        _stream(stream)), "tq_grouped_gemm_dense")
 

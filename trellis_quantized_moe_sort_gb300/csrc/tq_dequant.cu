@@ -183,7 +183,7 @@ int tq_dequantize(const uint8_t* packed, const uint16_t* lut, int L, const int32
   return launch_dequant(packed, lut, L, expert_ids, nullptr, m, E, N, K, w_out, err, s);
 }
 
-int tq_grouped_gemm_dense(const uint16_t* x_sorted, const uint16_t* w_dense, const int32_t* sorted_pairs,
+int tq_grouped_gemm_dense(const uint16_t* x, int x_layout, const uint16_t* w_dense, const int32_t* sorted_pairs,
                           const float* topk_w, const int32_t* tiles, const int32_t* num_tiles, int64_t cap,
                           int64_t n, int top_k, int E, int K, int N, int tile_m, float* y32, tq_stream_t stream) {
   if (E < 1 || top_k < 1 || top_k > E || n < 0 || K < 64 || K % 64 != 0 || N < 128 || N % 128 != 0)
@@ -191,17 +191,18 @@ int tq_grouped_gemm_dense(const uint16_t* x_sorted, const uint16_t* w_dense, con
   if (tile_m < 1 || tile_m > 256 || cap < 1 || cap >= (static_cast<int64_t>(1) << 31)) return TQ_ERR_INVALID_ARG;
   if (n * top_k >= (static_cast<int64_t>(1) << 31) || static_cast<int64_t>(E) * N >= (static_cast<int64_t>(1) << 31))
     return TQ_ERR_INVALID_ARG;
-  if (n > 0 && (!x_sorted || !w_dense || !sorted_pairs || !topk_w || !tiles || !num_tiles || !y32))
+  if (n > 0 && (!x || !w_dense || !sorted_pairs || !topk_w || !tiles || !num_tiles || !y32))
     return TQ_ERR_INVALID_ARG;
-  if (n > 0 && (!al16(x_sorted) || !al16(w_dense) || !al16(y32))) return TQ_ERR_INVALID_ARG;
+  if (n > 0 && (!al16(x) || !al16(w_dense) || !al16(y32))) return TQ_ERR_INVALID_ARG;
+  if (x_layout != TQ_X_TOKENS && x_layout != TQ_X_PAIR_SORTED) return TQ_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int rc = require_sm103(s);
   if (rc != TQ_OK) return rc;
   if (n == 0) return TQ_OK;
   int* err = error_word(&rc);
   if (!err) return rc;
-  return launch_grouped(x_sorted, nullptr, nullptr, 2, sorted_pairs, topk_w, tiles, num_tiles, cap, n, top_k, E,
-                        K, N, tile_m, y32, err, s, 0, w_dense);
+  return launch_grouped(x, nullptr, nullptr, 2, sorted_pairs, topk_w, tiles, num_tiles, cap, n, top_k, E, K, N,
+                        tile_m, y32, err, s, 0, w_dense, false, false, x_layout == TQ_X_PAIR_SORTED);
 }
 
 size_t tq_moe_dequant_workspace_size(int64_t n, int top_k, int E, int K, int N, int tile_m) {
@@ -237,18 +238,17 @@ int tq_moe_forward_dequant(const uint16_t* x, const uint8_t* packed, const uint1
 
   const int64_t cap = tq_tile_map_capacity(n, top_k, E, tile_m);
   const int P = static_cast<int>(n * top_k);
-  const MoeScratch ws = carve_moe_scratch(workspace, n, top_k, E, K, N, cap);
+  const MoeScratch ws = carve_moe_scratch(workspace, n, top_k, E, K, N, cap, tile_m);
   uint16_t* w_dense = reinterpret_cast<uint16_t*>(ws.end);   // [E][N][K]; slot e = expert e
   if ((rc = launch_route_tile_map(topk_ids, P, E, tile_m, ws.counts, ws.offsets, ws.sorted_pairs, ws.tiles,
-                                  ws.num_tiles, cap, err, s)) != TQ_OK)
+                                  ws.num_tiles, cap, err, s, ws.y32, static_cast<int64_t>(n) * N)) != TQ_OK)
     return rc;
-  if ((rc = launch_gather_zero(x, ws.sorted_pairs, P, top_k, K, ws.x_sorted, ws.y32, static_cast<int64_t>(n) * N,
-                               err, s)) != TQ_OK)
-    return rc;
+  if (ws.x_sorted && (rc = launch_gather(x, ws.sorted_pairs, P, top_k, K, ws.x_sorted, err, s)) != TQ_OK) return rc;
   // Materialize every woken expert (experts no pair routes to are skipped).
   if ((rc = launch_dequant(packed, lut, L, nullptr, ws.counts, E, E, N, K, w_dense, err, s)) != TQ_OK) return rc;
-  if ((rc = launch_grouped(ws.x_sorted, nullptr, nullptr, 2, ws.sorted_pairs, topk_w, ws.tiles, ws.num_tiles, cap,
-                           n, top_k, E, K, N, tile_m, ws.y32, err, s, 0, w_dense)) != TQ_OK)
+  if ((rc = launch_grouped(ws.x_sorted ? ws.x_sorted : x, nullptr, nullptr, 2, ws.sorted_pairs, topk_w, ws.tiles,
+                           ws.num_tiles, cap, n, top_k, E, K, N, tile_m, ws.y32, err, s, 0, w_dense, false, false,
+                           ws.x_sorted != nullptr)) != TQ_OK)
     return rc;
   return launch_combine(ws.y32, y, static_cast<int64_t>(n) * N, s);
 }

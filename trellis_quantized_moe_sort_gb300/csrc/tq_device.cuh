@@ -117,6 +117,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// Row gather: rows r0..r3 of a 2-D tensor whose map has a box one row high,
+// columns [x, x + box width), into four consecutive box rows at `dst` (the
+// map's swizzle applied as for a four-row tile at that address); completion
+// counted in bytes on `bar`.
+__device__ __forceinline__ void tma_gather4_2d(uint32_t dst, const CUtensorMap* m, int32_t x, int32_t r0,
+                                               int32_t r1, int32_t r2, int32_t r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
 
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

@@ -34,7 +34,14 @@
 //               memory with tcgen05.st.
 // Work: units = (m-tile, 128-row block of N) x super-stages, split into equal
 // contiguous ranges per CTA (a unit may be shared by two CTAs; the epilogue
-// adds partial sums atomically).
+// adds partial sums atomically), or, when every CTA has many units and the
+// output is large, whole units dealt round-robin (see Walk).
+// Modes: pair_out (per-pair outputs, no router weight: the MLP's gate|up),
+// store_out (with pair_out: whole units and plain stores), kDense (A read from
+// materialized bf16 weights: the dequantize-materialize comparator).
+// Launched with programmatic stream serialization: the kernel waits for its
+// predecessor at its start, or after its prologue (LUT staging, tensor memory)
+// when the caller knows the predecessor writes nothing the prologue reads.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -93,6 +100,8 @@ struct Params {
   int allow_interleave;  // whole units round-robin over CTAs when there are many (blocked order only)
   int store_out;         // whole units always, and plain stores: every output element has one writer
   int early_prologue;    // the previous kernel writes nothing the prologue reads (LUT): overlap it
+  int act_gather;        // activations: 1 = x holds token rows, gathered by sorted pair; 0 = x holds
+                         // the pair-sorted rows themselves
   int n_mma_max;    // largest MMA N (tile_m rounded up to 16)
   int pk_stages;    // packed super-stage buffers
   int act_stages;   // activation k-step buffers
@@ -405,36 +414,62 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     drain_ring(bar_pkfull, pk, SP, pk_issued, p.err);
   } else if (warp == kWarpActProducer) {
     // ------------------------------------------------------------ activation producer
-    // The tile's activation rows are consecutive in the pair-sorted copy of x:
-    // one box of n_mma_max rows per k-step (rows past the tile are never read
-    // back by the epilogue).
+    // Gathered (act_gather): the tile's rows are token rows of x, four per
+    // gather copy; lane l copies row groups l and l + 32 (rows 4g .. 4g+3)
+    // of the tile's n_mma rows, rows past the tile repeating its last pair.
+    // Pair-sorted: the rows are consecutive, one box of n_mma_max rows per
+    // k-step (rows past the tile are never read back by the epilogue).
     if (lane == 0) tma_prefetch_desc(&tm_xs);
     Pipe act;
     long long act_issued = 0;
     bool ok = true;
-    const uint32_t act_tx = static_cast<uint32_t>(p.n_mma_max) * kActRowBytes;
     Walk w = walk0;
     Segment sg;
     while (ok && walk_next(w, n_ss, num_tiles, rb_group, sg)) {
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
       const int ks0 = sg.ss0 * kSSSteps, ks1 = min(ksteps, sg.ss1 * kSSSteps);
-      // Activations of a tile are read by several CTAs at different times and
-      // may have left L2: ask for them kActPrefetch k-steps before the copy
-      // into shared memory needs them.
-      if (lane == 0)
+      const int n_mma = (tl.rows + 15) & ~15;
+      int tok[2][4];   // gathered: x rows of this lane's two row groups
+      if (p.act_gather) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int row = min(4 * (lane + 32 * j) + r, tl.rows - 1);
+            const int pair = __ldg(p.sorted_pairs + tl.slot0 + row);
+            // a pair id out of range is reported by the epilogue, which
+            // discards its column; copy a valid row in its place
+            tok[j][r] = (pair >= 0 && pair < p.P) ? pair / p.top_k : 0;
+          }
+        }
+      } else if (lane == 0) {
+        // Activations of a tile are read by several CTAs at different times
+        // and may have left L2: ask for them kActPrefetch k-steps before the
+        // copy into shared memory needs them.
         for (int j = ks0; j < min(ks1, ks0 + kActPrefetch); ++j) tma_prefetch_l2_2d(&tm_xs, j * kKStep, tl.slot0);
+      }
+      const uint32_t act_tx = static_cast<uint32_t>(p.act_gather ? n_mma : p.n_mma_max) * kActRowBytes;
       for (int ks = ks0; ks < ks1; ++ks) {
         if (!mbar_wait(bar_actempty + 8 * act.stage, act.phase ^ 1u, abort_flag, p.err,
                        kWhereGroupedProducer)) {
           ok = false;
           break;
         }
-        if (lane == 0) {
-          const uint32_t full = bar_actfull + 8 * act.stage;
-          mbar_arrive_expect_tx(full, act_tx);
-          tma_load_2d(act0 + static_cast<uint32_t>(act.stage * p.n_mma_max * kActRowBytes), &tm_xs,
-                      ks * kKStep, tl.slot0, full);
+        const uint32_t full = bar_actfull + 8 * act.stage;
+        const uint32_t dst = act0 + static_cast<uint32_t>(act.stage * p.n_mma_max * kActRowBytes);
+        if (lane == 0) mbar_arrive_expect_tx(full, act_tx);
+        if (p.act_gather) {
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int g = lane + 32 * j;
+            if (4 * g < n_mma)
+              tma_gather4_2d(dst + static_cast<uint32_t>(g * 4 * kActRowBytes), &tm_xs, ks * kKStep, tok[j][0],
+                             tok[j][1], tok[j][2], tok[j][3], full);
+          }
+        } else if (lane == 0) {
+          tma_load_2d(dst, &tm_xs, ks * kKStep, tl.slot0, full);
           if (ks + kActPrefetch < ks1) tma_prefetch_l2_2d(&tm_xs, (ks + kActPrefetch) * kKStep, tl.slot0);
         }
         ++act_issued;
@@ -728,11 +763,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
+int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
                    const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                    const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
                    int tile_m, float* y32, int* err, cudaStream_t s, int pair_out, const uint16_t* dense_w,
-                   bool pdl, bool store_out) {
+                   bool pdl, bool store_out, bool x_pair_sorted) {
   auto encode = encode_fn();
   if (!encode) return TQ_ERR_CUDA;
   const bool dense = dense_w != nullptr;
@@ -760,6 +795,7 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
   // in L2 while six scattered partial sums per element arrive.
   p.pair_out = pair_out;
   p.early_prologue = pdl ? 1 : 0;
+  p.act_gather = x_pair_sorted ? 0 : 1;
   // Per-pair outputs written once each: whole units (never split between
   // CTAs) and plain stores, so the caller need not clear the output first.
   p.store_out = (store_out && pair_out) ? 1 : 0;
@@ -833,11 +869,13 @@ int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16
       return TQ_ERR_INVALID_ARG;
   }
   {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(p.P)};
+    // Token rows [n][K] copied four rows at a time by gather (a box one row
+    // high), or pair-sorted rows [P][K] one n_mma_max-row box per k-step.
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(p.act_gather ? n : p.P)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {kKStep, static_cast<cuuint32_t>(p.n_mma_max)};
+    const cuuint32_t box[2] = {kKStep, p.act_gather ? 1u : static_cast<cuuint32_t>(p.n_mma_max)};
     const cuuint32_t estr[2] = {1, 1};
-    if (encode(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x_sorted), dims, strides, box,
+    if (encode(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return TQ_ERR_INVALID_ARG;

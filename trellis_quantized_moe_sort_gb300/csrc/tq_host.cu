@@ -175,7 +175,8 @@ bool resolve_tile(int64_t n, int top_k, int E, int tile_m, int* kernel_tile, int
 }
 
 // Every region is 256-byte aligned and sized as in tq_moe_workspace_size.
-MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K, int N, int64_t cap) {
+MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K, int N, int64_t cap,
+                             int kernel_tile_m) {
   const size_t P = static_cast<size_t>(n) * top_k;
   MoeScratch m{};
   uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -185,7 +186,10 @@ MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K
   m.tiles = reinterpret_cast<int32_t*>(w);         w += align256(sizeof(int32_t) * 3 * std::max<int64_t>(cap, 1));
   m.num_tiles = reinterpret_cast<int32_t*>(w);     w += align256(sizeof(int32_t));
   m.y32 = reinterpret_cast<float*>(w);             w += align256(sizeof(float) * static_cast<size_t>(n) * N);
-  m.x_sorted = reinterpret_cast<uint16_t*>(w);     w += align256(sizeof(uint16_t) * P * K);
+  m.x_sorted = nullptr;
+  if (!gathers_in_kernel(kernel_tile_m)) {
+    m.x_sorted = reinterpret_cast<uint16_t*>(w);   w += align256(sizeof(uint16_t) * P * K);
+  }
   m.end = w;
   return m;
 }
@@ -375,8 +379,8 @@ int tq_prepare(const int32_t* topk_ids, const uint16_t* x, int64_t n, int top_k,
   const int64_t P = n * top_k;
   if (P >= (static_cast<int64_t>(1) << 31)) return TQ_ERR_INVALID_ARG;
   if (!counts || !offsets || !tiles || !num_tiles) return TQ_ERR_INVALID_ARG;
-  if (P > 0 && (!topk_ids || !x || !sorted_pairs || !x_sorted || !aligned16(x) || !aligned16(x_sorted)))
-    return TQ_ERR_INVALID_ARG;
+  if (P > 0 && (!topk_ids || !sorted_pairs)) return TQ_ERR_INVALID_ARG;
+  if (P > 0 && x_sorted && (!x || !aligned16(x) || !aligned16(x_sorted))) return TQ_ERR_INVALID_ARG;
   if (y32_count > 0 && !y32) return TQ_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int rc = require_sm103(s);
@@ -384,17 +388,18 @@ int tq_prepare(const int32_t* topk_ids, const uint16_t* x, int64_t n, int top_k,
   int* err = error_word(&rc);
   if (!err) return rc;
   rc = launch_route_tile_map(topk_ids, static_cast<int>(P), E, tile_m, counts, offsets, sorted_pairs, tiles,
-                             num_tiles, cap, err, s);
-  if (rc != TQ_OK) return rc;
-  return launch_gather_zero(x, sorted_pairs, static_cast<int>(P), top_k, K, x_sorted, y32, y32_count, err, s);
+                             num_tiles, cap, err, s, y32, y32_count);
+  if (rc != TQ_OK || !x_sorted || P == 0) return rc;
+  return launch_gather(x, sorted_pairs, static_cast<int>(P), top_k, K, x_sorted, err, s);
 }
 
-int tq_grouped_gemm(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
+int tq_grouped_gemm(const uint16_t* x, int x_layout, const uint8_t* packed, const uint16_t* lut, int L,
                     const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                     const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
                     int tile_m, float* y32, tq_stream_t stream) {
-  int rc = check_gemm_common(x_sorted, packed, lut, L, topk_w, n, top_k, E, K, N, y32);
+  int rc = check_gemm_common(x, packed, lut, L, topk_w, n, top_k, E, K, N, y32);
   if (rc != TQ_OK) return rc;
+  if (x_layout != TQ_X_TOKENS && x_layout != TQ_X_PAIR_SORTED) return TQ_ERR_INVALID_ARG;
   if (N % 128 != 0 || tile_m < 1 || tile_m > 256 || cap < 1 || cap >= (static_cast<int64_t>(1) << 31))
     return TQ_ERR_INVALID_ARG;
   if (n > 0 && !aligned16(y32)) return TQ_ERR_INVALID_ARG;
@@ -405,8 +410,8 @@ int tq_grouped_gemm(const uint16_t* x_sorted, const uint8_t* packed, const uint1
   if (n == 0) return TQ_OK;
   int* err = error_word(&rc);
   if (!err) return rc;
-  return launch_grouped(x_sorted, packed, lut, L, sorted_pairs, topk_w, tiles, num_tiles, cap, n, top_k, E, K,
-                        N, tile_m, y32, err, s);
+  return launch_grouped(x, packed, lut, L, sorted_pairs, topk_w, tiles, num_tiles, cap, n, top_k, E, K, N, tile_m,
+                        y32, err, s, 0, nullptr, false, false, x_layout == TQ_X_PAIR_SORTED);
 }
 
 int tq_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L, const int32_t* topk_ids,
@@ -434,7 +439,9 @@ int tq_combine(const float* y32, uint16_t* y, int64_t count, tq_stream_t stream)
 
 int tq_native_tile_m(int64_t n, int top_k, int E) {
   if (bad_shape(top_k, E) || n < 0) return TQ_ERR_INVALID_ARG;
-  return (n > 0 && tq_pairs_per_woken_expert(n, top_k, E) >= 128.0) ? 256 : 128;
+  const double ppw = n > 0 ? tq_pairs_per_woken_expert(n, top_k, E) : 0.0;
+  if (ppw >= 128.0) return 256;
+  return ppw > 4.0 ? 128 : 16;
 }
 
 size_t tq_moe_workspace_size(int64_t n, int top_k, int E, int K, int N, int tile_m) {
@@ -450,7 +457,7 @@ size_t tq_moe_workspace_size(int64_t n, int top_k, int E, int K, int N, int tile
   b += align256(sizeof(int32_t) * 3 * std::max<int64_t>(cap, 1));   // tiles
   b += align256(sizeof(int32_t));                                   // num_tiles
   b += align256(sizeof(float) * static_cast<size_t>(n) * N);        // y32
-  b += align256(sizeof(uint16_t) * P * K);                          // pair-sorted activations
+  if (!gathers_in_kernel(kt)) b += align256(sizeof(uint16_t) * P * K);   // pair-sorted activations
   return b;
 }
 
@@ -480,27 +487,27 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
 
   const int64_t cap = tq_tile_map_capacity(n, top_k, E, tile_m);
   const size_t P = static_cast<size_t>(n) * top_k;
-  const MoeScratch ws = carve_moe_scratch(workspace, n, top_k, E, K, N, cap);
+  const MoeScratch ws = carve_moe_scratch(workspace, n, top_k, E, K, N, cap, tile_m);
   int32_t* counts = ws.counts;
   int32_t* offsets = ws.offsets;
   int32_t* sorted_pairs = ws.sorted_pairs;
   int32_t* tiles = ws.tiles;
   int32_t* num_tiles = ws.num_tiles;
   float* y32 = ws.y32;
-  uint16_t* x_sorted = ws.x_sorted;
 
   if (arm == TQ_ARM_GROUPED) {
-    // route + tile map in one launch, the gather clearing y32, then the
-    // grouped kernel as a programmatic dependent of the gather (its prologue
-    // overlaps the gather's tail)
+    // route + tile map in one launch (its other blocks clear y32); for large
+    // m-tiles the pair-sorted copy of x; then the grouped kernel as a
+    // programmatic dependent (its prologue overlaps the previous launch's tail)
     rc = launch_route_tile_map(topk_ids, static_cast<int>(P), E, tile_m, counts, offsets, sorted_pairs, tiles,
-                               num_tiles, cap, err, s);
+                               num_tiles, cap, err, s, y32, static_cast<int64_t>(n) * N);
     if (rc != TQ_OK) return rc;
-    rc = launch_gather_zero(x, sorted_pairs, static_cast<int>(P), top_k, K, x_sorted, y32,
-                            static_cast<int64_t>(n) * N, err, s);
-    if (rc != TQ_OK) return rc;
-    rc = launch_grouped(x_sorted, packed, lut, L, sorted_pairs, topk_w, tiles, num_tiles, cap, n, top_k, E, K,
-                        N, tile_m, y32, err, s, 0, nullptr, true);
+    if (ws.x_sorted) {
+      rc = launch_gather(x, sorted_pairs, static_cast<int>(P), top_k, K, ws.x_sorted, err, s);
+      if (rc != TQ_OK) return rc;
+    }
+    rc = launch_grouped(ws.x_sorted ? ws.x_sorted : x, packed, lut, L, sorted_pairs, topk_w, tiles, num_tiles, cap,
+                        n, top_k, E, K, N, tile_m, y32, err, s, 0, nullptr, true, false, ws.x_sorted != nullptr);
     if (rc != TQ_OK) return rc;
     std::call_once(g_log_once, [&] {
       const char* q = std::getenv("TQ_QUIET");

@@ -59,27 +59,35 @@ int launch_combine(const float* y32, uint16_t* y, int64_t count, cudaStream_t s)
 int launch_router(const float* logits, int n, int E, int top_k, int32_t* ids, float* w, cudaStream_t s);
 int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top_k, int K,
                   uint16_t* x_sorted, int* err, cudaStream_t s);
-// The gather, also clearing y32[0 .. y32_count) in the same launch.
-int launch_gather_zero(const uint16_t* x, const int32_t* sorted_pairs, int P, int top_k, int K,
-                       uint16_t* x_sorted, float* y32, int64_t y32_count, int* err, cudaStream_t s);
-// Route and tile map in one launch.
+// Route and tile map in one launch, also clearing y32[0 .. y32_count) (in
+// extra blocks of the same launch, or by a separate memset when y32 is not
+// 16-byte aligned or y32_count % 4 != 0).
 int launch_route_tile_map(const int32_t* topk_ids, int P, int E, int tile_m, int32_t* counts, int32_t* offsets,
                           int32_t* sorted_pairs, int32_t* tiles, int32_t* num_tiles, int64_t cap, int* err,
-                          cudaStream_t s);
-int launch_grouped(const uint16_t* x_sorted, const uint8_t* packed, const uint16_t* lut, int L,
+                          cudaStream_t s, float* y32 = nullptr, int64_t y32_count = 0);
+// x: token rows [n][K], gathered by sorted pair inside the kernel; or, with
+// x_pair_sorted, the pair-sorted rows [n*top_k][K] (row = sorted slot).
+int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
                    const int32_t* sorted_pairs, const float* topk_w, const int32_t* tiles,
                    const int32_t* num_tiles, int64_t cap, int64_t n, int top_k, int E, int K, int N,
                    int tile_m, float* y32, int* err, cudaStream_t s, int pair_out = 0,
-                   const uint16_t* dense_w = nullptr, bool pdl = false, bool store_out = false);
+                   const uint16_t* dense_w = nullptr, bool pdl = false, bool store_out = false,
+                   bool x_pair_sorted = false);
 // Materializes weights: out[i] = bf16(W_{e_i}) [N][K] for slot i < m, e_i =
 // expert_ids[i] (or i when expert_ids is null); a slot whose expert has
 // counts[e_i] == 0 (when counts is given) or e_i < 0 is skipped.
 int launch_dequant(const uint8_t* packed, const uint16_t* lut, int L, const int32_t* expert_ids,
                    const int32_t* counts, int m, int E, int N, int K, uint16_t* out, int* err, cudaStream_t s);
 
+// True when the whole-product calls let the grouped kernel gather the token
+// rows itself (kernel m-tile <= TQ_GATHER_MAX_TILE_M); above it they copy the
+// rows into pair-sorted order first (tq_gather_rows), which is faster there.
+inline bool gathers_in_kernel(int kernel_tile_m) { return kernel_tile_m <= TQ_GATHER_MAX_TILE_M; }
+
 // The scratch regions of tq_moe_forward inside a caller workspace (layout of
 // tq_moe_workspace_size: counts, offsets, sorted pairs, tiles, num_tiles, y32,
-// x_sorted, each 256-byte aligned); `end` is the first byte after them.
+// then x_sorted [P][K] only when the kernel m-tile does not gather in the
+// kernel, each 256-byte aligned); `end` is the first byte after them.
 struct MoeScratch {
   int32_t* counts;
   int32_t* offsets;
@@ -87,10 +95,11 @@ struct MoeScratch {
   int32_t* tiles;
   int32_t* num_tiles;
   float* y32;
-  uint16_t* x_sorted;
+  uint16_t* x_sorted;   // nullptr when the kernel gathers
   uint8_t* end;
 };
-MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K, int N, int64_t cap);
+MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K, int N, int64_t cap,
+                             int kernel_tile_m);
 
 // tile_m of the whole-product calls: 1..256 for both the arm selection and the
 // kernel, or TQ_TILE_NATIVE (the kernel's native tile, the pages' TILE_M for

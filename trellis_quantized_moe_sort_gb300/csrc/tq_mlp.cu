@@ -80,7 +80,7 @@ int tq_grouped_gemm_pairs(const uint16_t* x_sorted, const uint8_t* packed, const
   int* err = error_word(&rc);
   if (!err) return rc;
   return launch_grouped(x_sorted, packed, lut, L, sorted_pairs, nullptr, tiles, num_tiles, cap, n, top_k, E, K, N,
-                        tile_m, out32, err, s, /*pair_out=*/1);
+                        tile_m, out32, err, s, /*pair_out=*/1, nullptr, false, false, /*x_pair_sorted=*/true);
 }
 
 int tq_swiglu(const float* gate_up, int64_t P, int I, uint16_t* h, tq_stream_t stream) {
@@ -105,7 +105,7 @@ size_t tq_moe_mlp_workspace_size(int64_t n, int top_k, int E, int H, int I, int 
   b += align256(sizeof(int32_t) * std::max<size_t>(P, 1));         // sorted pairs
   b += align256(sizeof(int32_t) * 3 * std::max<int64_t>(cap, 1));  // tiles
   b += align256(sizeof(int32_t));                                  // num_tiles
-  b += align256(sizeof(uint16_t) * P * H);                         // x, pair-sorted
+  if (!gathers_in_kernel(kt)) b += align256(sizeof(uint16_t) * P * H);   // x, pair-sorted
   b += align256(sizeof(float) * P * 2 * I);                        // gate|up per pair
   b += align256(sizeof(uint16_t) * P * I);                         // h per pair
   b += align256(sizeof(float) * static_cast<size_t>(n) * H);       // y32
@@ -150,7 +150,10 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
   int32_t* sorted_pairs = reinterpret_cast<int32_t*>(w); w += align256(sizeof(int32_t) * P);
   int32_t* tiles = reinterpret_cast<int32_t*>(w);       w += align256(sizeof(int32_t) * 3 * cap);
   int32_t* num_tiles = reinterpret_cast<int32_t*>(w);   w += align256(sizeof(int32_t));
-  uint16_t* x_sorted = reinterpret_cast<uint16_t*>(w);  w += align256(sizeof(uint16_t) * P * H);
+  uint16_t* x_sorted = nullptr;   // large m-tiles: the gate|up input in pair-sorted order
+  if (!gathers_in_kernel(tile_m)) {
+    x_sorted = reinterpret_cast<uint16_t*>(w);          w += align256(sizeof(uint16_t) * P * H);
+  }
   float* gate_up = reinterpret_cast<float*>(w);         w += align256(sizeof(float) * P * 2 * I);
   uint16_t* h = reinterpret_cast<uint16_t*>(w);         w += align256(sizeof(uint16_t) * P * I);
   float* y32 = reinterpret_cast<float*>(w);
@@ -171,19 +174,21 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
     if (rc == TQ_OK) rc = launch_combine(y32, y, static_cast<int64_t>(n) * H, s);
     return rc;
   }
+  // route + tile map (its other blocks clear y32), gate|up (token rows of x
+  // gathered by the kernel, or copied into pair-sorted order first for large
+  // m-tiles), SwiGLU, down reading h in sorted order, combine
   rc = launch_route_tile_map(topk_ids, static_cast<int>(P), E, tile_m, counts, offsets, sorted_pairs, tiles,
-                             num_tiles, cap, err, s);
+                             num_tiles, cap, err, s, y32, static_cast<int64_t>(n) * H);
+  if (rc == TQ_OK && x_sorted) rc = launch_gather(x, sorted_pairs, static_cast<int>(P), top_k, H, x_sorted, err, s);
   if (rc == TQ_OK)
-    rc = launch_gather_zero(x, sorted_pairs, static_cast<int>(P), top_k, H, x_sorted, y32,
-                            static_cast<int64_t>(n) * H, err, s);
-  if (rc == TQ_OK)
-    rc = launch_grouped(x_sorted, packed_gu, lut_gu, L, sorted_pairs, nullptr, tiles, num_tiles, cap, n, top_k, E,
-                        H, 2 * I, tile_m, gate_up, err, s, /*pair_out=*/1, nullptr, false,
-                        /*store_out=*/true);   // every gate|up element written once: no clear needed
+    rc = launch_grouped(x_sorted ? x_sorted : x, packed_gu, lut_gu, L, sorted_pairs, nullptr, tiles, num_tiles, cap,
+                        n, top_k, E, H, 2 * I, tile_m, gate_up, err, s, /*pair_out=*/1, nullptr, true,
+                        /*store_out=*/true,    // every gate|up element written once: no clear needed
+                        x_sorted != nullptr);
   if (rc == TQ_OK) rc = launch_swiglu(gate_up, static_cast<int64_t>(P), I, h, s);
   if (rc == TQ_OK)
     rc = launch_grouped(h, packed_down, lut_down, L, sorted_pairs, topk_w, tiles, num_tiles, cap, n, top_k, E, I,
-                        H, tile_m, y32, err, s, /*pair_out=*/0);
+                        H, tile_m, y32, err, s, /*pair_out=*/0, nullptr, false, false, /*x_pair_sorted=*/true);
   if (rc == TQ_OK) rc = launch_combine(y32, y, static_cast<int64_t>(n) * H, s);
   return rc;
 }

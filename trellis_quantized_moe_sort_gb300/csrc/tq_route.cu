@@ -181,13 +181,22 @@ tile_map_kernel(const int32_t* __restrict__ offsets, int E, int tile_m, int32_t*
 }
 
 // Route and tile map in one launch: the tile map takes each expert's slot
-// range from the sort's registers, not from memory.
+// range from the sort's registers, not from memory.  Blocks after the first
+// clear zero4[0 .. zero_n4) (the fp32 accumulator of the grouped GEMM that
+// follows) meanwhile.
 __global__ void __launch_bounds__(kBlock, 1)
 route_tile_map_kernel(const int32_t* __restrict__ ids, int P, int E, int tile_m, int32_t* __restrict__ counts,
                       int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pairs,
-                      int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles, long long cap, int* err) {
+                      int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles, long long cap, int* err,
+                      float4* __restrict__ zero4, long long zero_n4) {
   pdl_wait();
   pdl_trigger();
+  if (blockIdx.x > 0) {
+    const long long stride = static_cast<long long>(gridDim.x - 1) * kBlock;
+    for (long long i = static_cast<long long>(blockIdx.x - 1) * kBlock + threadIdx.x; i < zero_n4; i += stride)
+      zero4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
   int first, count;
   route_block(ids, P, E, counts, offsets, sorted_pairs, err, &first, &count);
   tile_map_block(E, first, count, tile_m, tiles, num_tiles, cap, err);
@@ -219,16 +228,10 @@ __global__ void combine_kernel_scalar(const float* __restrict__ y32, uint16_t* _
 
 // x_sorted[slot] = x[sorted_pairs[slot] / top_k]: the activations in pair-sorted
 // order, 16 bytes per thread step; an out-of-range pair id yields a zero row.
-// When zero_n4 > 0 the same threads also clear zero4[0 .. zero_n4) (the fp32
-// accumulator of the grouped GEMM that follows), saving a launch.
 __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_pairs,
-                                   int P, int top_k, int row_vecs, uint4* __restrict__ x_sorted, int* err,
-                                   float4* __restrict__ zero4, long long zero_n4) {
+                                   int P, int top_k, int row_vecs, uint4* __restrict__ x_sorted, int* err) {
   pdl_wait();
   pdl_trigger();
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < zero_n4;
-       i += (long long)gridDim.x * blockDim.x)
-    zero4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   const long long total = static_cast<long long>(P) * row_vecs;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
@@ -327,32 +330,7 @@ int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<long long>((total + threads - 1) / threads, sm_count() * 8));
   int st = launch_pdl(gather_rows_kernel, dim3(blocks), dim3(threads), 0, s, reinterpret_cast<const uint4*>(x),
-                      sorted_pairs, P, top_k, row_vecs, reinterpret_cast<uint4*>(x_sorted), err,
-                      static_cast<float4*>(nullptr), 0ll);
-  if (st == TQ_OK) st = launch_status();
-  if (st == TQ_OK) count_launch(kCntGather);
-  return st;
-}
-
-int launch_gather_zero(const uint16_t* x, const int32_t* sorted_pairs, int P, int top_k, int K,
-                       uint16_t* x_sorted, float* y32, int64_t y32_count, int* err, cudaStream_t s) {
-  if (y32_count % 4 != 0 || (reinterpret_cast<uintptr_t>(y32) & 15u) != 0) {
-    // the accumulator cannot be cleared in 16-byte steps: clear it separately
-    if (y32_count > 0 && cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(y32_count), s) != cudaSuccess) {
-      cudaGetLastError();
-      return TQ_ERR_CUDA;
-    }
-    return launch_gather(x, sorted_pairs, P, top_k, K, x_sorted, err, s);
-  }
-  const long long z4 = y32_count / 4;
-  const int row_vecs = K / 8;
-  const long long total = std::max(static_cast<long long>(P) * row_vecs, z4);
-  if (total == 0) return TQ_OK;
-  const int threads = 256;
-  const int blocks = static_cast<int>(std::max<long long>(1, std::min<long long>((total + threads - 1) / threads, sm_count() * 8)));
-  int st = launch_pdl(gather_rows_kernel, dim3(blocks), dim3(threads), 0, s, reinterpret_cast<const uint4*>(x),
-                      sorted_pairs, P, top_k, row_vecs, reinterpret_cast<uint4*>(x_sorted), err,
-                      reinterpret_cast<float4*>(y32), z4);
+                      sorted_pairs, P, top_k, row_vecs, reinterpret_cast<uint4*>(x_sorted), err);
   if (st == TQ_OK) st = launch_status();
   if (st == TQ_OK) count_launch(kCntGather);
   return st;
@@ -360,15 +338,31 @@ int launch_gather_zero(const uint16_t* x, const int32_t* sorted_pairs, int P, in
 
 int launch_route_tile_map(const int32_t* topk_ids, int P, int E, int tile_m, int32_t* counts, int32_t* offsets,
                           int32_t* sorted_pairs, int32_t* tiles, int32_t* num_tiles, int64_t cap, int* err,
-                          cudaStream_t s) {
+                          cudaStream_t s, float* y32, int64_t y32_count) {
   const size_t smem = sizeof(int32_t) * kWarps * E;
   if (cudaFuncSetAttribute(route_tile_map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(sizeof(int32_t) * kWarps * 1024)) != cudaSuccess) {
     cudaGetLastError();
     return TQ_ERR_CUDA;
   }
-  int st = launch_pdl(route_tile_map_kernel, dim3(1), dim3(kBlock), smem, s, topk_ids, P, E, tile_m, counts, offsets,
-                      sorted_pairs, tiles, num_tiles, static_cast<long long>(cap), err);
+  long long z4 = 0;
+  if (y32_count > 0) {
+    if (y32_count % 4 != 0 || (reinterpret_cast<uintptr_t>(y32) & 15u) != 0) {
+      // not clearable in 16-byte steps: a separate clear
+      if (cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(y32_count), s) != cudaSuccess) {
+        cudaGetLastError();
+        return TQ_ERR_CUDA;
+      }
+    } else {
+      z4 = y32_count / 4;
+    }
+  }
+  // one routing block, plus clearing blocks (16 float4 stores per thread, at
+  // most two per SM)
+  const long long clear_blocks = std::min<long long>((z4 + 16ll * kBlock - 1) / (16ll * kBlock), 2ll * sm_count());
+  int st = launch_pdl(route_tile_map_kernel, dim3(static_cast<unsigned>(1 + clear_blocks)), dim3(kBlock), smem, s,
+                      topk_ids, P, E, tile_m, counts, offsets, sorted_pairs, tiles, num_tiles,
+                      static_cast<long long>(cap), err, reinterpret_cast<float4*>(y32), z4);
   if (st == TQ_OK) st = launch_status();
   if (st == TQ_OK) count_launch(kCntRouteTileMap);
   return st;
