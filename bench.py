@@ -609,11 +609,17 @@ def run_gate_study(args):
             tiles, nt = tq.tq_build_tile_map(offsets, T, cap)
 
             counts = torch.empty(s.E, dtype=torch.int32, device="cuda")
+            # the activation layout tq_moe_forward uses at this m-tile
+            lay = tq.X_TOKENS if T <= tq.GATHER_MAX_TILE_M else tq.X_PAIR_SORTED
+            xs = None if lay == tq.X_TOKENS else tq.tq_gather_rows(x, sp, s.top_k)
 
-            def whole():  # route + tile map + grouped GEMM (the arm's full device work)
+            def whole():  # route + tile map (+ pair-sorted copy) + grouped GEMM: the arm's device work
                 tq.tq_route(ids, s.E, counts, offsets, sp)
                 tq.tq_build_tile_map(offsets, T, cap, tiles, nt)
-                tq.tq_grouped_gemm(x, packed, lut, sp, w, tiles, nt, s.top_k, T, y32)
+                if xs is not None:
+                    tq.tq_gather_rows(x, sp, s.top_k, xs)
+                tq.tq_grouped_gemm(x if xs is None else xs, packed, lut, sp, w, tiles, nt, s.top_k, T, y32,
+                                   x_layout=lay)
             row[f"grouped_T{T}_us"] = round(timed(whole), 1)
         code, where = tq.tq_device_error()
         if code:

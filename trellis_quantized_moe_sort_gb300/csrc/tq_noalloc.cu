@@ -6,8 +6,9 @@
 // (that framework owns every allocation), or a serving loop that forbids
 // allocation after start-up because cudaMalloc can block and synchronize the
 // device.  They still pass inputs and outputs; the scratch this call needs
-// (counts, offsets, sorted pairs, tile map, fp32 accumulator, pair-sorted
-// activations) lives in one file-scope device array of fixed size, which
+// (counts, offsets, sorted pairs, tile map, fp32 accumulator, and for large
+// m-tiles the pair-sorted activations) lives in one file-scope device array
+// of fixed size, which
 // every GPU that loads this library holds until the process exits.
 #include <cuda_runtime.h>
 
