@@ -194,7 +194,20 @@ def run_ours(args, rank, world, dist):
     lay = tq.X_TOKENS if T <= tq.GATHER_MAX_TILE_M else tq.X_PAIR_SORTED
     x_sorted = None if lay == tq.X_TOKENS else torch.empty((P, K), dtype=torch.int16, device="cuda")
 
-    def step(i, timed_slot=None):
+    ws = torch.empty(tq.tq_moe_workspace_size(n, k, E, K, N, T), dtype=torch.uint8, device="cuda")
+
+    def step(i):
+        """One step as a caller runs it: the whole routed-expert product
+        (route + tile map clearing y32, grouped GEMM, combine) through the
+        public call, inputs resident, no allocation."""
+        s = sets[i % args.weight_sets]
+        tq.tq_moe_forward(s["x"], s["packed"], s["lut"], s["ids"], s["w"], tile_m=T, pin=tq.ARM_GROUPED,
+                          workspace=ws, y=y)
+
+    def kernel_step(i, timed_slot=None):
+        """The same step from the separate calls, with CUDA events around the
+        grouped kernel (events between launches cost the programmatic overlap
+        the whole-product call has, so the step above is timed without them)."""
         s = sets[i % args.weight_sets]
         # route + tile map clearing y32 (one launch), and for large m-tiles the
         # pair-sorted copy of x (a second launch)
@@ -210,15 +223,17 @@ def run_ours(args, rank, world, dist):
     lut_rate = tq.tq_probe_lut_rate(8)
     for i in range(args.warmup):
         step(i)
+        kernel_step(i)
     torch.cuda.synchronize()
     code, where = tq.tq_device_error()
     if code:
         raise RuntimeError(f"device error {code} at {where} during warm-up")
 
-    counts_before = tq.tq_launch_counts()
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
+    # timed region 1: the steps (the headline value)
+    counts_before = tq.tq_launch_counts()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -226,13 +241,19 @@ def run_ours(args, rank, world, dist):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(args.steps):
-        step(i, timed_slot=i)
+        step(i)
     t1.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    clk = clocks.stop()
     counts_after = tq.tq_launch_counts()
+    # timed region 2: the grouped kernel's own duration (the roofline's denominator)
+    for i in range(args.steps):
+        kernel_step(i, timed_slot=i)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
     code, where = tq.tq_device_error()
     if code:
         raise RuntimeError(f"device error {code} at {where} during the timed steps")
@@ -245,7 +266,7 @@ def run_ours(args, rank, world, dist):
     # tiles per set (device) for the traffic model; correctness spot check vs nothing on the hot path
     tiles_per_set = []
     for i in range(args.weight_sets):
-        step(i)
+        kernel_step(i)
         torch.cuda.synchronize()
         tiles_per_set.append(int(num_tiles.item()))
     mean_tiles = float(np.mean(tiles_per_set))
@@ -324,8 +345,12 @@ def decode_ceiling(mean_tiles, N, K, clk, rate, kernel_us, sms):
 
 
 def run_e2e(args, tq, torch, sets, n, k, E, K, N, T):
-    """Same step through tq_moe_forward with host buffers: H2D of the batch's
-    activations and routing from pinned memory, the call, D2H of y."""
+    """Same step through tq_moe_forward with host buffers: every step copies
+    its batch's activations and routing from pinned host memory, runs the
+    call and reads y back.  The copies run on a second stream into two
+    alternating device buffer sets, so step i+1's inputs travel while step i
+    computes and step i's output travels while step i+1 computes; the timed
+    region spans the first input copy to the last output copy."""
     hosts = []
     for s in sets:
         prob = s["prob"]
@@ -334,36 +359,52 @@ def run_e2e(args, tq, torch, sets, n, k, E, K, N, T):
             "ids": torch.from_numpy(np.ascontiguousarray(prob.topk_ids)).pin_memory(),
             "w": torch.from_numpy(np.ascontiguousarray(prob.topk_w)).pin_memory(),
         })
-    dx = torch.empty((n, K), dtype=torch.int16, device="cuda")
-    dids = torch.empty((n, k), dtype=torch.int32, device="cuda")
-    dw = torch.empty((n, k), dtype=torch.float32, device="cuda")
-    y = torch.empty((n, N), dtype=torch.bfloat16, device="cuda")
-    yh = torch.empty((n, N), dtype=torch.bfloat16).pin_memory()
-    ws = torch.empty(tq.tq_moe_workspace_size(n, k, E, K, N, T), dtype=torch.uint8, device="cuda")
-    stream = torch.cuda.current_stream()
+    bufs = [{"x": torch.empty((n, K), dtype=torch.int16, device="cuda"),
+             "ids": torch.empty((n, k), dtype=torch.int32, device="cuda"),
+             "w": torch.empty((n, k), dtype=torch.float32, device="cuda"),
+             "y": torch.empty((n, N), dtype=torch.bfloat16, device="cuda"),
+             "yh": torch.empty((n, N), dtype=torch.bfloat16).pin_memory(),
+             "ws": torch.empty(tq.tq_moe_workspace_size(n, k, E, K, N, T), dtype=torch.uint8, device="cuda"),
+             "in_ready": torch.cuda.Event(), "done": torch.cuda.Event()} for _ in range(2)]
+    compute = torch.cuda.current_stream()
+    copies = torch.cuda.Stream()
 
-    def one(i):
-        h = hosts[i % args.weight_sets]
-        dx.copy_(h["x"], non_blocking=True)
-        dids.copy_(h["ids"], non_blocking=True)
-        dw.copy_(h["w"], non_blocking=True)
-        tq.tq_moe_forward(dx, sets[i % args.weight_sets]["packed"], sets[i % args.weight_sets]["lut"], dids, dw,
-                          tile_m=T, pin=tq.ARM_GROUPED, workspace=ws, y=y)
-        yh.copy_(y, non_blocking=True)
+    def h2d(i):
+        b, h = bufs[i % 2], hosts[i % args.weight_sets]
+        with torch.cuda.stream(copies):
+            b["x"].copy_(h["x"], non_blocking=True)
+            b["ids"].copy_(h["ids"], non_blocking=True)
+            b["w"].copy_(h["w"], non_blocking=True)
+            b["in_ready"].record(copies)
 
-    for i in range(args.warmup):
-        one(i)
+    def run(steps, first):
+        h2d(first)
+        for i in range(first, first + steps):
+            if i + 1 < first + steps:
+                h2d(i + 1)   # after step i-1's output copy on the same stream: that buffer set is free
+            b = bufs[i % 2]
+            compute.wait_event(b["in_ready"])
+            tq.tq_moe_forward(b["x"], sets[i % args.weight_sets]["packed"], sets[i % args.weight_sets]["lut"],
+                              b["ids"], b["w"], tile_m=T, pin=tq.ARM_GROUPED, workspace=b["ws"], y=b["y"])
+            b["done"].record(compute)
+            copies.wait_event(b["done"])
+            with torch.cuda.stream(copies):
+                b["yh"].copy_(b["y"], non_blocking=True)
+        compute.wait_stream(copies)
+
+    run(args.warmup, 0)
     torch.cuda.synchronize()
     a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for i in range(args.steps):
-        one(i)
-    b_.record(stream)
+    a.record(compute)
+    copies.wait_stream(compute)
+    run(args.steps, args.warmup)
+    b_.record(compute)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b_) / args.steps
-    h2d = n * K * 2 + n * k * 4 + n * k * 4
-    return {"value": round(ms * 1e3, 2), "unit": "us/call", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": n * N * 2, "api": "tq_moe_forward (pin=grouped)"}
+    h2d_bytes = n * K * 2 + n * k * 4 + n * k * 4
+    return {"value": round(ms * 1e3, 2), "unit": "us/call", "h2d_bytes_per_step": h2d_bytes,
+            "d2h_bytes_per_step": n * N * 2,
+            "api": "tq_moe_forward (pin=grouped); copies on a second stream, overlapping the neighbouring steps"}
 
 
 # --------------------------------------------------------------- CPU oracle
