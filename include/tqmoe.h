@@ -443,10 +443,12 @@ int tq_probe_lut_rate(const uint16_t* table, int warps_per_sm, int iters, uint32
 
 /* Host-side counts of successful launches since process start, per kernel:
  * out[0] route, out[1] tile map, out[2] grouped GEMM (trellis or dense),
- * out[3] GEMV, out[4] combine, out[5] activation gather (alone or clearing
- * y32), out[6] router top-k, out[7] dequantize, out[8] route and tile map
- * fused in one launch ([P3]: counters prove which arm ran). */
-void tq_launch_counts(int64_t out[9]);
+ * out[3] GEMV, out[4] combine, out[5] activation gather, out[6] router
+ * top-k, out[7] dequantize, out[8] route and tile map fused in one launch
+ * (clearing y32 in its other blocks), out[9] accumulator clear (the GEMV
+ * arms), out[10] SwiGLU ([P3]: counters prove which arm ran). */
+#define TQ_NUM_LAUNCH_COUNTERS 11
+void tq_launch_counts(int64_t out[TQ_NUM_LAUNCH_COUNTERS]);
 
 #ifdef __cplusplus
 }

@@ -151,13 +151,38 @@ def test_moe_forward_gate_and_arms():
         ran = "grouped" if arm == 2 else "gemv"
         other = "gemv" if arm == 2 else "grouped"
         assert after[ran] == before[ran] + 1 and after[other] == before[other]
-        # the grouped arm: one routing launch, the kernel gathers activations itself
+        # the grouped arm: one routing launch (clearing y32), the kernel gathers
+        # activations itself; the GEMV arm: a clear launch before the GEMV
         assert after["gather"] == before["gather"]
         if arm == 2:
             assert after["route_tile_map"] == before["route_tile_map"] + 1
+            assert after["clear"] == before["clear"]
+        else:
+            assert after["clear"] == before["clear"] + 1
         ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, 12)
         got = y.float().cpu().numpy()
         assert normwise(got, ref) <= TOL
+
+
+@pytest.mark.parametrize("pin", [tq.ARM_GROUPED, tq.ARM_GEMV])
+@pytest.mark.parametrize("tile_m", [16, 64])
+def test_moe_forward_dirty_workspace(pin, tile_m):
+    """A workspace full of NaN bit patterns: every call clears what must start
+    at zero itself (the accumulator, in the routing launch or by the clear
+    kernel), so the result matches the oracle on every call."""
+    prob = moe_inputs.make_custom(8, 2, 40, 256, 256, 12, seed=55)
+    d = to_device(prob)
+    s = prob.shape
+    ws = torch.empty(tq.tq_moe_workspace_size(s.n, s.top_k, s.E, s.K, s.N, tile_m), dtype=torch.uint8,
+                     device="cuda")
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L)
+    for _ in range(2):
+        ws.fill_(0xFF)
+        y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=tile_m, pin=pin,
+                                   workspace=ws)
+        check_no_device_error()
+        assert arm == pin
+        assert normwise(y.float().cpu().numpy(), ref) <= TOL
 
 
 def test_moe_forward_empty_batch():

@@ -53,6 +53,27 @@ def test_mlp_tiny_all_outputs(tile_m, pin):
     assert normwise(y.float().cpu().numpy(), ref) <= TOL
 
 
+@pytest.mark.parametrize("tile_m,pin", [(16, tq.ARM_GROUPED), (64, tq.ARM_GROUPED), (16, tq.ARM_GEMV)])
+def test_mlp_dirty_workspace(tile_m, pin):
+    """A workspace of NaN bit patterns, twice: the gate|up rows are written
+    once each and the accumulator is cleared by the call itself."""
+    prob = moe_inputs.make_mlp_problem("tiny_mlp_e8_k2_n16")
+    d = _mlp_dev(prob)
+    n, k = prob.topk_ids.shape
+    E, I2, _ = prob.packed_gu.shape
+    H = prob.x_bits.shape[1]
+    ws = torch.empty(tq.tq_moe_mlp_workspace_size(n, k, E, H, I2 // 2, tile_m), dtype=torch.uint8, device="cuda")
+    ref = O.moe_mlp(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed_gu, prob.lut_gu, prob.packed_down,
+                    prob.lut_down, prob.L)
+    for _ in range(2):
+        ws.fill_(0xFF)
+        y, arm = tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"],
+                                       tile_m=tile_m, pin=pin, workspace=ws)
+        check_no_device_error()
+        assert arm == pin
+        assert normwise(y.float().cpu().numpy(), ref) <= TOL
+
+
 @pytest.mark.parametrize("pin", [tq.ARM_GROUPED, tq.ARM_GEMV])
 def test_mlp_v4_n32_sampled_tokens(pin):
     prob = moe_inputs.make_mlp_problem("v4_mlp_n32")

@@ -565,8 +565,11 @@ def tq_device_error() -> tuple[int, int]:
     return code.value, where.value
 
 
+LAUNCH_COUNTERS = ("route", "tile_map", "grouped", "gemv", "combine", "gather", "router", "dequant",
+                   "route_tile_map", "clear", "swiglu")
+
+
 def tq_launch_counts() -> dict:
-    arr = (ctypes.c_int64 * 9)()
+    arr = (ctypes.c_int64 * len(LAUNCH_COUNTERS))()
     lib().tq_launch_counts(arr)
-    return dict(zip(("route", "tile_map", "grouped", "gemv", "combine", "gather", "router", "dequant",
-                     "route_tile_map"), list(arr)))
+    return dict(zip(LAUNCH_COUNTERS, list(arr)))

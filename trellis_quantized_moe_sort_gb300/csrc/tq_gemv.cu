@@ -37,10 +37,44 @@ __global__ void __launch_bounds__(THREADS, 1)
 gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
             const uint16_t* __restrict__ lut, const int32_t* __restrict__ topk_ids,
             const float* __restrict__ topk_w, int P, int top_k, int E, int K, int N, int x_in_smem,
-            int pair_in, int pair_out, float* __restrict__ y32, int* err) {
+            int pair_in, int pair_out, int early_prologue, float* __restrict__ y32, int* err) {
   extern __shared__ __align__(16) uint16_t lut_s[];
   constexpr int kEntries = 1 << L;
   constexpr int kLutBytes = (kEntries * 2 + 15) & ~15;
+  // Launched as a programmatic dependent of the previous kernel: with
+  // early_prologue (that kernel writes none of the inputs, only the output)
+  // the staging and the first row's loads below run while it finishes, and
+  // the wait comes before the first output write.
+  if (!early_prologue) pdl_wait();
+
+  const int lane = threadIdx.x & 31;
+  const int warps_per_block = THREADS / 32;
+  const long long gwarp = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
+  const long long nwarps = static_cast<long long>(gridDim.x) * warps_per_block;
+  const int nchunks = K / kChunkSyms;
+  const size_t row_bytes = static_cast<size_t>(K / 4);
+  // This warp's contiguous range of (pair, row) items: consecutive rows of
+  // one pair share the token's activations.
+  const long long items = static_cast<long long>(P) * N;
+  const long long i0 = items * gwarp / nwarps, i1 = items * (gwarp + 1) / nwarps;
+
+  // packed bytes of item `it` (zeros for a bad expert id, reported once per pair)
+  auto load_row = [&](long long it, uint4 (&q)[CPL]) {
+    const int pair = static_cast<int>(it / N);
+    const int r = static_cast<int>(it - static_cast<long long>(pair) * N);
+    const int e = __ldg(topk_ids + pair);
+    const bool ok = e >= 0 && e < E;
+    const uint4* rp = reinterpret_cast<const uint4*>(packed + (static_cast<size_t>(ok ? e : 0) * N + r) * row_bytes);
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      q[i] = (ok && c < nchunks) ? __ldg(rp + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  // The first row's bytes are in flight while the tables are staged.
+  uint4 qa[CPL], qb[CPL];
+  if (i0 < i1) load_row(i0, qa);
+
   if constexpr (kEntries >= 8) {
     stage_to_smem(smem_u32(lut_s), lut, kEntries * 2);
   } else {
@@ -67,31 +101,8 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
   }
   __syncthreads();
   const uint32_t lut_base = smem_u32(lut_s);
-
-  const int lane = threadIdx.x & 31;
-  const int warps_per_block = THREADS / 32;
-  const long long gwarp = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
-  const long long nwarps = static_cast<long long>(gridDim.x) * warps_per_block;
-  const int nchunks = K / kChunkSyms;
-  const size_t row_bytes = static_cast<size_t>(K / 4);
-  // This warp's contiguous range of (pair, row) items: consecutive rows of
-  // one pair share the token's activations.
-  const long long items = static_cast<long long>(P) * N;
-  const long long i0 = items * gwarp / nwarps, i1 = items * (gwarp + 1) / nwarps;
-
-  // packed bytes of item `it` (zeros for a bad expert id, reported once per pair)
-  auto load_row = [&](long long it, uint4 (&q)[CPL]) {
-    const int pair = static_cast<int>(it / N);
-    const int r = static_cast<int>(it - static_cast<long long>(pair) * N);
-    const int e = __ldg(topk_ids + pair);
-    const bool ok = e >= 0 && e < E;
-    const uint4* rp = reinterpret_cast<const uint4*>(packed + (static_cast<size_t>(ok ? e : 0) * N + r) * row_bytes);
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-      const int c = lane + 32 * i;
-      q[i] = (ok && c < nchunks) ? __ldg(rp + c) : make_uint4(0u, 0u, 0u, 0u);
-    }
-  };
+  if (early_prologue) pdl_wait();
+  pdl_trigger();
 
   int cur_pair = -1, tok = 0;
   float wt = 0.f;
@@ -171,8 +182,6 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
 
   // The next row's bytes are in flight while this row decodes (two register
   // sets used in turn, so no copy waits for a load).
-  uint4 qa[CPL], qb[CPL];
-  if (i0 < i1) load_row(i0, qa);
   for (long long it = i0; it < i1; it += 2) {
     if (it + 1 < i1) load_row(it + 1, qb);
     process(it, qa);
@@ -185,7 +194,7 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
 template <int L, int CPL>
 int launch_one(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, const int32_t* ids,
                const float* w, int P, int top_k, int E, int K, int N, float* y32, int* err,
-               cudaStream_t s, int pair_in, int pair_out) {
+               cudaStream_t s, int pair_in, int pair_out, int early) {
   constexpr int kThreads = (CPL >= 4) ? 256 : 512;
   auto kfn = gemv_kernel<L, CPL, kThreads>;
   const size_t lut_bytes = ((sizeof(uint16_t) << L) + 15) & ~static_cast<size_t>(15);
@@ -201,38 +210,39 @@ int launch_one(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, co
   const int sms = sm_count();
   const long long items = static_cast<long long>(P) * N;
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(sms, (items + kThreads / 32 - 1) / (kThreads / 32))));
-  kfn<<<grid, kThreads, smem, s>>>(x, packed, lut, ids, w, P, top_k, E, K, N, x_in_smem, pair_in, pair_out, y32,
-                                   err);
-  return launch_status();
+  const int st = launch_pdl(kfn, dim3(grid), dim3(kThreads), smem, s, x, packed, lut, ids, w, P, top_k, E, K, N,
+                            x_in_smem, pair_in, pair_out, early, y32, err);
+  return st == TQ_OK ? launch_status() : st;
 }
 
 template <int L>
 int launch_L(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, const int32_t* ids,
              const float* w, int P, int top_k, int E, int K, int N, float* y32, int* err,
-             cudaStream_t s, int pi, int po) {
+             cudaStream_t s, int pi, int po, int early) {
   const int nchunks = K / kChunkSyms;
-  if (nchunks <= 32) return launch_one<L, 1>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s, pi, po);
-  if (nchunks <= 64) return launch_one<L, 2>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s, pi, po);
-  return launch_one<L, 4>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s, pi, po);
+  if (nchunks <= 32) return launch_one<L, 1>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s, pi, po, early);
+  if (nchunks <= 64) return launch_one<L, 2>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s, pi, po, early);
+  return launch_one<L, 4>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s, pi, po, early);
 }
 
 }  // namespace
 
 int launch_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
                 const int32_t* topk_ids, const float* topk_w, int64_t n, int top_k, int E, int K,
-                int N, float* y32, int* err, cudaStream_t s, int pair_in, int pair_out) {
+                int N, float* y32, int* err, cudaStream_t s, int pair_in, int pair_out, bool early_prologue) {
   const int P = static_cast<int>(n * top_k);
   if (P == 0) return TQ_OK;
+  const int early = early_prologue ? 1 : 0;
   int st;
   switch (L) {
-    case 2: st = launch_L<2>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
-    case 4: st = launch_L<4>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
-    case 6: st = launch_L<6>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
-    case 8: st = launch_L<8>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
-    case 10: st = launch_L<10>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
-    case 12: st = launch_L<12>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
-    case 14: st = launch_L<14>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
-    case 16: st = launch_L<16>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out); break;
+    case 2: st = launch_L<2>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
+    case 4: st = launch_L<4>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
+    case 6: st = launch_L<6>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
+    case 8: st = launch_L<8>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
+    case 10: st = launch_L<10>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
+    case 12: st = launch_L<12>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
+    case 14: st = launch_L<14>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
+    case 16: st = launch_L<16>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
     default: return TQ_ERR_INVALID_ARG;
   }
   if (st == TQ_OK) count_launch(kCntGemv);

@@ -521,11 +521,11 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
                    static_cast<long long>(tq_grouped_min_tokens(top_k, E, gate_tile)), tile_m);
     });
   } else {
-    if (cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(n) * N, s) != cudaSuccess) {
-      cudaGetLastError();
-      return TQ_ERR_CUDA;
-    }
-    rc = launch_gemv(x, packed, lut, L, topk_ids, topk_w, n, top_k, E, K, N, y32, err, s);
+    // clear y32, then the GEMV, whose prologue (LUT and activation staging,
+    // first row) overlaps the clear
+    rc = launch_clear(y32, static_cast<int64_t>(n) * N, s);
+    if (rc != TQ_OK) return rc;
+    rc = launch_gemv(x, packed, lut, L, topk_ids, topk_w, n, top_k, E, K, N, y32, err, s, 0, 0, true);
     if (rc != TQ_OK) return rc;
   }
   return launch_combine(y32, y, static_cast<int64_t>(n) * N, s);
@@ -548,7 +548,7 @@ int tq_device_error(int* code, int* where) {
   return TQ_OK;
 }
 
-void tq_launch_counts(int64_t out[9]) {
+void tq_launch_counts(int64_t out[TQ_NUM_LAUNCH_COUNTERS]) {
   if (!out) return;
   for (int i = 0; i < kCntNum; ++i) out[i] = g_counts[i].load();
 }

@@ -20,8 +20,9 @@ int launch_status();
 
 enum Counter {
   kCntRoute = 0, kCntTileMap, kCntGrouped, kCntGemv, kCntCombine, kCntGather, kCntRouter, kCntDequant,
-  kCntRouteTileMap, kCntNum
+  kCntRouteTileMap, kCntClear, kCntSwiglu, kCntNum
 };
+static_assert(kCntNum == TQ_NUM_LAUNCH_COUNTERS, "counter layout of tq_launch_counts");
 void count_launch(Counter c);
 
 // Number of SMs of the current device (cached per device).
@@ -56,6 +57,8 @@ int launch_route(const int32_t* topk_ids, int P, int E, int32_t* counts, int32_t
 int launch_tile_map(const int32_t* offsets, int E, int tile_m, int32_t* tiles, int32_t* num_tiles,
                     int64_t cap, int* err, cudaStream_t s);
 int launch_combine(const float* y32, uint16_t* y, int64_t count, cudaStream_t s);
+// y[0 .. count) = 0 (fp32), as a programmatic dependent of the previous kernel.
+int launch_clear(float* y, int64_t count, cudaStream_t s);
 int launch_router(const float* logits, int n, int E, int top_k, int32_t* ids, float* w, cudaStream_t s);
 int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top_k, int K,
                   uint16_t* x_sorted, int* err, cudaStream_t s);
@@ -108,10 +111,14 @@ bool resolve_tile(int64_t n, int top_k, int E, int tile_m, int* kernel_tile, int
 int launch_swiglu(const float* gate_up, int64_t P, int I, uint16_t* h, cudaStream_t s);
 // pair_in: x holds one row per pair (x[pair]) instead of per token;
 // pair_out: out[pair][row] = the row's dot product (plain store, no router
-// weight) instead of y32[token][row] += w * dot.
+// weight) instead of y32[token][row] += w * dot.  Launched as a programmatic
+// dependent of the previous kernel; early_prologue: that kernel writes none
+// of x, topk_ids, the LUT or packed, so the kernel stages them (and loads its
+// first row) before waiting for it.
 int launch_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
                 const int32_t* topk_ids, const float* topk_w, int64_t n, int top_k, int E, int K,
-                int N, float* y32, int* err, cudaStream_t s, int pair_in = 0, int pair_out = 0);
+                int N, float* y32, int* err, cudaStream_t s, int pair_in = 0, int pair_out = 0,
+                bool early_prologue = false);
 // TQ_FORCE_ARM (auto|gemv|grouped|measured) applied to an automatic pin.
 int env_pin(int pin);
 

@@ -18,6 +18,8 @@ namespace {
 // h[s][i] = bf16(silu(g) * u), g = gate_up[s][i], u = gate_up[s][I + i],
 // silu(g) = g / (1 + e^-g); four elements per thread step.
 __global__ void swiglu_kernel(const float4* __restrict__ gate_up, long long P, int I4, uint2* __restrict__ h) {
+  pdl_wait();
+  pdl_trigger();
   const long long total = P * I4;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
@@ -49,9 +51,11 @@ int launch_swiglu(const float* gate_up, int64_t P, int I, uint16_t* h, cudaStrea
   const long long total = static_cast<long long>(P) * I4;
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<long long>((total + threads - 1) / threads, sm_count() * 8));
-  swiglu_kernel<<<blocks, threads, 0, s>>>(reinterpret_cast<const float4*>(gate_up), P, I4,
-                                           reinterpret_cast<uint2*>(h));
-  return launch_status();
+  int st = launch_pdl(swiglu_kernel, dim3(blocks), dim3(threads), 0, s, reinterpret_cast<const float4*>(gate_up), P,
+                      I4, reinterpret_cast<uint2*>(h));
+  if (st == TQ_OK) st = launch_status();
+  if (st == TQ_OK) count_launch(kCntSwiglu);
+  return st;
 }
 
 }  // namespace tq
@@ -161,12 +165,10 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
   if (arm == TQ_ARM_GEMV) {
     // per-pair GEMVs: gate|up per pair (plain stores), SwiGLU, down per pair
     // with the router weights into y32 (no routing sort, no tile map)
-    if (cudaMemsetAsync(y32, 0, sizeof(float) * static_cast<size_t>(n) * H, s) != cudaSuccess) {
-      cudaGetLastError();
-      return TQ_ERR_CUDA;
-    }
-    rc = launch_gemv(x, packed_gu, lut_gu, L, topk_ids, nullptr, n, top_k, E, H, 2 * I, gate_up, err, s,
-                     /*pair_in=*/0, /*pair_out=*/1);
+    rc = launch_clear(y32, static_cast<int64_t>(n) * H, s);
+    if (rc == TQ_OK)
+      rc = launch_gemv(x, packed_gu, lut_gu, L, topk_ids, nullptr, n, top_k, E, H, 2 * I, gate_up, err, s,
+                       /*pair_in=*/0, /*pair_out=*/1, /*early_prologue=*/true);
     if (rc == TQ_OK) rc = launch_swiglu(gate_up, static_cast<int64_t>(P), I, h, s);
     if (rc == TQ_OK)
       rc = launch_gemv(h, packed_down, lut_down, L, topk_ids, topk_w, n, top_k, E, I, H, y32, err, s,

@@ -202,6 +202,21 @@ route_tile_map_kernel(const int32_t* __restrict__ ids, int P, int E, int tile_m,
   tile_map_block(E, first, count, tile_m, tiles, num_tiles, cap, err);
 }
 
+// y[0 .. n) = 0: float4 stores over the 16-byte aligned middle, scalar
+// stores over the ragged head and tail.
+__global__ void clear_kernel(float* __restrict__ y, long long n) {
+  pdl_wait();
+  pdl_trigger();
+  const long long head = min(n, static_cast<long long>(((16 - (reinterpret_cast<uintptr_t>(y) & 15)) & 15) / 4));
+  const long long n4 = (n - head) / 4;
+  float4* y4 = reinterpret_cast<float4*>(y + head);
+  const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = tid; i < n4; i += stride) y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long i = tid; i < head; i += stride) y[i] = 0.f;
+  for (long long i = head + 4 * n4 + tid; i < n; i += stride) y[i] = 0.f;
+}
+
 __global__ void combine_kernel_v4(const float4* __restrict__ y32, uint2* __restrict__ y, long long n4) {
   pdl_wait();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
@@ -388,6 +403,18 @@ int launch_tile_map(const int32_t* offsets, int E, int tile_m, int32_t* tiles, i
                       static_cast<long long>(cap), err);
   if (st == TQ_OK) st = launch_status();
   if (st == TQ_OK) count_launch(kCntTileMap);
+  return st;
+}
+
+int launch_clear(float* y, int64_t count, cudaStream_t s) {
+  if (count <= 0) return TQ_OK;
+  const int threads = 256;
+  const long long per_block = 4ll * threads * 4;   // four float4 stores per thread
+  const int blocks = static_cast<int>(std::max<long long>(
+      1, std::min<long long>((count + per_block - 1) / per_block, 4ll * sm_count())));
+  int st = launch_pdl(clear_kernel, dim3(blocks), dim3(threads), 0, s, y, static_cast<long long>(count));
+  if (st == TQ_OK) st = launch_status();
+  if (st == TQ_OK) count_launch(kCntClear);
   return st;
 }
 
