@@ -185,6 +185,24 @@ def test_moe_forward_dirty_workspace(pin, tile_m):
         assert normwise(y.float().cpu().numpy(), ref) <= TOL
 
 
+def test_moe_forward_gemv_ragged_output():
+    """The GEMV arm of the whole product takes any N: 7 tokens x 130 rows is
+    an odd accumulator length, cleared and combined through the scalar head
+    and tail paths, from a NaN-filled workspace."""
+    prob = moe_inputs.make_custom(8, 2, 7, 256, 130, 12, seed=61)
+    d = to_device(prob)
+    s = prob.shape
+    ws = torch.empty(tq.tq_moe_workspace_size(s.n, s.top_k, s.E, s.K, s.N, 16) + 256, dtype=torch.uint8,
+                     device="cuda")
+    ws.fill_(0xFF)
+    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=16, pin=tq.ARM_GEMV,
+                               workspace=ws)
+    check_no_device_error()
+    assert arm == tq.ARM_GEMV
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L)
+    assert normwise(y.float().cpu().numpy(), ref) <= TOL
+
+
 def test_moe_forward_empty_batch():
     prob = moe_inputs.make_custom(8, 2, 4, 256, 128, 12, seed=3)
     d = to_device(prob)
