@@ -242,24 +242,36 @@ __global__ void combine_kernel_scalar(const float* __restrict__ y32, uint16_t* _
 }
 
 // x_sorted[slot] = x[sorted_pairs[slot] / top_k]: the activations in pair-sorted
-// order, 16 bytes per thread step; an out-of-range pair id yields a zero row.
+// order.  One warp per slot; each lane has four 16-byte loads in flight
+// before it stores them (row_vecs = K / 8 vectors per row).  An out-of-range
+// pair id yields a zero row and is reported.
 __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_pairs,
                                    int P, int top_k, int row_vecs, uint4* __restrict__ x_sorted, int* err) {
   pdl_wait();
   pdl_trigger();
-  const long long total = static_cast<long long>(P) * row_vecs;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int slot = static_cast<int>(i / row_vecs);
-    const int v = static_cast<int>(i - static_cast<long long>(slot) * row_vecs);
+  constexpr int kUnroll = 4;
+  const int lane = threadIdx.x & 31;
+  const long long warp = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long slot = warp; slot < P; slot += nwarps) {
     const int pair = sorted_pairs[slot];
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (pair >= 0 && pair < P) {
-      val = __ldg(x + static_cast<size_t>(pair / top_k) * row_vecs + v);
-    } else if (v == 0) {
-      record_error(err, TQ_ERR_INVALID_ARG, kWhereRoute);
+    const bool ok = pair >= 0 && pair < P;
+    if (!ok && lane == 0) record_error(err, TQ_ERR_INVALID_ARG, kWhereRoute);
+    const uint4* src = x + static_cast<size_t>(ok ? pair / top_k : 0) * row_vecs;
+    uint4* dst = x_sorted + static_cast<size_t>(slot) * row_vecs;
+    for (int v0 = 0; v0 < row_vecs; v0 += 32 * kUnroll) {
+      uint4 t[kUnroll];
+#pragma unroll
+      for (int j = 0; j < kUnroll; ++j) {
+        const int v = v0 + 32 * j + lane;
+        t[j] = (ok && v < row_vecs) ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < kUnroll; ++j) {
+        const int v = v0 + 32 * j + lane;
+        if (v < row_vecs) dst[v] = t[j];
+      }
     }
-    x_sorted[i] = val;
   }
 }
 
@@ -341,9 +353,9 @@ int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top
                   int* err, cudaStream_t s) {
   if (P == 0) return TQ_OK;
   const int row_vecs = K / 8;
-  const long long total = static_cast<long long>(P) * row_vecs;
-  const int threads = 256;
-  const int blocks = static_cast<int>(std::min<long long>((total + threads - 1) / threads, sm_count() * 8));
+  const int threads = 256;   // 8 warps, one slot each per pass
+  const int blocks = static_cast<int>(std::max<long long>(
+      1, std::min<long long>((static_cast<long long>(P) + 7) / 8, sm_count() * 8ll)));
   int st = launch_pdl(gather_rows_kernel, dim3(blocks), dim3(threads), 0, s, reinterpret_cast<const uint4*>(x),
                       sorted_pairs, P, top_k, row_vecs, reinterpret_cast<uint4*>(x_sorted), err);
   if (st == TQ_OK) st = launch_status();
