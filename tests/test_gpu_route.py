@@ -35,6 +35,11 @@ def _ids_cases():
         "E1_k1": (np.zeros((5, 1), np.int32), 1),
         "ragged_P_37x3": (moe_inputs.draw_routing(rng, 37, 5, 3)[0], 5),
         "empty": (np.zeros((0, 6), np.int32), 256),
+        # more than 8192 pairs: the sort is shared by several blocks (ragged
+        # chunks, one expert spanning every chunk, many experts)
+        "multi_one_expert_20000": (np.full((20000, 1), 3, np.int32), 8),
+        "multi_E1024_n3000_k8": (moe_inputs.draw_routing(rng, 3000, 1024, 8)[0], 1024),
+        "multi_ragged_9001x3": (moe_inputs.draw_routing(rng, 9001, 5, 3)[0], 5),
     }
     return cases
 
@@ -54,7 +59,8 @@ def test_route_bitexact(name):
     assert np.array_equal(sp.cpu().numpy(), s)
 
 
-@pytest.mark.parametrize("name", ["tiny", "v4_n32", "v4_zipf_n8192", "one_expert_all", "E1024", "ragged_P_37x3"])
+@pytest.mark.parametrize("name", ["tiny", "v4_n32", "v4_zipf_n8192", "one_expert_all", "E1024", "ragged_P_37x3",
+                                  "multi_E1024_n3000_k8"])
 @pytest.mark.parametrize("tile_m", [1, 7, 16, 64, 256])
 def test_tile_map_bitexact(name, tile_m):
     ids, E = CASES[name]
@@ -93,6 +99,27 @@ def test_route_flags_out_of_range_expert():
     assert code == -1 and where == 1
     c = counts.cpu().numpy()
     assert c.sum() == 5 and c[8 - 1] == 0
+    check_no_device_error()
+
+
+def test_route_multi_block_flags_out_of_range_expert():
+    """More than 8192 pairs with a few ids out of range: they are reported,
+    left out of the counts, and the rest sort exactly as the oracle sorts the
+    valid pairs."""
+    rng = np.random.Generator(np.random.PCG64(21))
+    ids = moe_inputs.draw_routing(rng, 4000, 16, 4)[0].copy()
+    ids[17, 2] = 16
+    ids[3999, 0] = -2
+    counts, offsets, sp = tq.tq_route(torch.from_numpy(ids).cuda(), 16)
+    torch.cuda.synchronize()
+    code, where = tq.tq_device_error()
+    assert code == -1 and where == 1
+    flat = ids.reshape(-1)
+    valid = np.flatnonzero((flat >= 0) & (flat < 16))
+    want = valid[np.argsort(flat[valid], kind="stable")]
+    c = counts.cpu().numpy()
+    assert c.sum() == len(valid)
+    assert np.array_equal(sp[:len(valid)].cpu().numpy(), want)
     check_no_device_error()
 
 

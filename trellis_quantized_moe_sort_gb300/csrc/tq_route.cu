@@ -56,89 +56,140 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total) {
   return excl;
 }
 
-// The routing sort of one block; thread e < E returns expert e's first sorted
-// slot in *first and its pair count in *count.
-__device__ __forceinline__ void route_block(const int32_t* __restrict__ ids, int P, int E,
+// The routing sort, by `sorters` blocks (block b of them handles the
+// contiguous pairs [P*b/sorters, P*(b+1)/sorters)); thread e < E of every
+// sorting block returns expert e's first sorted slot in *first and its pair
+// count in *count.  Each block counts its own chunk per warp (match.any
+// leaders), and with more than one block also counts every pair by shared
+// atomics: the totals per expert (every block derives the same offsets) and
+// the pairs before its chunk (its base inside each expert's range).  Ranks
+// follow (chunk, warp, lane) order, i.e. ascending pair ids: a stable sort.
+__device__ __forceinline__ void route_chunk(const int32_t* __restrict__ ids, int P, int E, int sorters,
                                             int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                             int32_t* __restrict__ sorted_pairs, int* err, int* first,
                                             int* count) {
-  extern __shared__ int32_t wcnt[];  // [kWarps][E]: per-warp count, then per-warp base
+  // [kWarps][E] per-warp count, then per-warp base; [E] totals; [E] pairs before the chunk
+  extern __shared__ int32_t wcnt[];
+  int32_t* tot = wcnt + kWarps * E;
+  int32_t* pre = tot + E;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < kWarps * E; i += kBlock) wcnt[i] = 0;
+  for (int i = threadIdx.x; i < (kWarps + 2) * E; i += kBlock) wcnt[i] = 0;
   __syncthreads();
 
-  const int per_warp = (((P + kWarps - 1) / kWarps) + 31) & ~31;
-  const int beg = min(P, warp * per_warp);
-  const int end = min(P, beg + per_warp);
+  const int b = blockIdx.x;
+  const int c0 = static_cast<int>(static_cast<long long>(P) * b / sorters);
+  const int c1 = static_cast<int>(static_cast<long long>(P) * (b + 1) / sorters);
+  const int per_warp = ((((c1 - c0) + kWarps - 1) / kWarps) + 31) & ~31;
+  const int beg = min(c1, c0 + warp * per_warp);
+  const int end = min(c1, beg + per_warp);
   int32_t* mine = wcnt + warp * E;
 
-  // 1. per-warp histogram of its slice
-  for (int base = beg; base < end; base += 32) {
-    const int p = base + lane;
-    int e = -1;
-    if (p < end) {
-      e = ids[p];
-      if (e < 0 || e >= E) {
+  // Expert ids, kBatch rows of 32 at a time: all of a batch's loads are in
+  // flight before the first is used.
+  constexpr int kBatch = 8;
+  auto load_batch = [&](int base, int lim, int (&eb)[kBatch]) {
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int p = base + 32 * i + lane;
+      eb[i] = p < lim ? ids[p] : -1;
+    }
+  };
+
+  // 0. (several blocks) totals and the prefix over all pairs
+  if (sorters > 1) {
+    for (int base = warp * 32; base < P; base += kBlock * kBatch) {
+      int eb[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int p = base + kBlock * i + lane;
+        eb[i] = p < P ? ids[p] : -1;
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int p = base + kBlock * i + lane;
+        const int e = eb[i];
+        if (e >= 0 && e < E) {
+          atomicAdd(&tot[e], 1);
+          if (p < c0) atomicAdd(&pre[e], 1);
+        }
+      }
+    }
+  }
+
+  // 1. per-warp histogram of its slice of the chunk
+  for (int base = beg; base < end; base += 32 * kBatch) {
+    int eb[kBatch];
+    load_batch(base, end, eb);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      int e = eb[i];
+      if (base + 32 * i + lane < end && (e < 0 || e >= E)) {   // past the slice: loaded as -1
         record_error(err, TQ_ERR_INVALID_ARG, kWhereRoute);
         e = -1;
       }
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+      __syncwarp();
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
-    __syncwarp();
   }
   __syncthreads();
 
-  // 2. totals per expert, exclusive scan over experts, per-warp bases
+  // 2. per expert: exclusive counts over this block's warps, the totals and
+  // their exclusive scan over experts, per-warp bases
   const int e = threadIdx.x;
-  int total = 0;
+  int own = 0;
   if (e < E) {
     for (int w = 0; w < kWarps; ++w) {
       const int c = wcnt[w * E + e];
-      wcnt[w * E + e] = total;
-      total += c;
+      wcnt[w * E + e] = own;
+      own += c;
     }
   }
+  const int total = sorters > 1 ? (e < E ? tot[e] : 0) : own;
+  const int before = sorters > 1 && e < E ? pre[e] : 0;
   int all = 0;
   const int excl = block_exclusive_scan(total, &all);
   if (e < E) {
-    counts[e] = total;
-    offsets[e] = excl;
-    for (int w = 0; w < kWarps; ++w) wcnt[w * E + e] += excl;
+    if (b == 0) {
+      counts[e] = total;
+      offsets[e] = excl;
+    }
+    for (int w = 0; w < kWarps; ++w) wcnt[w * E + e] += excl + before;
   }
-  if (threadIdx.x == 0) offsets[E] = all;
+  if (b == 0 && threadIdx.x == 0) offsets[E] = all;
   *first = excl;
   *count = e < E ? total : 0;
   __syncthreads();
 
   // 3. stable scatter: rank among equal experts of lower lanes, then advance
   const unsigned lower = (1u << lane) - 1u;
-  for (int base = beg; base < end; base += 32) {
-    const int p = base + lane;
-    int ex = -1;
-    if (p < end) {
-      ex = ids[p];
-      if (ex < 0 || ex >= E) ex = -1;
+  for (int base = beg; base < end; base += 32 * kBatch) {
+    int eb[kBatch];
+    load_batch(base, end, eb);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int p = base + 32 * i + lane;
+      const int ex = (eb[i] < 0 || eb[i] >= E) ? -1 : eb[i];
+      const unsigned peers = __match_any_sync(0xffffffffu, ex);
+      int slot = 0;
+      if (ex >= 0) slot = mine[ex] + __popc(peers & lower);
+      __syncwarp();
+      if (ex >= 0) {
+        sorted_pairs[slot] = p;
+        if (lane == __ffs(peers) - 1) mine[ex] += __popc(peers);
+      }
+      __syncwarp();
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, ex);
-    int slot = 0;
-    if (ex >= 0) slot = mine[ex] + __popc(peers & lower);
-    __syncwarp();
-    if (ex >= 0) {
-      sorted_pairs[slot] = p;
-      if (lane == __ffs(peers) - 1) mine[ex] += __popc(peers);
-    }
-    __syncwarp();
   }
 }
 
 __global__ void __launch_bounds__(kBlock, 1)
-route_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ counts,
+route_kernel(const int32_t* __restrict__ ids, int P, int E, int sorters, int32_t* __restrict__ counts,
              int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pairs, int* err) {
   pdl_wait();
   pdl_trigger();
   int first, count;
-  route_block(ids, P, E, counts, offsets, sorted_pairs, err, &first, &count);
+  route_chunk(ids, P, E, sorters, counts, offsets, sorted_pairs, err, &first, &count);
 }
 
 // The m-tile map of one block from expert e's (first slot, count) in thread e.
@@ -180,26 +231,28 @@ tile_map_kernel(const int32_t* __restrict__ offsets, int E, int tile_m, int32_t*
   tile_map_block(E, off, cnt, tile_m, tiles, num_tiles, cap, err);
 }
 
-// Route and tile map in one launch: the tile map takes each expert's slot
-// range from the sort's registers, not from memory.  Blocks after the first
-// clear zero4[0 .. zero_n4) (the fp32 accumulator of the grouped GEMM that
-// follows) meanwhile.
+// Route and tile map in one launch: the first `sorters` blocks sort, block 0
+// then builds the tile map from each expert's slot range held in registers;
+// the blocks after them clear zero4[0 .. zero_n4) (the fp32 accumulator of
+// the grouped GEMM that follows) meanwhile.
 __global__ void __launch_bounds__(kBlock, 1)
-route_tile_map_kernel(const int32_t* __restrict__ ids, int P, int E, int tile_m, int32_t* __restrict__ counts,
-                      int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pairs,
-                      int32_t* __restrict__ tiles, int32_t* __restrict__ num_tiles, long long cap, int* err,
-                      float4* __restrict__ zero4, long long zero_n4) {
+route_tile_map_kernel(const int32_t* __restrict__ ids, int P, int E, int sorters, int tile_m,
+                      int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                      int32_t* __restrict__ sorted_pairs, int32_t* __restrict__ tiles,
+                      int32_t* __restrict__ num_tiles, long long cap, int* err, float4* __restrict__ zero4,
+                      long long zero_n4) {
   pdl_wait();
   pdl_trigger();
-  if (blockIdx.x > 0) {
-    const long long stride = static_cast<long long>(gridDim.x - 1) * kBlock;
-    for (long long i = static_cast<long long>(blockIdx.x - 1) * kBlock + threadIdx.x; i < zero_n4; i += stride)
+  if (static_cast<int>(blockIdx.x) >= sorters) {
+    const long long stride = static_cast<long long>(gridDim.x - sorters) * kBlock;
+    for (long long i = static_cast<long long>(blockIdx.x - sorters) * kBlock + threadIdx.x; i < zero_n4;
+         i += stride)
       zero4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
   int first, count;
-  route_block(ids, P, E, counts, offsets, sorted_pairs, err, &first, &count);
-  tile_map_block(E, first, count, tile_m, tiles, num_tiles, cap, err);
+  route_chunk(ids, P, E, sorters, counts, offsets, sorted_pairs, err, &first, &count);
+  if (blockIdx.x == 0) tile_map_block(E, first, count, tile_m, tiles, num_tiles, cap, err);
 }
 
 // y[0 .. n) = 0: float4 stores over the 16-byte aligned middle, scalar
@@ -363,12 +416,21 @@ int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top
   return st;
 }
 
+// Blocks sharing the routing sort: one up to 8192 pairs (a block's own
+// histogram is all it needs), else one per 2048 pairs, at most 64.
+static int route_sorters(int P) {
+  if (P <= 8192) return 1;
+  return static_cast<int>(std::min<long long>(64, (static_cast<long long>(P) + 2047) / 2048));
+}
+
+static size_t route_smem(int E) { return sizeof(int32_t) * (kWarps + 2) * static_cast<size_t>(E); }
+
 int launch_route_tile_map(const int32_t* topk_ids, int P, int E, int tile_m, int32_t* counts, int32_t* offsets,
                           int32_t* sorted_pairs, int32_t* tiles, int32_t* num_tiles, int64_t cap, int* err,
                           cudaStream_t s, float* y32, int64_t y32_count) {
-  const size_t smem = sizeof(int32_t) * kWarps * E;
+  const size_t smem = route_smem(E);
   if (cudaFuncSetAttribute(route_tile_map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(sizeof(int32_t) * kWarps * 1024)) != cudaSuccess) {
+                           static_cast<int>(route_smem(1024))) != cudaSuccess) {
     cudaGetLastError();
     return TQ_ERR_CUDA;
   }
@@ -387,8 +449,9 @@ int launch_route_tile_map(const int32_t* topk_ids, int P, int E, int tile_m, int
   // one routing block, plus clearing blocks (16 float4 stores per thread, at
   // most two per SM)
   const long long clear_blocks = std::min<long long>((z4 + 16ll * kBlock - 1) / (16ll * kBlock), 2ll * sm_count());
-  int st = launch_pdl(route_tile_map_kernel, dim3(static_cast<unsigned>(1 + clear_blocks)), dim3(kBlock), smem, s,
-                      topk_ids, P, E, tile_m, counts, offsets, sorted_pairs, tiles, num_tiles,
+  const int sorters = route_sorters(P);
+  int st = launch_pdl(route_tile_map_kernel, dim3(static_cast<unsigned>(sorters + clear_blocks)), dim3(kBlock), smem,
+                      s, topk_ids, P, E, sorters, tile_m, counts, offsets, sorted_pairs, tiles, num_tiles,
                       static_cast<long long>(cap), err, reinterpret_cast<float4*>(y32), z4);
   if (st == TQ_OK) st = launch_status();
   if (st == TQ_OK) count_launch(kCntRouteTileMap);
@@ -397,13 +460,15 @@ int launch_route_tile_map(const int32_t* topk_ids, int P, int E, int tile_m, int
 
 int launch_route(const int32_t* topk_ids, int P, int E, int32_t* counts, int32_t* offsets,
                  int32_t* sorted_pairs, int* err, cudaStream_t s) {
-  const size_t smem = sizeof(int32_t) * kWarps * E;
+  const size_t smem = route_smem(E);
   if (cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(sizeof(int32_t) * kWarps * 1024)) != cudaSuccess) {
+                           static_cast<int>(route_smem(1024))) != cudaSuccess) {
     cudaGetLastError();
     return TQ_ERR_CUDA;
   }
-  int st = launch_pdl(route_kernel, dim3(1), dim3(kBlock), smem, s, topk_ids, P, E, counts, offsets, sorted_pairs, err);
+  const int sorters = route_sorters(P);
+  int st = launch_pdl(route_kernel, dim3(sorters), dim3(kBlock), smem, s, topk_ids, P, E, sorters, counts, offsets,
+                      sorted_pairs, err);
   if (st == TQ_OK) st = launch_status();
   if (st == TQ_OK) count_launch(kCntRoute);
   return st;
