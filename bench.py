@@ -758,7 +758,7 @@ def main(argv=None):
     ap.add_argument("--mlp-sweep", action="store_true", help="whole SwiGLU expert MLP per workload")
     ap.add_argument("--gate-ns", default="1,2,4,8,9,16,32,64,128,256,512,682,683,1024")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu dram bytes (read+write) per grouped launch, if captured for this build")
+                    help="ncu dram bytes (read+write) per grouped launch, if captured for the current kernel source")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -295,14 +295,16 @@ __global__ void combine_kernel_scalar(const float* __restrict__ y32, uint16_t* _
 }
 
 // x_sorted[slot] = x[sorted_pairs[slot] / top_k]: the activations in pair-sorted
-// order.  One warp per slot; each lane has four 16-byte loads in flight
-// before it stores them (row_vecs = K / 8 vectors per row).  An out-of-range
-// pair id yields a zero row and is reported.
+// order.  One warp per slot; each lane has eight 16-byte loads in flight
+// before it stores them (row_vecs = K / 8 vectors per row), and the stores
+// are marked streaming so that the copy, read once later, does not push x
+// (read top_k times) out of L2.  An out-of-range pair id yields a zero row
+// and is reported.
 __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_pairs,
                                    int P, int top_k, int row_vecs, uint4* __restrict__ x_sorted, int* err) {
   pdl_wait();
   pdl_trigger();
-  constexpr int kUnroll = 4;
+  constexpr int kUnroll = 8;
   const int lane = threadIdx.x & 31;
   const long long warp = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -322,7 +324,7 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* _
 #pragma unroll
       for (int j = 0; j < kUnroll; ++j) {
         const int v = v0 + 32 * j + lane;
-        if (v < row_vecs) dst[v] = t[j];
+        if (v < row_vecs) __stcs(dst + v, t[j]);
       }
     }
   }
