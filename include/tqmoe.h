@@ -328,7 +328,8 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
  * TQ_STATIC_SCRATCH_BYTES (16 MiB) that every GPU loading this library holds
  * until the process exits; a shape whose tq_moe_workspace_size() exceeds it
  * is rejected with TQ_ERR_WORKSPACE before anything is launched (at
- * K = 4096, N = 2048, top-6 that is n > 2040 tokens).  The call allocates nothing (no cudaMalloc,
+ * K = 4096, N = 2048, top-6 that is n > 2040 tokens at tile_m 16, where the kernel gathers its own
+ * rows, and n > 292 with larger m-tiles, which add the pair-sorted copy of x).  The call allocates nothing (no cudaMalloc,
  * no cudaFree, no allocating library routine).
  *
  * The first call on a device looks up the array's device address with that
