@@ -87,26 +87,27 @@ __device__ __forceinline__ void route_chunk(const int32_t* __restrict__ ids, int
   // Expert ids, kBatch rows of 32 at a time: all of a batch's loads are in
   // flight before the first is used.
   constexpr int kBatch = 8;
-  auto load_batch = [&](int base, int lim, int (&eb)[kBatch]) {
+  // (positions are 64-bit: a batch may run past 2^31 - 1 at the end of the list)
+  auto load_batch = [&](long long base, int lim, int (&eb)[kBatch]) {
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
-      const int p = base + 32 * i + lane;
+      const long long p = base + 32 * i + lane;
       eb[i] = p < lim ? ids[p] : -1;
     }
   };
 
   // 0. (several blocks) totals and the prefix over all pairs
   if (sorters > 1) {
-    for (int base = warp * 32; base < P; base += kBlock * kBatch) {
+    for (long long base = warp * 32; base < P; base += kBlock * kBatch) {
       int eb[kBatch];
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
-        const int p = base + kBlock * i + lane;
+        const long long p = base + kBlock * i + lane;
         eb[i] = p < P ? ids[p] : -1;
       }
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
-        const int p = base + kBlock * i + lane;
+        const long long p = base + kBlock * i + lane;
         const int e = eb[i];
         if (e >= 0 && e < E) {
           atomicAdd(&tot[e], 1);
@@ -117,7 +118,7 @@ __device__ __forceinline__ void route_chunk(const int32_t* __restrict__ ids, int
   }
 
   // 1. per-warp histogram of its slice of the chunk
-  for (int base = beg; base < end; base += 32 * kBatch) {
+  for (long long base = beg; base < end; base += 32 * kBatch) {
     int eb[kBatch];
     load_batch(base, end, eb);
 #pragma unroll
@@ -163,19 +164,19 @@ __device__ __forceinline__ void route_chunk(const int32_t* __restrict__ ids, int
 
   // 3. stable scatter: rank among equal experts of lower lanes, then advance
   const unsigned lower = (1u << lane) - 1u;
-  for (int base = beg; base < end; base += 32 * kBatch) {
+  for (long long base = beg; base < end; base += 32 * kBatch) {
     int eb[kBatch];
     load_batch(base, end, eb);
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
-      const int p = base + 32 * i + lane;
+      const long long p = base + 32 * i + lane;
       const int ex = (eb[i] < 0 || eb[i] >= E) ? -1 : eb[i];
       const unsigned peers = __match_any_sync(0xffffffffu, ex);
       int slot = 0;
       if (ex >= 0) slot = mine[ex] + __popc(peers & lower);
       __syncwarp();
       if (ex >= 0) {
-        sorted_pairs[slot] = p;
+        sorted_pairs[slot] = static_cast<int32_t>(p);   // p < end <= P < 2^31
         if (lane == __ffs(peers) - 1) mine[ex] += __popc(peers);
       }
       __syncwarp();
