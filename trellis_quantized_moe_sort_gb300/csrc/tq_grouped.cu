@@ -16,10 +16,11 @@
 //               rows x 128 bytes (512 symbols = 8 k-steps of 64) per
 //               "super-stage", 128B-swizzled; wide rows keep the TMA unit's
 //               per-row cost low.
-//   warp 14     TMA producer for activations: the pair-sorted copy of x puts a
-//               tile's rows next to each other, so one 128B-swizzled box of
-//               64 columns x (tile_m rounded up to 16) rows per k-step lands
-//               directly in the MMA's B layout.
+//   warp 14     TMA producer for activations, 64 columns per k-step into the
+//               MMA's 128B-swizzled B layout: gathered from the token rows of
+//               x, four rows per copy (small m-tiles), or, from the
+//               pair-sorted copy of x, one box of (tile_m rounded up to 16)
+//               consecutive rows.
 //   warp 1      MMA issuer: tcgen05.mma kind::f16, A = decoded weights in tensor
 //               memory (M = 128 rows), B = activations in shared memory
 //               (N = pairs of the tile padded to 16), fp32 accumulator in
