@@ -128,6 +128,13 @@ int64_t tq_grouped_min_tokens(int top_k, int E, int tile_m);
  * pages' TILE_M (TQ_GATE_TILE_M).  Negative on invalid arguments. */
 #define TQ_TILE_NATIVE 0
 #define TQ_GATE_TILE_M 16
+/* Environment (read at each call):
+ *   TQ_FORCE_ARM=auto|gemv|grouped|measured  replaces pin = TQ_ARM_AUTO in the
+ *       whole-product calls (the pages' env pin of the GEMV arm).
+ *   TQ_TILE_M=1..256  the kernel m-tile of whole-product calls made with
+ *       tile_m = TQ_TILE_NATIVE (the arm selection keeps TQ_GATE_TILE_M).
+ *   TQ_QUIET=1  no engagement log line.
+ * An unrecognised value is ignored with one warning on stderr. */
 int tq_native_tile_m(int64_t n, int top_k, int E);
 
 /* Upper bound on the number of m-tiles sum_e ceil(count_e / tile_m) for ANY

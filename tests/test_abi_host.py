@@ -95,6 +95,22 @@ def test_host_functions_reject_invalid_arguments(tq):
         + a256(32 * 256 * 2))
 
 
+def test_env_tile_m_overrides_native_tile(tq, monkeypatch):
+    """TQ_TILE_M sets the kernel m-tile of TILE_NATIVE calls (seen in the
+    workspace they need); 0, out-of-range and non-numeric values leave the
+    native tile."""
+    n, k, E, K, N = 512, 6, 256, 4096, 2048
+    native = tq.tq_moe_workspace_size(n, k, E, K, N, 0)
+    assert native == tq.tq_moe_workspace_size(n, k, E, K, N, tq.tq_native_tile_m(n, k, E))
+    monkeypatch.setenv("TQ_TILE_M", "16")
+    assert tq.tq_moe_workspace_size(n, k, E, K, N, 0) == tq.tq_moe_workspace_size(n, k, E, K, N, 16)
+    assert tq.tq_moe_workspace_size(n, k, E, K, N, 0) != native
+    assert tq.tq_moe_mlp_workspace_size(n, k, E, K, N, 0) == tq.tq_moe_mlp_workspace_size(n, k, E, K, N, 16)
+    for bad in ("0", "257", "-3", "x16", ""):
+        monkeypatch.setenv("TQ_TILE_M", bad)
+        assert tq.tq_moe_workspace_size(n, k, E, K, N, 0) == native, bad
+
+
 def test_native_tile(tq):
     """TQ_TILE_NATIVE: 16 while the expected pairs per woken expert stay at
     most 4, 128 above, 256 once they reach 128 (the oracle's closed form

@@ -161,11 +161,28 @@ int sm_count() {
   return v;
 }
 
+// TQ_TILE_M=<1..256>: the kernel m-tile of whole-product calls made with
+// TQ_TILE_NATIVE (0 or unset: the native tile; anything else is ignored with
+// one warning).
+static int env_tile_m() {
+  const char* v = std::getenv("TQ_TILE_M");
+  if (!v || !*v) return 0;
+  char* endp = nullptr;
+  const long t = std::strtol(v, &endp, 10);
+  if (endp && *endp == '\0' && t >= 0 && t <= 256) return static_cast<int>(t);
+  static std::once_flag warned;
+  std::call_once(warned, [v] {
+    std::fprintf(stderr, "tqmoe: ignoring TQ_TILE_M=%s (expected 0..256)\n", v);
+  });
+  return 0;
+}
+
 bool resolve_tile(int64_t n, int top_k, int E, int tile_m, int* kernel_tile, int* gate_tile) {
   if (tile_m == TQ_TILE_NATIVE) {
     const int t = tq_native_tile_m(n, top_k, E);
     if (t < 0) return false;
-    *kernel_tile = t;
+    const int forced = env_tile_m();
+    *kernel_tile = forced > 0 ? forced : t;
     *gate_tile = TQ_GATE_TILE_M;
     return true;
   }

@@ -105,8 +105,9 @@ MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K
                              int kernel_tile_m);
 
 // tile_m of the whole-product calls: 1..256 for both the arm selection and the
-// kernel, or TQ_TILE_NATIVE (the kernel's native tile, the pages' TILE_M for
-// the selection).  Returns false on an invalid value.
+// kernel, or TQ_TILE_NATIVE (the kernel's native tile or TQ_TILE_M from the
+// environment, the pages' TILE_M for the selection).  Returns false on an
+// invalid value.
 bool resolve_tile(int64_t n, int top_k, int E, int tile_m, int* kernel_tile, int* gate_tile);
 int launch_swiglu(const float* gate_up, int64_t P, int I, uint16_t* h, cudaStream_t s);
 // pair_in: x holds one row per pair (x[pair]) instead of per token;
