@@ -95,6 +95,33 @@ def test_host_functions_reject_invalid_arguments(tq):
         + a256(32 * 256 * 2))
 
 
+def test_device_calls_reject_bad_arguments_before_any_device_work(tq):
+    """Argument checks come first: with no GPU present, a bad layout, size,
+    window width, m-tile or workspace is reported as such (the addresses
+    below are never dereferenced)."""
+    lib = tq.lib()
+    A = 0x10000            # 16-byte aligned stand-in address
+
+    def gg(x_layout=0, L=16, K=256, N=128, tile_m=16):
+        return lib.tq_grouped_gemm(A, x_layout, A, A, L, A, A, A, A, 16, 4, 2, 8, K, N, tile_m, A, None)
+
+    INVALID, WORKSPACE = -1, -8
+    assert gg(x_layout=7) == INVALID
+    assert gg(N=100) == INVALID           # the grouped arm needs N % 128 == 0
+    assert gg(K=100) == INVALID           # K % 64 != 0
+    assert gg(L=15) == INVALID            # odd window
+    assert gg(L=18) == INVALID            # window wider than 16 bits
+    assert gg(tile_m=0) == INVALID and gg(tile_m=257) == INVALID
+    assert lib.tq_grouped_gemm_dense(A, 5, A, A, A, A, A, 16, 4, 2, 8, 256, 128, 16, A, None) == INVALID
+    arm = ctypes.c_int(-1)
+    # grouped pin with a workspace one byte short
+    need = tq.tq_moe_workspace_size(4, 2, 8, 256, 128, 16)
+    rc = lib.tq_moe_forward(A, A, A, 12, A, A, 4, 2, 8, 256, 128, 16, 2, A, need - 1, A, ctypes.byref(arm), None)
+    assert rc == WORKSPACE
+    rc = lib.tq_moe_forward(A, A, A, 12, A, A, 4, 2, 8, 256, 128, 16, 9, A, need, A, ctypes.byref(arm), None)
+    assert rc == INVALID                  # unknown pin
+
+
 def test_env_tile_m_overrides_native_tile(tq, monkeypatch):
     """TQ_TILE_M sets the kernel m-tile of TILE_NATIVE calls (seen in the
     workspace they need); 0, out-of-range and non-numeric values leave the
