@@ -15,15 +15,13 @@ from __future__ import annotations
 
 import os
 
-# the CPU baseline (the numpy oracle) runs on exactly one core: pin every BLAS
-# and OpenMP pool before numpy loads, so its reported "cores": 1 holds
-for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
-    os.environ[_v] = "1"
-
 import argparse
+import concurrent.futures
 import json
 import math
+import multiprocessing
 import platform
+import shutil
 import subprocess
 import sys
 import tempfile
@@ -40,6 +38,9 @@ import moe_inputs  # noqa: E402
 METRIC = "trellis-MoE grouped GEMM us/call, pairs/s, packed-weight GB/s vs roofline"
 DEFAULT_WORKLOAD = "v4_decode_n32"
 NUM_WEIGHT_SETS = 4
+# the 8192-token prefill projections (Zipf routing), timed beside the headline
+PREFILL_WORKLOADS = ("v4_prefill_n8192_up", "v4_prefill_n8192_down")
+BLAS_THREAD_VARS = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
 
 
 # --------------------------------------------------------------- traffic model
@@ -273,23 +274,36 @@ def run_ours(args, rank, world, dist):
 
     # ---- end to end through the public call with host buffers
     e2e = run_e2e(args, tq, torch, sets, n, k, E, K, N, T)
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    del sets, ws, x_sorted, y32, y
+    torch.cuda.empty_cache()
+
+    # ---- the 8192-token prefill projections at the native m-tile
+    prefill = None
+    if args.prefill:
+        prefill = {}
+        for name in PREFILL_WORKLOADS:
+            prefill[name] = run_prefill_leg(args, tq, torch, name, local, lut_rate, sms, dist)
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return None
+    # each grouped launch is timed on its own (events around it): the burst
+    # tensor peak is the matching denominator
     hbm, bf16, bf16_sus, peak_src = measured_peaks()
     alg_bytes = grouped_algorithmic_bytes(int(round(mean_tiles)), n, k, K, N, L)
     achieved = alg_bytes / (grouped_ms * 1e-3) / 1e9
     flops = grouped_flops(n, k, K, N)
     t_hbm_us = alg_bytes / (hbm * 1e9) * 1e6
-    t_tc_us = flops / (bf16_sus * 1e12) * 1e6
+    t_tc_us = flops / (bf16 * 1e12) * 1e6
     bound = "hbm" if t_hbm_us >= t_tc_us else "tensor"
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4)}
     else:
         tf = flops / (grouped_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(tf, 2), "peak": bf16_sus, "unit": "TFLOP/s",
-                "frac": round(tf / bf16_sus, 4)}
+        roof = {"bound": "tensor", "achieved": round(tf, 2), "peak": bf16, "unit": "TFLOP/s",
+                "frac": round(tf / bf16, 4)}
     traffic = args.traffic if args.traffic is not None else recorded_traffic(args.workload)
     roof.update({"traffic": traffic, "peak_source": peak_src, "kernel": "grouped_kernel",
                  "algorithmic_bytes": alg_bytes, "kernel_us": round(grouped_ms * 1e3, 2)})
@@ -320,15 +334,120 @@ def run_ours(args, rank, world, dist):
         "packed_GBps": round(mean_tiles * N * K / 4 / (grouped_ms * 1e-3) / 1e9, 1),
         "grouped_kernel_us": round(grouped_ms * 1e3, 2),
         "roofline": roof,
-        "decode_ceiling": decode_ceiling(mean_tiles, N, K, clk, lut_rate, grouped_ms * 1e3,
-                                         torch.cuda.get_device_properties(local).multi_processor_count),
+        "decode_ceiling": decode_ceiling(mean_tiles, N, K, clk, lut_rate, grouped_ms * 1e3, sms),
         "gpu_launches": int(launches),
         "clocks": clk,
         "e2e": e2e,
     }
+    if prefill is not None:
+        line["prefill"] = prefill
     if args.cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, sets[0]["prob"], budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.workload, moe_inputs.make_problem(args.workload, layer=0),
+                                            budget_s=args.cpu_seconds)
     return line
+
+
+def run_prefill_leg(args, tq, torch, name, local, lut_rate, sms, dist):
+    """One 8192-token prefill projection (Zipf routing) as a caller runs it:
+    tq_moe_forward at the native m-tile on the grouped arm, inputs resident
+    (512 MiB of packed weights per call, all 256 experts woken: larger than
+    L2).  The whole call is timed over the steps; then the same steps from
+    the separate calls with CUDA events around each grouped launch.  Clocks
+    are sampled throughout.  The roofline is the dense bf16 tensor roofline
+    (2 * pairs * K * N flops) against the measured burst peak, since each
+    launch is timed on its own."""
+    prob = moe_inputs.make_problem(name)
+    s = prob.shape
+    n, k, E, K, N, L = s.n, s.top_k, s.E, s.K, s.N, s.L
+    P = n * k
+    d = {"x": _cuda(torch, prob.x_bits.view(np.int16)), "ids": _cuda(torch, prob.topk_ids),
+         "w": _cuda(torch, prob.topk_w), "packed": _cuda(torch, prob.packed),
+         "lut": _cuda(torch, prob.lut_bits.view(np.int16))}
+    del prob
+    T = tq.tq_native_tile_m(n, k, E)
+    cap = tq.tq_tile_map_capacity(n, k, E, T)
+    ws = torch.empty(tq.tq_moe_workspace_size(n, k, E, K, N, tq.TILE_NATIVE), dtype=torch.uint8, device="cuda")
+    y = torch.empty((n, N), dtype=torch.bfloat16, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    sp = torch.empty(P, dtype=torch.int32, device="cuda")
+    tiles = torch.empty((cap, 3), dtype=torch.int32, device="cuda")
+    nt = torch.empty(1, dtype=torch.int32, device="cuda")
+    y32 = torch.empty((n, N), dtype=torch.float32, device="cuda")
+    lay = tq.X_TOKENS if T <= tq.GATHER_MAX_TILE_M else tq.X_PAIR_SORTED
+    xs = None if lay == tq.X_TOKENS else torch.empty((P, K), dtype=torch.int16, device="cuda")
+    stream = torch.cuda.current_stream()
+    steps = args.prefill_steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+
+    def call():
+        tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=tq.TILE_NATIVE,
+                          pin=tq.ARM_GROUPED, workspace=ws, y=y)
+
+    def kernel(ev=None):
+        tq.tq_prepare(d["ids"], d["x"], E, T, cap, counts, offsets, sp, tiles, nt, xs, y32)
+        if ev is not None:
+            ev[0].record(stream)
+        tq.tq_grouped_gemm(d["x"] if xs is None else xs, d["packed"], d["lut"], sp, d["w"], tiles, nt, k, T, y32,
+                           x_layout=lay)
+        if ev is not None:
+            ev[1].record(stream)
+        tq.tq_combine(y32, y)
+
+    for _ in range(args.warmup):
+        call()
+        kernel()
+    torch.cuda.synchronize()
+    code, where = tq.tq_device_error()
+    if code:
+        raise RuntimeError(f"device error {code} at {where} during {name} warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        call()
+    t1.record(stream)
+    for i in range(steps):
+        kernel(evs[i])
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    code, where = tq.tq_device_error()
+    if code:
+        raise RuntimeError(f"device error {code} at {where} during {name}")
+    us_call = t0.elapsed_time(t1) / steps * 1e3
+    kern_us = float(np.mean([a.elapsed_time(b_) for a, b_ in evs])) * 1e3
+    if dist is not None:
+        us_call, kern_us = max_over_ranks([us_call, kern_us], dist, "cuda")
+    ntiles = int(nt.item())
+    _, bf16, _, peak_src = measured_peaks()
+    flops = grouped_flops(n, k, K, N)
+    tf = flops / (kern_us * 1e-6) / 1e12
+    lookups = ntiles * N * K
+    mhz = (clk or {}).get("sm_mhz") or 2070.0
+    ceiling_us = lookups / (sms * mhz * 1e6 * lut_rate) * 1e6
+    return {
+        "workload": f"{name}: E={E} top-{k} (Zipf s={s.zipf_s}), n={n} tokens ({P} pairs), K={K} -> N={N}, "
+                    f"2-bit trellis L={L}, kernel TILE_M={T} (native)",
+        "api": "tq_moe_forward (tile_m=TQ_TILE_NATIVE, pin=grouped)",
+        "tile_m": T, "m_tiles": ntiles, "steps": steps,
+        "us_per_call": round(us_call, 1),
+        "grouped_kernel_us": round(kern_us, 1),
+        "pairs_per_s": round(P / (us_call * 1e-6), 1),
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": bf16, "unit": "TFLOP/s",
+                     "frac": round(tf / bf16, 4), "peak_kind": "burst (each launch timed on its own)",
+                     "peak_source": peak_src, "kernel": "grouped_kernel", "flops": flops,
+                     "traffic": recorded_traffic(name)},
+        "lookups": lookups,
+        "decode_ceiling": {"ceiling_us": round(ceiling_us, 1), "frac": round(ceiling_us / kern_us, 4),
+                           "lookups_per_clk_per_sm_measured": round(lut_rate, 3)},
+        "l2": "inputs larger than L2: 512 MiB of packed weights per call (every expert woken)",
+        "clocks": clk,
+    }
 
 
 def decode_ceiling(mean_tiles, N, K, clk, rate, kernel_us, sms):
@@ -409,37 +528,139 @@ def run_e2e(args, tq, torch, sets, n, k, E, K, N, T):
 
 # --------------------------------------------------------------- CPU oracle
 
-def cpu_baseline(workload, prob, budget_s=15.0, rows_per_call=None):
-    """The CPU oracle on the host, one core, on a bounded sample: all pairs of
-    the batch against a subset of output rows; the time scales linearly in the
-    rows, so us/call = time x N / rows."""
+_ORACLE = {}
+
+
+def _oracle_worker_init(folder, L):
+    """Worker set-up: the batch's arrays, memory-mapped from the files the
+    parent wrote (the packed weights are read only for the rows a task asks)."""
+    for key in ("x", "ids", "w", "packed", "lut"):
+        _ORACLE[key] = np.load(os.path.join(folder, key + ".npy"), mmap_mode="r")
+    _ORACLE["L"] = L
+
+
+def _oracle_worker_rows(rows):
+    """One task: the oracle's product for every pair of the batch on the given
+    output rows; returns the seconds it took on this worker's core."""
     import oracle.trellis_moe as O
-    s = prob.shape
-    rows_per_call = rows_per_call or 16
-    rng = np.random.Generator(np.random.PCG64(1))
-    done_rows, t_total = 0, 0.0
-    while t_total < budget_s and done_rows < s.N:
-        rows = np.sort(rng.choice(s.N, size=rows_per_call, replace=False))
+    d = _ORACLE
+    t0 = time.perf_counter()
+    O.moe_forward(d["x"], d["ids"], d["w"], d["packed"], d["lut"], d["L"], rows=np.asarray(rows))
+    return time.perf_counter() - t0
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
+
+
+class OraclePool:
+    """The CPU oracle, as it stands, on every host core: one worker process
+    per core (started with spawn; single-threaded BLAS each, so the workers
+    do not oversubscribe the cores), each computing a slice of the output rows
+    of the same batch.  Throughput = output rows finished / wall time, scaled
+    to the whole call (the oracle's cost is linear in the rows)."""
+
+    def __init__(self, prob, cores=None):
+        self.prob = prob
+        self.cores = max(1, int(cores or os.cpu_count() or 1))
+        self.dir = tempfile.mkdtemp(prefix="tq_oracle_")
+        for key, arr in (("x", prob.x_bits), ("ids", prob.topk_ids), ("w", prob.topk_w),
+                         ("packed", prob.packed), ("lut", prob.lut_bits)):
+            np.save(os.path.join(self.dir, key + ".npy"), np.ascontiguousarray(arr))
+        saved = {v: os.environ.get(v) for v in BLAS_THREAD_VARS}
+        for v in BLAS_THREAD_VARS:
+            os.environ[v] = "1"                      # inherited by the spawned workers
+        try:
+            self.pool = concurrent.futures.ProcessPoolExecutor(
+                self.cores, mp_context=multiprocessing.get_context("spawn"),
+                initializer=_oracle_worker_init, initargs=(self.dir, prob.shape.L))
+        finally:
+            for v, old in saved.items():
+                if old is None:
+                    os.environ.pop(v, None)
+                else:
+                    os.environ[v] = old
+        # start every worker (imports, first call) outside any timed sample
+        list(self.pool.map(_oracle_worker_rows, [[0]] * self.cores))
+
+    def sample(self, budget_s, rows_per_task=16, seed=1):
+        """Row slices on all workers until `budget_s` of wall time has passed
+        (then the tasks in flight finish).  Returns (wall s, rows done, summed
+        per-task seconds)."""
+        N = self.prob.shape.N
+        order = np.random.Generator(np.random.PCG64(seed)).permutation(N)
+        chunks = [np.sort(order[i:i + rows_per_task]).tolist() for i in range(0, N, rows_per_task)]
+        pending, done_rows, busy, nxt = {}, 0, 0.0, 0
         t0 = time.perf_counter()
-        O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L, rows=rows)
-        t_total += time.perf_counter() - t0
-        done_rows += rows_per_call
-    us_call = t_total / done_rows * s.N * 1e6
-    return {"value": round(us_call, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
-            "sample": f"{workload}: all {s.pairs} pairs x {done_rows} of {s.N} output rows "
-                      f"({t_total:.1f} s), scaled by N/rows",
-            "cpu": platform.processor() or platform.machine()}
+        while True:
+            while len(pending) < 2 * self.cores and time.perf_counter() - t0 < budget_s:
+                rows = chunks[nxt % len(chunks)]
+                nxt += 1
+                pending[self.pool.submit(_oracle_worker_rows, rows)] = len(rows)
+            if not pending:
+                break
+            finished, _ = concurrent.futures.wait(list(pending), return_when=concurrent.futures.FIRST_COMPLETED)
+            for f in finished:
+                busy += f.result()
+                done_rows += pending.pop(f)
+        return time.perf_counter() - t0, done_rows, busy
+
+    def close(self):
+        self.pool.shutdown(wait=True)
+        shutil.rmtree(self.dir, ignore_errors=True)
+
+
+def cpu_baseline(workload, prob, budget_s=15.0, pool=None):
+    """The CPU oracle on every host core, on a bounded sample of the batch:
+    all its pairs against as many output rows as the budget allows (rows
+    cycle through a fixed permutation); us/call = wall time x N / rows.  The
+    one-core figure (summed per-task seconds x N / rows) is reported beside."""
+    own = pool is None
+    pool = pool or OraclePool(prob)
+    try:
+        wall, rows, busy = pool.sample(budget_s)
+    finally:
+        if own:
+            pool.close()
+    s = prob.shape
+    return {"value": round(wall / rows * s.N * 1e6, 1), "unit": "us/call", "cores": pool.cores, "kind": "oracle",
+            "sample": f"{workload}: all {s.pairs} pairs x {rows} output rows (of {s.N}, cycling) on "
+                      f"{pool.cores} worker processes in {wall:.1f} s wall, scaled by N/rows",
+            "cpu": cpu_model(),
+            "one_core_us_per_call": round(busy / rows * s.N * 1e6, 1)}
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle on every host core, each step a
+    bounded sample of the workload (rank 0 only)."""
     if rank != 0:
         return None
     prob = moe_inputs.make_problem(args.workload)
     per_step = []
-    for i in range(args.warmup + args.steps):
-        r = cpu_baseline(args.workload, prob, budget_s=max(1.0, args.cpu_seconds / max(args.steps, 1)))
-        if i >= args.warmup:
-            per_step.append(r)
+    pool = OraclePool(prob)
+    try:
+        for i in range(args.warmup + args.steps):
+            r = cpu_baseline(args.workload, prob, budget_s=max(0.5, args.cpu_seconds / max(args.steps, 1)),
+                             pool=pool)
+            if i >= args.warmup:
+                per_step.append(r)
+    finally:
+        pool.close()
     value = float(np.mean([r["value"] for r in per_step]))
     s = prob.shape
     return {
@@ -449,8 +670,10 @@ def run_reference(args, rank, world):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": f"{args.workload}: E={s.E} top-{s.top_k}, n={s.n}, K={s.K} -> N={s.N}, "
                                f"L={s.L}, TILE_M={args.tile_m}"},
-        "cpu_baseline": {"value": round(value, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
-                         "sample": per_step[0]["sample"]},
+        "cpu_baseline": {"value": round(value, 1), "unit": "us/call", "cores": per_step[0]["cores"],
+                         "kind": "oracle", "sample": per_step[0]["sample"], "cpu": per_step[0]["cpu"],
+                         "one_core_us_per_call": round(float(np.mean([r["one_core_us_per_call"]
+                                                                      for r in per_step])), 1)},
         "e2e": {"value": round(value, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -471,6 +694,10 @@ def run_sweep(args):
     for name in names:
         prob = moe_inputs.make_problem(name)
         s = prob.shape
+        lines = []
+        clocks = ClockSampler(0)
+        clocks.start()
+        time.sleep(0.3)
         d = {"x": _cuda(torch, prob.x_bits.view(np.int16)), "ids": _cuda(torch, prob.topk_ids),
              "w": _cuda(torch, prob.topk_w), "packed": _cuda(torch, prob.packed),
              "lut": _cuda(torch, prob.lut_bits.view(np.int16))}
@@ -568,7 +795,7 @@ def run_sweep(args):
             alg = grouped_algorithmic_bytes(m_tiles, s.n, s.top_k, s.K, s.N, s.L)
             flops = grouped_flops(s.n, s.top_k, s.K, s.N)
             t_hbm = alg / (hbm * 1e9) * 1e6
-            t_tc = flops / (bf16_sus * 1e12) * 1e6
+            t_tc = flops / (bf16 * 1e12) * 1e6        # each launch timed alone: the burst peak
             lookups = (ntiles if ntiles is not None else s.pairs) * s.N * s.K
             if arm == "dequant":
                 lookups = woken * s.N * s.K
@@ -576,14 +803,17 @@ def run_sweep(args):
             extra["dispatch_measured"] = {1: "gemv", 2: "grouped"}[tq.tq_select_arm(s.n, s.top_k, s.E, 16,
                                                                                     tq.ARM_MEASURED)]
             extra["native_tile_m"] = tq.tq_native_tile_m(s.n, s.top_k, s.E)
-            print(json.dumps({**extra, 
+            lines.append(({**extra, 
                 "workload": name, "arm": arm, "tile_m": T, "n": s.n, "pairs": s.pairs, "woken": woken,
                 "m_tiles": ntiles, "us": round(us, 1), "pairs_per_s": round(s.pairs / (us * 1e-6), 1),
                 "staged_packed_GBps": round(staged / (us * 1e-6) / 1e9, 1),
                 "roofline_us": round(max(t_hbm, t_tc), 1), "bound": "hbm" if t_hbm >= t_tc else "tensor",
                 "frac": round(max(t_hbm, t_tc) / us, 4),
                 "decode_lookups_per_clk_per_sm": round(lookups / (us * 1e-6) / 152 / 2.07e9, 2),
-                "peak_source": peak_src}), flush=True)
+                "peak_source": peak_src, "peak_kind": "burst"}))
+        clk = clocks.stop()
+        for line in lines:
+            print(json.dumps({**line, "clocks": clk}), flush=True)
         del d, y32, w_dense
         torch.cuda.empty_cache()
 
@@ -638,6 +868,9 @@ def run_gate_study(args):
                 ts.append(a.elapsed_time(b_) * 1e3)
             return float(np.median(ts))
 
+        clocks = ClockSampler(0)
+        clocks.start()
+        time.sleep(0.3)
         row = {"n": n, "pairs": n * s.top_k, "woken": int(len(np.unique(prob.topk_ids))),
                "pairs_per_woken_expert": round(tq.tq_pairs_per_woken_expert(n, s.top_k, s.E), 3),
                "predicate_arm_T16": {1: "gemv", 2: "grouped"}[tq.tq_select_arm(n, s.top_k, s.E, 16)],
@@ -662,6 +895,7 @@ def run_gate_study(args):
                 tq.tq_grouped_gemm(x if xs is None else xs, packed, lut, sp, w, tiles, nt, s.top_k, T, y32,
                                    x_layout=lay)
             row[f"grouped_T{T}_us"] = round(timed(whole), 1)
+        row["clocks"] = clocks.stop()
         code, where = tq.tq_device_error()
         if code:
             raise RuntimeError(f"device error {code} at {where} (n={n})")
@@ -694,15 +928,21 @@ def run_mlp_sweep(args):
                          dtype=torch.uint8, device="cuda")
         y = torch.empty((prob.n, prob.H), dtype=torch.bfloat16, device="cuda")
         for pin in ([tq.ARM_GROUPED, tq.ARM_GEMV] if prob.n <= 128 else [tq.ARM_GROUPED]):
-            _mlp_time(args, tq, torch, flush, rate, name, prob, T, pin,
-                      lambda: tq.tq_moe_mlp_forward(x, pgu, lgu, pd, ld, ids, w, tile_m=T, pin=pin, workspace=ws,
-                                                    y=y))
+            clocks = ClockSampler(0)
+            clocks.start()
+            time.sleep(0.3)
+            line = _mlp_time(args, tq, torch, flush, rate, name, prob, T, pin,
+                             lambda: tq.tq_moe_mlp_forward(x, pgu, lgu, pd, ld, ids, w, tile_m=T, pin=pin,
+                                                           workspace=ws, y=y))
+            print(json.dumps({**line, "clocks": clocks.stop()}), flush=True)
         del x, pgu, pd, ws, y
         torch.cuda.empty_cache()
 
 
 def _mlp_time(args, tq, torch, flush, rate, name, prob, T, pin, call):
-    """One line of --mlp-sweep: the call's median time after an L2 flush."""
+    """One line of --mlp-sweep (returned): the call's median time after an
+    L2 flush; the tensor roofline against the burst peak (each call timed on
+    its own)."""
     call()
     torch.cuda.synchronize()
     ts = []
@@ -724,12 +964,12 @@ def _mlp_time(args, tq, torch, flush, rate, name, prob, T, pin, call):
     us = float(np.median(ts))
     ceiling = lookups / (152 * rate * 2.07e9) * 1e6
     flops = 2 * prob.n * prob.top_k * 3 * prob.H * prob.I
-    print(json.dumps({"workload": name, "arm": {tq.ARM_GROUPED: "grouped", tq.ARM_GEMV: "gemv"}[pin],
+    return ({"workload": name, "arm": {tq.ARM_GROUPED: "grouped", tq.ARM_GEMV: "gemv"}[pin],
                       "tile_m": T, "n": prob.n, "pairs": prob.n * prob.top_k, "m_tiles": tiles,
                       "us_per_call": round(us, 1), "tokens_per_s": round(prob.n / (us * 1e-6), 1),
                       "lookups": lookups, "decode_ceiling_us": round(ceiling, 1),
                       "decode_frac": round(ceiling / us, 3),
-                      "tensor_roofline_us": round(flops / (measured_peaks()[2] * 1e12) * 1e6, 1)}), flush=True)
+                      "tensor_roofline_us": round(flops / (measured_peaks()[1] * 1e12) * 1e6, 1)})
 
 
 def main(argv=None):
@@ -744,6 +984,9 @@ def main(argv=None):
                     help="independent weight sets cycled over the steps (defeats L2 reuse)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false",
+                    help="skip the 8192-token prefill projections timed beside the headline")
+    ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--sweep", action="store_true",
                     help="per-workload table of both arms instead of the single bench line")
     ap.add_argument("--sweep-workloads", default="", help="comma-separated subset for --sweep")

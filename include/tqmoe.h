@@ -41,9 +41,12 @@
  *    grouped GEMM and combine kernels are launched as programmatic dependents
  *    of the previous kernel on the stream (they may start while it drains)
  *    and wait for it to finish before touching memory, so stream order holds
- *    as for ordinary launches.  (Inside tq_moe_forward the grouped kernel
- *    reads its LUT before that wait; the kernel before it there is the
- *    library's own gather, which does not write the LUT.)  Status codes
+ *    as for ordinary launches.  (Inside tq_moe_forward and the grouped arm
+ *    of tq_moe_mlp_forward, the first grouped kernel sets up its tensor
+ *    memory and stages its LUT before that wait.  Its predecessor there is
+ *    always one of this library's own launches, and neither writes the LUT:
+ *    the fused route / tile-map launch when the kernel m-tile is at most
+ *    TQ_GATHER_MAX_TILE_M, the activation gather above it.)  Status codes
  *    report argument and launch errors only; device-side faults of the data
  *    (an expert id out of range, a tile map over capacity, a wait that timed
  *    out) are recorded in a device error word read by tq_device_error().
@@ -169,7 +172,9 @@ int tq_select_arm(int64_t n, int top_k, int E, int tile_m, int pin);
  *             ascending p within an expert (a stable sort).
  * Limits: 1 <= top_k <= E <= 1024, 0 <= n*top_k < 2^31.  An expert id out of
  * range is skipped and sets TQ_ERR_INVALID_ARG in the device error word.
- * One thread block; no scratch memory.
+ * One thread block up to 8192 pairs; above that one block per 2048 pairs
+ * (at most 64), each sorting a contiguous chunk after counting every pair
+ * itself, so no block waits for another.  No scratch memory.
  * ------------------------------------------------------------------------- */
 int tq_route(const int32_t* topk_ids, int64_t n, int top_k, int E,
              int32_t* counts, int32_t* offsets, int32_t* sorted_pairs,
@@ -294,7 +299,11 @@ int tq_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L
             float* y32, tq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
- * Combine: y[i] = bf16(y32[i]), round to nearest even, for i < count.
+ * Combine: y[i] = bf16(y32[i]), round to nearest even, for i < count.  The
+ * stated numerics of the product: fp32 accumulation, bf16 output (the routed
+ * outputs are summed per token in fp32 by the arms above; this call rounds
+ * the sum once).  [P1] "The cause is a threshold": the grouped GEMM's output
+ * is the per-token combined projection.
  * y32 (device) fp32 [count]; y (device) bf16 [count].
  * ------------------------------------------------------------------------- */
 int tq_combine(const float* y32, uint16_t* y, int64_t count, tq_stream_t stream);
@@ -339,9 +348,13 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
  * rows, and n > 292 with larger m-tiles, which add the pair-sorted copy of x).  The call allocates nothing (no cudaMalloc,
  * no cudaFree, no allocating library routine).
  *
- * The first call on a device looks up the array's device address with that
- * device current (cudaGetSymbolAddress) and caches it; make that first call
- * before any stream capture.  Every call on a device shares the one array and
+ * The first call on a device does one-time set-up there: it looks up the
+ * array's device address with that device current (cudaGetSymbolAddress) and
+ * caches it, and, unless tq_init(device) ran first, takes the arch witness
+ * (which creates a private stream, launches one tiny kernel, synchronizes
+ * that stream and destroys it) and looks up the driver's tensor-map encoder.
+ * That first call can therefore stall the host; make it (or tq_init) at
+ * start-up, before any stream capture.  Later calls only enqueue.  Every call on a device shares the one array and
  * it keeps the last call's contents (each call zeroes what must start at
  * zero): calls that overlap on the GPU — on different streams or threads —
  * race and corrupt each other's results; serialize them.

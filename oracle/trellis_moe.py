@@ -204,19 +204,11 @@ def tile_map_capacity(n: int, top_k: int, E: int, tile_m: int) -> int:
     return min(P, P // tile_m + min(E, P))
 
 
-MEASURED_CROSSOVER_PPW = 1.16
-
-
 def dispatch_arm(n: int, top_k: int, E: int, tile_m: int, pin: str = "auto") -> str:
     """[P1] post-merge note: n <= 8 or not amortized -> per-pair GEMV, else the
-    grouped GEMM; ``pin`` forces an arm (the pages' A/B knob).  ``pin =
-    "measured"``: the grouped GEMM once the expected pairs per woken expert
-    reach the crossover measured on GB300 (1.16), no floor ([P3] "Two things
-    that were built, correct, and switched off")."""
+    grouped GEMM; ``pin`` forces an arm (the pages' A/B knob)."""
     if pin in ("gemv", "grouped"):
         return pin
-    if pin == "measured":
-        return "grouped" if n > 0 and pairs_per_woken_expert(n, top_k, E) >= MEASURED_CROSSOVER_PPW else "gemv"
     if pin != "auto":
         raise ValueError(f"unknown pin {pin!r}")
     if n <= DECODE_REGIME_MAX_TOKENS or not tiles_amortize(n, top_k, E, tile_m):

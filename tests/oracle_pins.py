@@ -75,23 +75,6 @@ def pin_gate_points():
     assert T.dispatch_arm(5000, 6, 256, 16, pin="gemv") == "gemv"
 
 
-def pin_measured_policy():
-    """The GB300 policy: grouped iff the expected pairs per woken expert reach
-    1.16.  k == E gives exactly n pairs per expert, so it selects from n = 2;
-    at the V4 shape (top-6 of 256) pairs per woken expert grows by about
-    k / (2E) = 3/256 per token (first order in k/E): n = 13 gives 1.148 and
-    n = 14 gives 1.161 by the closed form, so the flip is at 14."""
-    for E in (1, 4, 64):
-        assert T.dispatch_arm(1, E, E, 16, pin="measured") == "gemv"
-        assert T.dispatch_arm(2, E, E, 16, pin="measured") == "grouped"
-    assert T.dispatch_arm(0, 6, 256, 16, pin="measured") == "gemv"
-    arms = [T.dispatch_arm(n, 6, 256, 16, pin="measured") for n in range(1, 40)]
-    assert arms[:13] == ["gemv"] * 13 and set(arms[13:]) == {"grouped"}, arms
-    # independent of TILE_M (the policy has no tile-fill term)
-    assert all(T.dispatch_arm(n, 6, 256, tm, pin="measured") == T.dispatch_arm(n, 6, 256, 16, pin="measured")
-               for n in (3, 5, 100) for tm in (1, 64, 256))
-
-
 def pin_gate_closed_forms():
     """Special cases with exact answers.  k == E wakes every expert for every
     token, so pairs per woken expert is exactly n and the gate is n >= T (the
@@ -459,4 +442,4 @@ ALL_PINS = [pin_fill_table, pin_gate_points, pin_gate_closed_forms, pin_min_toke
             pin_capacity_bound, pin_decode_bitfield, pin_run_decode_identity,
             pin_special_luts, pin_bruteforce_tiny, pin_constant_lut, pin_onehot_x,
             pin_route_bruteforce, pin_tile_map, pin_bf16_rne, pin_router_topk,
-            pin_mlp_bruteforce, pin_measured_policy]
+            pin_mlp_bruteforce]

@@ -66,10 +66,38 @@ def test_gate_and_flip_bitexact(tq):
                     continue
                 assert tq.tq_tiles_amortize(n, k, E, T) == O.tiles_amortize(n, k, E, T)
                 assert tq.tq_tile_map_capacity(n, k, E, T) == O.tile_map_capacity(n, k, E, T)
-                for pin, name in ((0, "auto"), (1, "gemv"), (2, "grouped"), (3, "measured")):
+                for pin, name in ((0, "auto"), (1, "gemv"), (2, "grouped")):
                     arm = tq.tq_select_arm(n, k, E, T, pin)
                     assert {1: "gemv", 2: "grouped"}[arm] == O.dispatch_arm(n, k, E, T, name)
     assert tq.tq_grouped_min_tokens(6, 256, 16) == 683
+
+
+def _header_crossover():
+    """The measured policy's threshold as the header defines it (a library
+    tuning value, read from the header rather than restated here)."""
+    m = re.search(r"#define\s+TQ_MEASURED_CROSSOVER_PPW\s+([0-9.eE+-]+)", open(HEADER).read())
+    assert m, "TQ_MEASURED_CROSSOVER_PPW not found in the header"
+    return float(m.group(1))
+
+
+def test_measured_policy_follows_closed_form(tq):
+    """pin = TQ_ARM_MEASURED: the grouped arm iff n > 0 and the oracle's
+    pairs-per-woken-expert closed form reaches the header's threshold, with
+    no token floor and no tile-fill term (TILE_M does not matter)."""
+    thr = _header_crossover()
+    assert 1.0 < thr < 16.0
+    for k, E in SHAPES:
+        for n in list(range(0, 64)) + [127, 128, 512, 682, 683, 1024, 8192]:
+            want = "grouped" if n > 0 and O.pairs_per_woken_expert(n, k, E) >= thr else "gemv"
+            for T in (1, 16, 256):
+                arm = tq.tq_select_arm(n, k, E, T, 3)
+                assert {1: "gemv", 2: "grouped"}[arm] == want, (n, k, E, T)
+    # k == E puts exactly n pairs on every expert: one token never selects,
+    # two tokens always do (the threshold lies strictly between 1 and 2)
+    if thr <= 2.0:
+        for E in (1, 4, 64):
+            assert tq.tq_select_arm(1, E, E, 16, 3) == 1
+            assert tq.tq_select_arm(2, E, E, 16, 3) == 2
 
 
 def test_host_functions_reject_invalid_arguments(tq):

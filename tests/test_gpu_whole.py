@@ -74,17 +74,33 @@ def test_moe_forward_in_cuda_graph(pin):
         assert normwise(y.float().cpu().numpy(), eager.float().cpu().numpy()) <= 1e-2
 
 
-@pytest.mark.parametrize("name", ["tiny_e8_k2_n16", "v4_decode_n32", "v4_prefill_n8192_up"])
-def test_moe_forward_native_tile(name):
+@pytest.mark.parametrize("name,pin,want_arm,want_tile", [
+    ("tiny_e8_k2_n16", tq.ARM_GROUPED, tq.ARM_GROUPED, 128),
+    ("tiny_e8_k2_n16", tq.ARM_AUTO, tq.ARM_GEMV, 128),
+    ("v4_decode_n32", tq.ARM_GROUPED, tq.ARM_GROUPED, 16),
+    ("v4_prefill_n8192_up", tq.ARM_AUTO, tq.ARM_GROUPED, 256),
+    ("v4_prefill_n8192_down", tq.ARM_AUTO, tq.ARM_GROUPED, 256)])
+def test_moe_forward_native_tile(name, pin, want_arm, want_tile):
     """tile_m = TQ_TILE_NATIVE: the pages' TILE_M gates the arm, the kernel runs
-    its native tile (256 at the prefill size); output rows match the oracle."""
+    its native tile (256 at the prefill sizes: the down projection's K = 2048
+    and 128 MiB accumulator take the blocked row order and the round-robin
+    unit walk); the launch counters show the arm and, through the gather
+    launch that only m-tiles above 16 use, the tile; output rows match the
+    oracle."""
     prob = moe_inputs.make_problem(name)
     d = to_device(prob)
     s = prob.shape
-    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=tq.TILE_NATIVE,
-                               pin=tq.ARM_AUTO if s.n > 1024 or s.E <= 8 else tq.ARM_GROUPED)
+    assert tq.tq_native_tile_m(s.n, s.top_k, s.E) == want_tile
+    before = tq.tq_launch_counts()
+    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=tq.TILE_NATIVE, pin=pin)
     check_no_device_error()
-    assert arm == tq.tq_select_arm(s.n, s.top_k, s.E, 16) or s.n <= 1024
+    after = tq.tq_launch_counts()
+    assert arm == want_arm
+    if want_arm == tq.ARM_GROUPED:
+        assert after["grouped"] == before["grouped"] + 1 and after["gemv"] == before["gemv"]
+        assert after["gather"] - before["gather"] == (1 if want_tile > tq.GATHER_MAX_TILE_M else 0)
+    else:
+        assert after["gemv"] == before["gemv"] + 1 and after["grouped"] == before["grouped"]
     rows = sample_rows(s.N, 24, seed=3) if s.N > 256 else np.arange(s.N)
     ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L, rows=rows)
     assert normwise(y.float().cpu().numpy()[:, rows], ref) <= TOL

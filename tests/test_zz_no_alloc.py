@@ -55,20 +55,47 @@ def _normwise(a, b):
     return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
 
 
+def _oracle_rows(prob, rows):
+    import oracle.trellis_moe as O
+    return O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, prob.shape.L,
+                         rows=rows)
+
+
+def _sample_rows(N, count, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    fixed = [0, 1, 127, 128, N - 1] if N >= 256 else [0, N - 1]
+    return np.unique(np.concatenate([fixed, rng.choice(N, size=min(count, N), replace=False)]))
+
+
+# tile_m 16: the kernel gathers its token rows itself; tile_m 128: the call
+# also carves the pair-sorted activation copy out of the array (v4_n128_up at
+# 128 needs about 7.3 MB of it)
 @pytest.mark.parametrize("name,tile_m,pin", [("v4_decode_n32", 16, tq.ARM_GROUPED),
+                                              ("v4_n128_up", 128, tq.ARM_GROUPED),
                                               ("tiny_e8_k2_n16", 16, tq.ARM_AUTO)])
 def test_static_matches_workspace_entry_point_two_calls(name, tile_m, pin):
+    s = moe_inputs.shape(name)
+    need = tq.tq_moe_workspace_size(s.n, s.top_k, s.E, s.K, s.N, tile_m)
+    assert need <= tq.STATIC_SCRATCH_BYTES
     probs = [moe_inputs.make_problem(name, layer=0), moe_inputs.make_problem(name, layer=1)]
     for prob in probs:                                     # two calls in a row
         x, packed, lut, ids, w = _dev(prob)
         want, want_arm = tq.tq_moe_forward(x, packed, lut, ids, w, tile_m=tile_m, pin=pin)
         y = torch.empty_like(want)
+        before = tq.tq_launch_counts()
         rc, arm = _call_static(x, packed, lut, ids, w, tile_m, pin, y)
         assert rc == 0, tq.tq_status_string(rc)
         torch.cuda.synchronize()
+        after = tq.tq_launch_counts()
         assert tq.tq_device_error() == (0, 0)
         assert arm == want_arm
+        if arm == tq.ARM_GROUPED:
+            assert after["gather"] - before["gather"] == (1 if tile_m > tq.GATHER_MAX_TILE_M else 0)
         assert _normwise(y, want) <= TOL
+        rows = _sample_rows(s.N, 24, seed=11)
+        got = y[:, torch.from_numpy(rows).cuda()]
+        ref = torch.from_numpy(_oracle_rows(prob, rows))
+        assert _normwise(got, ref) <= TOL
 
 
 def test_static_rejects_shapes_beyond_its_array():
@@ -78,6 +105,8 @@ def test_static_rejects_shapes_beyond_its_array():
     x, packed, lut, ids, w = _dev(prob)
     y = torch.empty((4, 128), dtype=torch.bfloat16, device="cuda")
     p = lambda t: ctypes.c_void_p(t.data_ptr())
+    before = tq.tq_launch_counts()
     rc = tq.lib().tq_moe_forward_static(p(x), p(packed), p(lut), 12, p(ids), p(w), 8192, 6, 256, 256, 2048,
                                         16, 0, p(y), None, None)
-    assert rc == -8                                        # TQ_ERR_WORKSPACE, nothing launched
+    assert rc == -8                                        # TQ_ERR_WORKSPACE
+    assert tq.tq_launch_counts() == before                 # nothing was launched
