@@ -59,9 +59,7 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
   const long long i0 = items * gwarp / nwarps, i1 = items * (gwarp + 1) / nwarps;
 
   // packed bytes of item `it` (zeros for a bad expert id, reported once per pair)
-  auto load_row = [&](long long it, uint4 (&q)[CPL]) {
-    const int pair = static_cast<int>(it / N);
-    const int r = static_cast<int>(it - static_cast<long long>(pair) * N);
+  auto load_row = [&](int pair, int r, uint4 (&q)[CPL]) {
     const int e = __ldg(topk_ids + pair);
     const bool ok = e >= 0 && e < E;
     const uint4* rp = reinterpret_cast<const uint4*>(packed + (static_cast<size_t>(ok ? e : 0) * N + r) * row_bytes);
@@ -71,9 +69,16 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
       q[i] = (ok && c < nchunks) ? __ldg(rp + c) : make_uint4(0u, 0u, 0u, 0u);
     }
   };
+  // The warp walks its range in order: only the first item's (pair, row) is
+  // found by division, the others step a counter.
+  int p0 = 0, r0 = 0;
+  if (i0 < i1) {
+    p0 = static_cast<int>(i0 / N);
+    r0 = static_cast<int>(i0 - static_cast<long long>(p0) * N);
+  }
   // The first row's bytes are in flight while the tables are staged.
   uint4 qa[CPL], qb[CPL];
-  if (i0 < i1) load_row(i0, qa);
+  if (i0 < i1) load_row(p0, r0, qa);
 
   if constexpr (kEntries >= 8) {
     stage_to_smem(smem_u32(lut_s), lut, kEntries * 2);
@@ -108,15 +113,13 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
   float wt = 0.f;
   bool pair_ok = false;
   uint32_t xr[CPL][32];
-  auto process = [&](long long it, const uint4 (&qv)[CPL]) {
-    const int pair = static_cast<int>(it / N);
-    const int r = static_cast<int>(it - static_cast<long long>(pair) * N);
+  auto process = [&](bool first_item, int pair, int r, const uint4 (&qv)[CPL]) {
     if (pair != cur_pair) {
       cur_pair = pair;
       tok = pair_in ? pair : pair / top_k;   // the row of x this pair multiplies
       const int e = __ldg(topk_ids + pair);
       pair_ok = e >= 0 && e < E;
-      if (!pair_ok && lane == 0 && (r == 0 || it == i0)) record_error(err, TQ_ERR_INVALID_ARG, kWhereRoute);
+      if (!pair_ok && lane == 0 && (r == 0 || first_item)) record_error(err, TQ_ERR_INVALID_ARG, kWhereRoute);
       wt = pair_out ? 1.f : __ldg(topk_w + pair);   // per-pair outputs carry no router weight
       // activations of this token: chunk c = lane + 32 i, 64 bf16 = 32 words
 #pragma unroll
@@ -182,12 +185,24 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
 
   // The next row's bytes are in flight while this row decodes (two register
   // sets used in turn, so no copy waits for a load).
+  int pa = p0, ra = r0;
   for (long long it = i0; it < i1; it += 2) {
-    if (it + 1 < i1) load_row(it + 1, qb);
-    process(it, qa);
+    int pb = pa, rb = ra + 1;
+    if (rb == N) {
+      rb = 0;
+      ++pb;
+    }
+    if (it + 1 < i1) load_row(pb, rb, qb);
+    process(it == i0, pa, ra, qa);
     if (it + 1 >= i1) break;
-    if (it + 2 < i1) load_row(it + 2, qa);
-    process(it + 1, qb);
+    pa = pb;
+    ra = rb + 1;
+    if (ra == N) {
+      ra = 0;
+      ++pa;
+    }
+    if (it + 2 < i1) load_row(pa, ra, qa);
+    process(false, pb, rb, qb);
   }
 }
 
