@@ -62,6 +62,44 @@ def test_grouped_small_all_outputs(name, lay):
     assert err <= TOL, err
 
 
+# Expert sizes whose m-tiles at TILE_M 256 run through every transition of the
+# accumulator slots (m-tiles above 128 pairs take both 128-column slots, the
+# others one, alternating): 296 -> 256 + 40 (big -> small), 40 -> 200 (small ->
+# big), 200 -> 130 (big -> big), 130 -> 128, 128 -> 1 (small -> small),
+# 1 -> 129, 512 -> 256 + 256, 17, 255, 257 -> 256 + 1.
+SLOT_PATTERN = [296, 200, 130, 128, 1, 129, 512, 17, 255, 257]
+
+
+def _slot_problem(reps, N, seed):
+    """top-1 routing with the expert sizes of SLOT_PATTERN repeated `reps`
+    times (token order shuffled), K = 64, router weights drawn in [0.5, 1.5)."""
+    counts = np.array(SLOT_PATTERN * reps)
+    E, n, K, L = len(counts), int(counts.sum()), 64, 12
+    rx, rr, rp, rl = moe_inputs._streams((moe_inputs.BASE_SEED, 4242, seed, reps, N))
+    ids = np.repeat(np.arange(E, dtype=np.int32), counts)
+    rr.shuffle(ids)
+    w = rr.uniform(0.5, 1.5, size=(n, 1)).astype(np.float32)
+    shp = moe_inputs.Shape(f"slots_{reps}_{N}", E, 1, n, K, N, L)
+    return moe_inputs.Problem(shp, moe_inputs.draw_x(rx, n, K), ids.reshape(n, 1), w,
+                              moe_inputs.draw_packed(rp, E, N, K), moe_inputs.draw_lut(rl, L, K))
+
+
+@pytest.mark.parametrize("reps,N,T", [(60, 128, 256), (60, 128, 192), (30, 1024, 256)])
+def test_grouped_accumulator_slots_all_outputs(reps, N, T):
+    """m-tiles above 128 pairs with small and big tiles interleaved on every
+    CTA: 780 one-row-block units (each CTA walks ~5 units in a row), and 3120
+    units over eight row blocks (whole units dealt round-robin).  Every output
+    against the oracle, and the tile sizes the map holds are the pattern's."""
+    prob = _slot_problem(reps, N, seed=T)
+    counts, offsets, _ = O.route(prob.topk_ids, prob.shape.E)
+    rows = O.tile_map(offsets, T)[:, 2]
+    assert (rows > 128).any() and (rows <= 128).any() and (rows == 1).any()
+    d = to_device(prob)
+    y = grouped_y32(prob, d, T, tq.X_PAIR_SORTED).cpu().numpy()
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, prob.shape.L)
+    assert normwise(y, ref) <= TOL
+
+
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_gemv_small_all_outputs(name):
     prob, _ = _small(name)

@@ -106,7 +106,9 @@ struct Params {
   int n_mma_max;    // largest MMA N (tile_m rounded up to 16)
   int pk_stages;    // packed super-stage buffers
   int act_stages;   // activation k-step buffers
-  int nacc;         // accumulator buffers in tensor memory (1 or 2)
+  int nacc;         // accumulator buffers of n_mma_max columns in tensor memory (1 or 2)
+  int acc_slots;    // 1: no room for two buffers; two 128-column slots instead (see AccSlots)
+  int acol0;        // first tensor-memory column of the A stages
   int tmem_cols;    // allocated tensor-memory columns
   uint32_t off_pk, off_lut, off_bar;  // byte offsets from the 1024-aligned base
 };
@@ -120,6 +122,23 @@ struct Pipe {
       phase ^= 1u;
     }
   }
+};
+
+// Accumulator slots, for m-tiles above 128 pairs, where two accumulators of
+// n_mma_max columns do not fit beside the 8 A stages: the 256 accumulator
+// columns are two slots of 128.  A unit of at most 128 pairs takes one slot,
+// alternating, so consecutive small units are double-buffered; a larger unit
+// takes both (one MMA of N = n_mma at column 0), and the epilogue frees slot 0
+// as soon as it has drained the first 128 columns, so a small unit after it can
+// start while the rest drains.  The MMA warp and the epilogue walk the same
+// units and step this state alike.
+struct AccSlots {
+  int next = 0;           // slot of the next small unit
+  uint32_t full_ph = 0;   // bit k: phase of slot k's full barrier (epilogue)
+  uint32_t empty_ph = 0;  // bit k: phase of slot k's empty barrier (MMA warp)
+  __device__ __forceinline__ static bool big(uint32_t n_mma) { return n_mma > 128u; }
+  __device__ __forceinline__ int first(uint32_t n_mma) const { return big(n_mma) ? 0 : next; }
+  __device__ __forceinline__ void step(uint32_t n_mma) { next = big(n_mma) ? 0 : (next ^ 1); }
 };
 
 // A tile entry is used only if it describes 1..tile_m consecutive sorted slots
@@ -370,7 +389,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   const int num_tiles = static_cast<int>(min(static_cast<long long>(*p.num_tiles), p.cap));
   const int ksteps = p.K / kKStep;
   const int n_ss = (ksteps + kSSSteps - 1) / kSSSteps;
-  const uint32_t acol0 = static_cast<uint32_t>(p.nacc * p.n_mma_max);
+  const uint32_t acol0 = static_cast<uint32_t>(p.acol0);
   const int rb_group = p.rb_group;
   // This CTA's share of the (unit, super-stage) work; every role walks it in
   // the same order, one segment at a time.
@@ -482,6 +501,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     Pipe act, apipe, accp;
+    AccSlots slots;
     Pipe& wpipe = apipe;   // kDense: the A ring is the packed-byte ring
     bool ok = true;
     Walk w = walk0;
@@ -491,12 +511,31 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
       if (!tl.ok) continue;
       const uint32_t n_mma = static_cast<uint32_t>((tl.rows + 15) & ~15);
       const uint32_t idesc = idesc_bf16_f32(kBlockRows, n_mma);
-      if (!mbar_wait(bar_accempty + 8 * accp.stage, accp.phase ^ 1u, abort_flag, p.err, kWhereGroupedMma)) {
-        ok = false;
-        break;
+      uint32_t d_tmem;
+      int acc_bar;   // the full barrier this unit's commit arrives on
+      if (p.acc_slots) {
+        const int first = slots.first(n_mma);
+        const int last = AccSlots::big(n_mma) ? 1 : first;
+        for (int k = first; k <= last && ok; ++k) {
+          if (!mbar_wait(bar_accempty + 8 * k, ((slots.empty_ph >> k) & 1u) ^ 1u, abort_flag, p.err,
+                         kWhereGroupedMma))
+            ok = false;
+          slots.empty_ph ^= 1u << k;
+        }
+        if (!ok) break;
+        d_tmem = tmem_base + static_cast<uint32_t>(128 * first);
+        acc_bar = first;
+        slots.step(n_mma);
+      } else {
+        if (!mbar_wait(bar_accempty + 8 * accp.stage, accp.phase ^ 1u, abort_flag, p.err, kWhereGroupedMma)) {
+          ok = false;
+          break;
+        }
+        d_tmem = tmem_base + static_cast<uint32_t>(accp.stage * p.n_mma_max);
+        acc_bar = accp.stage;
+        accp.advance(p.nacc);
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(accp.stage * p.n_mma_max);
       const int ks0 = sg.ss0 * kSSSteps, ks1 = min(ksteps, sg.ss1 * kSSSteps);
       for (int ks = ks0; ks < ks1; ++ks) {
         const uint32_t bar_wfull = kDense ? bar_pkfull : bar_afull;
@@ -533,9 +572,8 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
         wpipe.advance(kDense ? SP : kNumAStages);
       }
       if (!ok) break;
-      if (lane == 0) mma_commit(bar_accfull + 8 * accp.stage);
+      if (lane == 0) mma_commit(bar_accfull + 8 * acc_bar);
       __syncwarp();
-      accp.advance(p.nacc);
     }
     // Drain: every MMA issued by this warp has completed before teardown.
     if (lane == 0) {
@@ -553,6 +591,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     Pipe accp;
+    AccSlots slots;
     Walk w = walk0;
     Segment sg;
     while (walk_next(w, n_ss, num_tiles, rb_group, sg)) {
@@ -585,10 +624,25 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
           }
         }
       }
-      if (!mbar_wait(bar_accfull + 8 * accp.stage, accp.phase, abort_flag, p.err, kWhereGroupedEpilogue)) break;
+      const uint32_t n_mma = static_cast<uint32_t>((rows + 15) & ~15);
+      const bool two_slots = p.acc_slots && AccSlots::big(n_mma);
+      int acc_first, acc_done;   // full barrier to wait on; empty barrier to arrive on at the end
+      uint32_t acc_ph;
+      if (p.acc_slots) {
+        acc_first = slots.first(n_mma);
+        acc_ph = (slots.full_ph >> acc_first) & 1u;
+        slots.full_ph ^= 1u << acc_first;
+        acc_done = two_slots ? 1 : acc_first;
+        slots.step(n_mma);
+      } else {
+        acc_first = acc_done = accp.stage;
+        acc_ph = accp.phase;
+        accp.advance(p.nacc);
+      }
+      if (!mbar_wait(bar_accfull + 8 * acc_first, acc_ph, abort_flag, p.err, kWhereGroupedEpilogue)) break;
       tc_fence_after();
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
-                             static_cast<uint32_t>(accp.stage * p.n_mma_max);
+                             static_cast<uint32_t>(p.acc_slots ? 128 * acc_first : acc_first * p.n_mma_max);
       // Each 4x4 block (4 lanes = 4 consecutive rows, 4 pair columns) is
       // transposed by shuffles so that a lane holds 4 consecutive rows of one
       // pair and adds them with one 16-byte vector reduction.
@@ -636,11 +690,16 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
             }
           }
         }
+        if (two_slots && b == 3) {
+          // the first 128 columns are read: slot 0 is free for the next unit
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_accempty);
+        }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_accempty + 8 * accp.stage);
-      accp.advance(p.nacc);
+      if (lane == 0) mbar_arrive(bar_accempty + 8 * acc_done);
     }
   } else if constexpr (!kDense) {
     // ------------------------------------------------------------ decode
@@ -814,7 +873,10 @@ int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
   p.n_mma_max = (tile_m + 15) & ~15;
   const int a_cols = dense ? 0 : kNumAStages * kATmemCols;   // decoded A stages in tensor memory
   p.nacc = (2 * p.n_mma_max + a_cols <= 512) ? 2 : 1;
-  const int cols_needed = p.nacc * p.n_mma_max + a_cols;
+  // m-tiles above 128 pairs beside the 8 A stages: two 128-column slots
+  p.acc_slots = (!dense && p.nacc == 1) ? 1 : 0;
+  p.acol0 = p.acc_slots ? 256 : p.nacc * p.n_mma_max;
+  const int cols_needed = p.acol0 + a_cols;
   int cols = 32;
   while (cols < cols_needed) cols <<= 1;
   p.tmem_cols = cols;
