@@ -862,8 +862,16 @@ int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
   p.rb_group = p.row_blocks;
   const long long out_rows = pair_out ? n * static_cast<long long>(top_k) : n;
   if (out_rows * N * 4 > (24ll << 20)) {
-    for (int g = 8; g >= 1; g >>= 1) {
-      if (p.row_blocks % g == 0) {
+    // The largest group of row blocks whose slice of the fp32 output (which the
+    // CTAs running together add into) stays within 64 MiB of L2: fewer groups
+    // mean fewer passes over the tiles' activations (each group reads them
+    // once from DRAM).  At least one row block; a divisor of row_blocks.
+    // Plain stores (store_out) write each output once and need no slice in
+    // L2: one group.
+    const long long slice_per_rb = out_rows * kBlockRows * 4;
+    p.rb_group = 1;
+    for (int g = p.row_blocks; g >= 1; --g) {
+      if (p.row_blocks % g == 0 && (slice_per_rb * g <= (64ll << 20) || (store_out && pair_out))) {
         p.rb_group = g;
         break;
       }
