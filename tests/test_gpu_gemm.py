@@ -70,12 +70,12 @@ def test_grouped_small_all_outputs(name, lay):
 SLOT_PATTERN = [296, 200, 130, 128, 1, 129, 512, 17, 255, 257]
 
 
-def _slot_problem(reps, N, seed):
+def _slot_problem(reps, N, seed, K=64):
     """top-1 routing with the expert sizes of SLOT_PATTERN repeated `reps`
-    times (token order shuffled), K = 64, router weights drawn in [0.5, 1.5)."""
+    times (token order shuffled), router weights drawn in [0.5, 1.5)."""
     counts = np.array(SLOT_PATTERN * reps)
-    E, n, K, L = len(counts), int(counts.sum()), 64, 12
-    rx, rr, rp, rl = moe_inputs._streams((moe_inputs.BASE_SEED, 4242, seed, reps, N))
+    E, n, L = len(counts), int(counts.sum()), 12
+    rx, rr, rp, rl = moe_inputs._streams((moe_inputs.BASE_SEED, 4242, seed, reps, N, K))
     ids = np.repeat(np.arange(E, dtype=np.int32), counts)
     rr.shuffle(ids)
     w = rr.uniform(0.5, 1.5, size=(n, 1)).astype(np.float32)
@@ -84,13 +84,16 @@ def _slot_problem(reps, N, seed):
                               moe_inputs.draw_packed(rp, E, N, K), moe_inputs.draw_lut(rl, L, K))
 
 
-@pytest.mark.parametrize("reps,N,T", [(60, 128, 256), (60, 128, 192), (30, 1024, 256)])
-def test_grouped_accumulator_slots_all_outputs(reps, N, T):
+@pytest.mark.parametrize("reps,N,T,K", [(60, 128, 256, 64), (60, 128, 192, 64), (30, 1024, 256, 64),
+                                         (20, 128, 256, 1024)])
+def test_grouped_accumulator_slots_all_outputs(reps, N, T, K):
     """m-tiles above 128 pairs with small and big tiles interleaved on every
-    CTA: 780 one-row-block units (each CTA walks ~5 units in a row), and 3120
-    units over eight row blocks (whole units dealt round-robin).  Every output
-    against the oracle, and the tile sizes the map holds are the pattern's."""
-    prob = _slot_problem(reps, N, seed=T)
+    CTA: 780 one-row-block units (each CTA walks ~5 units in a row), 3120
+    units over eight row blocks (whole units dealt round-robin), and 260 units
+    of two super-stages each (K = 1024), which the contiguous walk splits
+    between CTAs at super-stage boundaries.  Every output against the oracle,
+    and the tile sizes the map holds are the pattern's."""
+    prob = _slot_problem(reps, N, seed=T, K=K)
     counts, offsets, _ = O.route(prob.topk_ids, prob.shape.E)
     rows = O.tile_map(offsets, T)[:, 2]
     assert (rows > 128).any() and (rows <= 128).any() and (rows == 1).any()
