@@ -38,6 +38,52 @@ def test_moe_forward_full_size(name, tile_m, pin):
     assert normwise(got, ref) <= TOL
 
 
+@pytest.mark.parametrize("n", [1, 2, 8])
+def test_moe_forward_small_batch_decode_steps(n):
+    """The decode steps at 1, 2 and 8 tokens at the V4 up shape through
+    tq_moe_forward with the default selection: the n <= 8 floor sends them to
+    the per-pair GEMV (launch counters), and sampled output rows match the
+    oracle."""
+    prob = moe_inputs.make_problem("v4_decode_n32", n=n)
+    d = to_device(prob)
+    s = prob.shape
+    assert tq.tq_select_arm(n, s.top_k, s.E, 16) == tq.ARM_GEMV
+    before = tq.tq_launch_counts()
+    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=tq.TILE_NATIVE)
+    check_no_device_error()
+    after = tq.tq_launch_counts()
+    assert arm == tq.ARM_GEMV
+    assert after["gemv"] == before["gemv"] + 1 and after["grouped"] == before["grouped"]
+    rows = sample_rows(s.N, 32, seed=11 + n)
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L, rows=rows)
+    assert normwise(y.float().cpu().numpy()[:, rows], ref) <= TOL
+
+
+@pytest.mark.parametrize("n", [13, 14])
+def test_moe_forward_measured_policy_at_its_crossover(n):
+    """pin = ARM_MEASURED at the V4 up shape on either side of the library's
+    crossover (13 tokens: 1.148 pairs per woken expert -> GEMV; 14: 1.161 ->
+    grouped, the threshold being TQ_MEASURED_CROSSOVER_PPW = 1.16): the arm the
+    closed form predicts runs (launch counters) and sampled rows match the
+    oracle."""
+    prob = moe_inputs.make_problem("v4_decode_n32", n=n)
+    d = to_device(prob)
+    s = prob.shape
+    want = tq.tq_select_arm(n, s.top_k, s.E, 16, tq.ARM_MEASURED)
+    assert want == (tq.ARM_GROUPED if n == 14 else tq.ARM_GEMV)
+    before = tq.tq_launch_counts()
+    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=tq.TILE_NATIVE,
+                               pin=tq.ARM_MEASURED)
+    check_no_device_error()
+    after = tq.tq_launch_counts()
+    assert arm == want
+    ran = "grouped" if arm == tq.ARM_GROUPED else "gemv"
+    assert after[ran] == before[ran] + 1
+    rows = sample_rows(s.N, 32, seed=21 + n)
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L, rows=rows)
+    assert normwise(y.float().cpu().numpy()[:, rows], ref) <= TOL
+
+
 def test_lut_probe_rate_is_sane():
     rate = tq.tq_probe_lut_rate(8, 128)
     # between random-address bank conflicts at their worst and 32 banks per clock
