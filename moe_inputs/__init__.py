@@ -207,6 +207,18 @@ MLP_WORKLOADS = {
 }
 
 
+def make_mlp_custom(E: int, top_k: int, n: int, H: int, I: int, L: int, seed: int,
+                    routing: str = "uniform") -> MLPProblem:
+    """Small ad-hoc expert-MLP problem for edge-case tests."""
+    ss = np.random.SeedSequence([BASE_SEED, 778, seed, E, top_k, n, H, I, L])
+    rx, rr, rg, rlg, rd, rld = [np.random.Generator(np.random.PCG64(s)) for s in ss.spawn(6)]
+    x = draw_x(rx, n, H)
+    ids, w = draw_routing(rr, n, E, top_k, routing)
+    return MLPProblem(f"mlp_custom_{seed}", E, top_k, n, H, I, L, x, ids, w,
+                      draw_packed(rg, E, 2 * I, H), draw_lut(rlg, L, H),
+                      draw_packed(rd, E, H, I), draw_lut(rld, L, I))
+
+
 def make_mlp_problem(name: str, n: int | None = None, layer: int = 0) -> MLPProblem:
     E, k, n0, H, I, L, routing = MLP_WORKLOADS[name]
     n = n0 if n is None else n

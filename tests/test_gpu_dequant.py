@@ -101,6 +101,8 @@ FWD = {
     "ragged_n37_K192_N256_T7": (4, 4, 37, 192, 256, 16, 7, "uniform"),
     "zipf_T128": (32, 4, 200, 256, 256, 14, 128, "zipf"),
     "T256": (8, 2, 300, 128, 384, 16, 256, "uniform"),
+    # 19 k-steps of materialized weights: two full super-stages and 3
+    "ragged_ss_K1216_T128": (6, 3, 60, 1216, 256, 14, 128, "zipf"),
 }
 
 

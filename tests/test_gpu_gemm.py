@@ -1,7 +1,7 @@
 """Grouped GEMM and per-pair GEMV arms on the GPU against the CPU oracle.
 
-Small problems (several tiles, ragged tails, every L, K of 1..many k-steps,
-several 128-row blocks) are compared on every output; the five workloads at
+Small problems (several tiles, ragged tails, every L, K of 1..many k-steps
+and super-stages with a ragged last one, several 128-row blocks) are compared on every output; the five workloads at
 full size on sampled rows.  Tolerance: max|y - ref| / max|ref| <= 1e-2 on the
 fp32 accumulator (bf16 weights on the tensor cores; the GEMV widens fp16
 weights exactly and is held to 1e-4)."""
@@ -43,6 +43,17 @@ SMALL = {
     # fp32 output > 24 MB and thousands of units: blocked row order, whole
     # units round-robin over the CTAs
     "interleaved_n6000_N1024": (64, 2, 6000, 64, 1024, 8, 16, "uniform"),
+    # K past one super-stage (8 k-steps) with a ragged last one: the 4 stream
+    # bytes carried across each boundary, and a final super-stage of 1 or 3
+    # k-steps.  The first three hold fewer super-stage positions than there are
+    # CTAs, so the walk splits every unit at every boundary; in the fourth each
+    # CTA walks ~6 positions, crossing boundaries inside its own range.
+    "ragged_ss_K576_L16": (4, 2, 24, 576, 128, 16, 16, "uniform"),
+    "ragged_ss_K1216_T128": (6, 3, 60, 1216, 256, 14, 128, "zipf"),
+    "ragged_ss_K2112_T256": (3, 2, 400, 2112, 1024, 12, 256, "uniform"),
+    "ragged_ss_K1088_T64_zipf": (16, 4, 500, 1088, 1024, 16, 64, "zipf"),
+    # the GEMV arm's largest K (one row = 16 super-stages)
+    "kmax_K8192": (2, 1, 4, 8192, 128, 16, 16, "uniform"),
 }
 
 

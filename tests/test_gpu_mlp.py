@@ -53,6 +53,24 @@ def test_mlp_tiny_all_outputs(tile_m, pin):
     assert normwise(y.float().cpu().numpy(), ref) <= TOL
 
 
+@pytest.mark.parametrize("tile_m,pin", [(16, tq.ARM_GROUPED), (64, tq.ARM_GROUPED), (256, tq.ARM_GROUPED),
+                                        (16, tq.ARM_GEMV)])
+def test_mlp_ragged_superstages_all_outputs(tile_m, pin):
+    """H = 640, I = 576: the gate|up projection takes 10 k-steps (one full
+    super-stage of 8, then 2) and the down projection 9 (8, then 1), so both
+    carry the stream history across a super-stage boundary into a ragged last
+    one; every output of both arms against the oracle."""
+    prob = moe_inputs.make_mlp_custom(6, 2, 40, 640, 576, 14, seed=5, routing="zipf")
+    d = _mlp_dev(prob)
+    y, arm = tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"], tile_m=tile_m,
+                                   pin=pin)
+    check_no_device_error()
+    assert arm == pin
+    ref = O.moe_mlp(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed_gu, prob.lut_gu, prob.packed_down,
+                    prob.lut_down, prob.L)
+    assert normwise(y.float().cpu().numpy(), ref) <= TOL
+
+
 @pytest.mark.parametrize("tile_m,pin", [(16, tq.ARM_GROUPED), (64, tq.ARM_GROUPED), (16, tq.ARM_GEMV)])
 def test_mlp_dirty_workspace(tile_m, pin):
     """A workspace of NaN bit patterns, twice: the gate|up rows are written
