@@ -54,6 +54,11 @@ SMALL = {
     "ragged_ss_K1088_T64_zipf": (16, 4, 500, 1088, 1024, 16, 64, "zipf"),
     # the GEMV arm's largest K (one row = 16 super-stages)
     "kmax_K8192": (2, 1, 4, 8192, 128, 16, 16, "uniform"),
+    # one expert holding every pair (128 + 128 + 44); the most experts the
+    # routing sort takes, 393 of them woken by one or two pairs; one token
+    "one_expert_E1": (1, 1, 300, 256, 128, 16, 128, "uniform"),
+    "E1024_k8_n64": (1024, 8, 64, 256, 128, 12, 16, "uniform"),
+    "one_token_n1": (16, 4, 1, 256, 256, 16, 16, "uniform"),
 }
 
 
