@@ -13,6 +13,7 @@ namespace tq {
 enum ErrWhere : int {
   kWhereRoute = 1, kWhereTileMap = 2, kWhereGroupedProducer = 3, kWhereGroupedDecode = 4,
   kWhereGroupedMma = 5, kWhereGroupedEpilogue = 6, kWhereGroupedTeardown = 7, kWhereDequant = 8,
+  kWhereTableStage = 9,
 };
 
 // A wait gives up after this long (ns of %globaltimer) and reports
@@ -74,6 +75,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       "selp.u32 %0, 1, 0, P;\n\t}"
       : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
   return ok != 0;
+}
+
+// Copies `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// global to shared memory with the bulk copy engine, as requests of at most
+// 32 KiB whose completion is counted in bytes on `bar`; this call makes the
+// barrier's one expected arrival.  Issued by one thread, after the barrier's
+// init (and fence_init); readers wait on the barrier's phase 0.
+__device__ __forceinline__ void bulk_stage_to_smem(uint32_t smem_dst, const void* gsrc, uint32_t bytes,
+                                                   uint32_t bar) {
+  mbar_arrive_expect_tx(bar, bytes);
+  const char* src = static_cast<const char*>(gsrc);
+  for (uint32_t off = 0; off < bytes; off += 32768u) {
+    const uint32_t len = (bytes - off < 32768u) ? bytes - off : 32768u;
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_dst + off), "l"(src + off), "r"(len), "r"(bar)
+                 : "memory");
+  }
 }
 
 // Wait for the phase with the given parity to complete.  Gives up when the

@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
             const uint16_t* __restrict__ lut, const int32_t* __restrict__ topk_ids,
             const float* __restrict__ topk_w, int P, int top_k, int E, int K, int N, int x_in_smem,
-            int pair_in, int pair_out, int early_prologue, float* __restrict__ y32, int* err) {
+            int pair_in, int pair_out, int early_prologue, float* __restrict__ y32, int* err, int bar_off) {
   extern __shared__ __align__(16) uint16_t lut_s[];
   constexpr int kEntries = 1 << L;
   constexpr int kLutBytes = (kEntries * 2 + 15) & ~15;
@@ -80,8 +80,17 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
   uint4 qa[CPL], qb[CPL];
   if (i0 < i1) load_row(p0, r0, qa);
 
+  // The table by the bulk copy engine (one thread; the barrier sits after
+  // the table and the activations), waited for after the activations.
+  __shared__ int abort_flag;
+  const uint32_t bar = smem_u32(lut_s) + static_cast<uint32_t>(bar_off);
   if constexpr (kEntries >= 8) {
-    stage_to_smem(smem_u32(lut_s), lut, kEntries * 2);
+    if (threadIdx.x == 0) {
+      abort_flag = 0;
+      mbar_init(bar, 1);
+      mbar_fence_init();
+      bulk_stage_to_smem(smem_u32(lut_s), lut, kEntries * 2, bar);
+    }
   } else {
     for (int i = threadIdx.x; i < kEntries; i += THREADS) lut_s[i] = lut[i];
   }
@@ -105,6 +114,9 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
     asm volatile("cp.async.wait_all;" ::: "memory");
   }
   __syncthreads();
+  if constexpr (kEntries >= 8) {
+    if (!mbar_wait(bar, 0, &abort_flag, err, kWhereTableStage)) return;
+  }
   const uint32_t lut_base = smem_u32(lut_s);
   if (early_prologue) pdl_wait();
   pdl_trigger();
@@ -216,7 +228,8 @@ int launch_one(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, co
   const size_t x_bytes = static_cast<size_t>(pair_in ? P : P / top_k) * K * 2;
   // activations go to shared memory when they fit beside the LUT (small batches)
   const int x_in_smem = (lut_bytes + x_bytes <= 200u * 1024u) ? 1 : 0;
-  const size_t smem = std::max<size_t>(16, lut_bytes + (x_in_smem ? x_bytes : 0));
+  const size_t bar_off = lut_bytes + (x_in_smem ? x_bytes : 0);   // a multiple of 16
+  const size_t smem = bar_off + 16;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess) {
     cudaGetLastError();
@@ -226,7 +239,7 @@ int launch_one(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, co
   const long long items = static_cast<long long>(P) * N;
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(sms, (items + kThreads / 32 - 1) / (kThreads / 32))));
   const int st = launch_pdl(kfn, dim3(grid), dim3(kThreads), smem, s, x, packed, lut, ids, w, P, top_k, E, K, N,
-                            x_in_smem, pair_in, pair_out, early, y32, err);
+                            x_in_smem, pair_in, pair_out, early, y32, err, static_cast<int>(bar_off));
   return st == TQ_OK ? launch_status() : st;
 }
 

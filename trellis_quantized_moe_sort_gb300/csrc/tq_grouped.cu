@@ -79,7 +79,7 @@ constexpr int kMaxPkStages = 6;
 constexpr int kActPrefetch = 8;                       // k-steps of activations asked into L2 ahead
 constexpr int kMaxActStages = 8;
 constexpr int kSmemLimit = 232448;                   // 227 KiB opt-in per block
-constexpr int kNumBars = 2 * kMaxPkStages + 2 * kMaxActStages + 2 * kNumAStages + 2 + 2 + 1;
+constexpr int kNumBars = 2 * kMaxPkStages + 2 * kMaxActStages + 2 * kNumAStages + 2 + 2 + 1 + 1;
 static_assert(kNumDecodeWarps == 8, "decode mapping assumes 2 warps per TMEM lane quarter");
 static_assert(kWarpEpi0 % 4 == 2 && kWarpDec0 % 4 == 2, "role warps must cover all four quarters");
 
@@ -322,6 +322,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   const uint32_t bar_arel = (SA == kNumAStages) ? bar_actempty : bar_aempty;
   const uint32_t bar_accempty = bar_accfull + 16;
   const uint32_t bar_drain = bar_accempty + 16;
+  const uint32_t bar_lut = bar_drain + 8;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + p.off_bar + 8 * kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -343,8 +344,11 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
       mbar_init(bar_accempty + 8 * b, kNumEpiWarps);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_lut, 1);
     *abort_flag = 0;
     mbar_fence_init();
+    // the fp16 table by the bulk copy engine, converted below once it is in
+    if constexpr (!kDense && (1 << L) >= 8) bulk_stage_to_smem(lut_s, p.lut, (1u << L) * 2u, bar_lut);
   }
   if (warp == kWarpProducer) tmem_alloc(smem_u32(tmem_holder), static_cast<uint32_t>(p.tmem_cols));
 
@@ -353,12 +357,13 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     constexpr int kEntries = 1 << L;
     uint16_t* lut_dst = reinterpret_cast<uint16_t*>(gbase + p.off_lut);
     if constexpr (kEntries >= 8) {
-      // fp16 table in by asynchronous copies (all in flight), then converted
-      // in place, 8 entries per step
-      stage_to_smem(lut_s, p.lut, kEntries * 2);
+      // the bulk copy issued with the barrier inits, then converted in place,
+      // 8 entries per step (a timed-out wait raises the abort flag, which
+      // every role's next wait sees)
       __syncthreads();
+      const bool in = mbar_wait(bar_lut, 0, abort_flag, p.err, kWhereTableStage);
       uint4* dst = reinterpret_cast<uint4*>(lut_dst);
-      for (int i = threadIdx.x; i < kEntries / 8; i += kThreads) {
+      for (int i = threadIdx.x; in && i < kEntries / 8; i += kThreads) {
         uint4 v = dst[i];
         uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
