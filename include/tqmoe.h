@@ -462,6 +462,17 @@ int tq_device_error(int* code, int* where);
 int tq_probe_lut_rate(const uint16_t* table, int warps_per_sm, int iters, uint32_t* sink,
                       unsigned long long* cycles, tq_stream_t stream);
 
+/* The bounded device-side wait ([P2] "The two changes": a failed or stuck
+ * launch must surface as an error, never as a silent result): launches one
+ * kernel whose single thread waits, through the same bounded mbarrier wait the
+ * pipelined kernels use, on a barrier that nothing arrives on, with a limit of
+ * timeout_ns (1e3 .. 2e9).  The wait gives up, records TQ_ERR_DEVICE_TIMEOUT
+ * (location tag 10) in the device error word and the kernel returns, leaving
+ * the context usable.  out (device) int[2], 4-byte aligned: out[0] = 1 if the
+ * wait completed (0 expected), out[1] = microseconds waited.  Returns
+ * TQ_ERR_INVALID_ARG on a bad argument, else the launch status. */
+int tq_probe_wait_timeout(int64_t timeout_ns, int* out, tq_stream_t stream);
+
 /* Host-side counts of successful launches since process start, per kernel:
  * out[0] route, out[1] tile map, out[2] grouped GEMM (trellis or dense),
  * out[3] GEMV, out[4] combine, out[5] activation gather, out[6] router

@@ -20,7 +20,7 @@ __all__ = [
     "tq_tiles_amortize", "tq_grouped_min_tokens", "tq_tile_map_capacity", "tq_native_tile_m", "TILE_NATIVE", "tq_select_arm",
     "tq_route", "tq_router_topk", "tq_route_logits", "tq_build_tile_map", "tq_gather_rows", "tq_prepare", "tq_grouped_gemm", "tq_gemv", "tq_combine",
     "tq_moe_workspace_size", "tq_moe_forward", "tq_moe_forward_static", "tq_device_error", "tq_launch_counts",
-    "tq_status_string", "tq_probe_lut_rate", "tq_grouped_gemm_pairs", "tq_swiglu",
+    "tq_status_string", "tq_probe_lut_rate", "tq_probe_wait_timeout", "tq_grouped_gemm_pairs", "tq_swiglu",
     "tq_moe_mlp_workspace_size", "tq_moe_mlp_forward", "tq_dequantize", "tq_grouped_gemm_dense",
     "tq_moe_dequant_workspace_size", "tq_moe_forward_dequant", "ARM_AUTO", "ARM_GEMV", "ARM_GROUPED", "ARM_MEASURED", "EXPORTED_SYMBOLS",
     "X_TOKENS", "X_PAIR_SORTED", "GATHER_MAX_TILE_M",
@@ -65,6 +65,7 @@ _SIGS = {
     "tq_moe_forward_static": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_int,
                                        _c_int, _c_int, _c_int, _c_int, _c_p, ctypes.POINTER(_c_int), _c_p]),
     "tq_probe_lut_rate": (_c_int, [_c_p, _c_int, _c_int, _c_p, _c_p, _c_p]),
+    "tq_probe_wait_timeout": (_c_int, [_c_i64, _c_p, _c_p]),
     "tq_grouped_gemm_pairs": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_int, _c_int,
                                        _c_int, _c_int, _c_int, _c_p, _c_p]),
     "tq_swiglu": (_c_int, [_c_p, _c_i64, _c_int, _c_p, _c_p]),
@@ -436,6 +437,18 @@ def tq_moe_forward_static(x, packed, lut, topk_ids, topk_w, tile_m: int = 16, pi
                                        pin, _dev_ptr(y, _bits16(), "y"), ctypes.byref(arm), _stream(stream)),
            "tq_moe_forward_static")
     return y, arm.value
+
+
+def tq_probe_wait_timeout(timeout_ns: int, stream=None) -> tuple[bool, int]:
+    """Run the bounded-wait probe: (whether the wait completed, microseconds
+    waited).  The give-up is recorded in the device error word."""
+    torch = _torch()
+    out = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    _check(lib().tq_probe_wait_timeout(int(timeout_ns), _dev_ptr(out, (torch.int32,), "out"), _stream(stream)),
+           "tq_probe_wait_timeout")
+    torch.cuda.synchronize()
+    done, us = out.tolist()
+    return bool(done), int(us)
 
 
 def tq_probe_lut_rate(warps_per_sm: int = 8, iters: int = 512, stream=None) -> float:

@@ -13,7 +13,7 @@ namespace tq {
 enum ErrWhere : int {
   kWhereRoute = 1, kWhereTileMap = 2, kWhereGroupedProducer = 3, kWhereGroupedDecode = 4,
   kWhereGroupedMma = 5, kWhereGroupedEpilogue = 6, kWhereGroupedTeardown = 7, kWhereDequant = 8,
-  kWhereTableStage = 9,
+  kWhereTableStage = 9, kWhereProbe = 10,
 };
 
 // A wait gives up after this long (ns of %globaltimer) and reports
@@ -95,17 +95,17 @@ __device__ __forceinline__ void bulk_stage_to_smem(uint32_t smem_dst, const void
 }
 
 // Wait for the phase with the given parity to complete.  Gives up when the
-// CTA-wide abort flag is raised or after kWaitTimeoutNs; in the latter case
+// CTA-wide abort flag is raised or after timeout_ns; in the latter case
 // raises the flag and records TQ_ERR_DEVICE_TIMEOUT.  Returns false on give-up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err, int where) {
+                                          int* err, int where, uint64_t timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitTimeoutNs) {
+      if (globaltimer() - t0 > timeout_ns) {
         *abort_flag = 1;
         record_error(err, TQ_ERR_DEVICE_TIMEOUT, where);
         return false;

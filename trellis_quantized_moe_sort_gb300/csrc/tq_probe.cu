@@ -47,8 +47,39 @@ __global__ void lut_probe_kernel(const uint16_t* __restrict__ table, int iters, 
   if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
 }
 
+// One thread waits, through the bounded wait of the pipelined kernels, on a
+// barrier that nothing arrives on: the wait gives up after timeout_ns, records
+// TQ_ERR_DEVICE_TIMEOUT in the device error word, and the kernel returns.
+// out[0] = 1 if the wait completed (it cannot), out[1] = microseconds waited.
+__global__ void wait_timeout_probe_kernel(uint64_t timeout_ns, int* __restrict__ err, int* __restrict__ out) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = smem_u32(&bar);
+  abort_flag = 0;
+  mbar_init(b, 1);
+  mbar_fence_init();
+  const uint64_t t0 = globaltimer();
+  const bool done = mbar_wait(b, 0, &abort_flag, err, kWhereProbe, timeout_ns);
+  const uint64_t us = (globaltimer() - t0) / 1000u;
+  out[0] = done ? 1 : 0;
+  out[1] = static_cast<int>(us < 0x7fffffffull ? us : 0x7fffffffull);
+}
+
 }  // namespace
 }  // namespace tq
+
+extern "C" int tq_probe_wait_timeout(int64_t timeout_ns, int* out, tq_stream_t stream) {
+  if (!out || (reinterpret_cast<uintptr_t>(out) & 3u) != 0 || timeout_ns < 1000 ||
+      timeout_ns > static_cast<int64_t>(tq::kWaitTimeoutNs))
+    return TQ_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int rc = tq::require_sm103(s);
+  if (rc != TQ_OK) return rc;
+  int* err = tq::error_word(&rc);
+  if (rc != TQ_OK) return rc;
+  tq::wait_timeout_probe_kernel<<<1, 1, 0, s>>>(static_cast<uint64_t>(timeout_ns), err, out);
+  return tq::launch_status();
+}
 
 extern "C" int tq_probe_lut_rate(const uint16_t* table, int warps_per_sm, int iters, uint32_t* sink,
                                  unsigned long long* cycles, tq_stream_t stream) {
