@@ -77,6 +77,11 @@ WORKLOADS: dict[str, list[Shape]] = {
                                   routing="zipf")],
     "v4_prefill_n8192_down": [Shape("v4_prefill_n8192_down", 256, 6, 8192, 2048, 4096, 16,
                                     routing="zipf")],
+    # The same prefill with the popularity ranks shuffled over the expert ids
+    # (the heavy experts anywhere in id order); appended last so the others
+    # keep their seeds.
+    "v4_prefill_n8192_up_zipf_perm": [Shape("v4_prefill_n8192_up_zipf_perm", 256, 6, 8192, 4096, 2048, 16,
+                                            routing="zipf_perm")],
 }
 
 # Stable numeric id per workload (enters the seed).
@@ -108,8 +113,11 @@ def draw_routing(rng: np.random.Generator, n: int, E: int, k: int, routing: str 
     """Return (topk_ids int32 [n,k], topk_w float32 [n,k])."""
     if routing == "uniform":
         scores = rng.standard_normal((n, E)).astype(np.float32).astype(np.float64)
-    elif routing == "zipf":
-        logp = -zipf_s * np.log(np.arange(1, E + 1, dtype=np.float64))
+    elif routing in ("zipf", "zipf_perm"):
+        # popularity rank r (0 = most popular) has p ~ (r + 1)^-s; "zipf" gives
+        # expert e rank e, "zipf_perm" a random bijection of experts to ranks
+        rank = np.arange(E) if routing == "zipf" else rng.permutation(E)
+        logp = -zipf_s * np.log(rank.astype(np.float64) + 1.0)
         scores = logp[None, :] + rng.gumbel(size=(n, E))
     else:
         raise ValueError(f"unknown routing {routing!r}")

@@ -40,6 +40,7 @@ SMALL = {
     "L2": (3, 3, 20, 320, 128, 2, 16, "uniform"),
     "L4_L6_mix": (5, 2, 24, 128, 128, 6, 16, "uniform"),
     "zipf_T128": (32, 4, 200, 256, 256, 14, 128, "zipf"),
+    "zipf_perm_T256": (32, 4, 400, 320, 256, 16, 256, "zipf_perm"),
     # fp32 output > 24 MB and thousands of units: blocked row order, whole
     # units round-robin over the CTAs
     "interleaved_n6000_N1024": (64, 2, 6000, 64, 1024, 8, 16, "uniform"),

@@ -125,7 +125,8 @@ def test_moe_forward_in_cuda_graph(pin):
     ("tiny_e8_k2_n16", tq.ARM_AUTO, tq.ARM_GEMV, 128),
     ("v4_decode_n32", tq.ARM_GROUPED, tq.ARM_GROUPED, 16),
     ("v4_prefill_n8192_up", tq.ARM_AUTO, tq.ARM_GROUPED, 256),
-    ("v4_prefill_n8192_down", tq.ARM_AUTO, tq.ARM_GROUPED, 256)])
+    ("v4_prefill_n8192_down", tq.ARM_AUTO, tq.ARM_GROUPED, 256),
+    ("v4_prefill_n8192_up_zipf_perm", tq.ARM_AUTO, tq.ARM_GROUPED, 256)])
 def test_moe_forward_native_tile(name, pin, want_arm, want_tile):
     """tile_m = TQ_TILE_NATIVE: the pages' TILE_M gates the arm, the kernel runs
     its native tile (256 at the prefill sizes: the down projection's K = 2048

@@ -19,6 +19,7 @@ STATED = {
     "v4_fill_n1024": (256, 6, 1024, 4096, 2048, 16, "uniform"),
     "v4_prefill_n8192_up": (256, 6, 8192, 4096, 2048, 16, "zipf"),
     "v4_prefill_n8192_down": (256, 6, 8192, 2048, 4096, 16, "zipf"),
+    "v4_prefill_n8192_up_zipf_perm": (256, 6, 8192, 4096, 2048, 16, "zipf_perm"),
 }
 
 
@@ -63,7 +64,7 @@ def test_packed_bytes_are_uniform():
     assert chi2 < 400   # 255 degrees of freedom: mean 255, sd ~23
 
 
-@pytest.mark.parametrize("name", ["v4_decode_n32", "v4_prefill_n8192_up"])
+@pytest.mark.parametrize("name", ["v4_decode_n32", "v4_prefill_n8192_up", "v4_prefill_n8192_up_zipf_perm"])
 def test_routing_structure(name):
     p = moe_inputs.make_problem(name, with_packed=False)
     s = p.shape
@@ -81,6 +82,13 @@ def test_routing_structure(name):
         # more than their 1/16 share of pairs, and the most popular is expert 0
         assert counts[:16].sum() > 0.25 * counts.sum()
         assert int(np.argmax(counts)) == 0
+    elif s.routing == "zipf_perm":
+        # the same skew with the ranks shuffled over the ids: the 16 most
+        # popular experts still take far more than their share, but they are
+        # not the lowest ids
+        top = np.argsort(-counts, kind="stable")[:16]
+        assert counts[top].sum() > 0.25 * counts.sum()
+        assert top.max() >= 64 and int(np.argmax(counts)) != 0
     else:
         # uniform: no expert far above its share n*k/E
         assert counts.max() < 5 * s.n * s.top_k / s.E + 5
