@@ -151,3 +151,27 @@ def test_moe_forward_native_tile(name, pin, want_arm, want_tile):
     rows = sample_rows(s.N, 24, seed=3) if s.N > 256 else np.arange(s.N)
     ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L, rows=rows)
     assert normwise(y.float().cpu().numpy()[:, rows], ref) <= TOL
+
+
+def test_moe_forward_offsets_past_2_gib():
+    """65,536 tokens x top-6 of 256 experts at K = 4096, N = 2048 through the
+    whole product at its native m-tile (256): the pair-sorted activations are
+    393,216 rows x 8 KiB = 3.2 GB, so every address past row 262,144 is beyond
+    2^31 bytes, and the route runs its largest grid (64 blocks of 6,144 pairs).
+    Sampled tokens (their pairs land anywhere in the sorted order) and rows
+    against the oracle."""
+    E, k, n, K, N, L = 256, 6, 65536, 4096, 2048, 16
+    prob = moe_inputs.make_custom(E, k, n, K, N, L, seed=65536)
+    d = to_device(prob)
+    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=tq.TILE_NATIVE,
+                               pin=tq.ARM_AUTO)
+    check_no_device_error()
+    assert arm == tq.ARM_GROUPED and tq.tq_native_tile_m(n, k, E) == 256
+    rng = np.random.Generator(np.random.PCG64(11))
+    toks = np.unique(np.concatenate([[0, n - 1], rng.choice(n, 254, replace=False)]))
+    rows = sample_rows(N, 32, seed=5)
+    ref = O.moe_forward(prob.x_bits[toks], prob.topk_ids[toks], prob.topk_w[toks], prob.packed, prob.lut_bits, L,
+                        rows=rows)
+    got = y[torch.from_numpy(toks).cuda()][:, torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    assert normwise(got, ref) <= TOL
+

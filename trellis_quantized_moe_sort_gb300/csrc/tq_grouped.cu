@@ -150,9 +150,10 @@ struct Tile {
 };
 __device__ __forceinline__ Tile read_tile(const Params& p, int tile) {
   Tile t;
-  t.e = p.tiles[3 * tile];
-  t.slot0 = p.tiles[3 * tile + 1];
-  t.rows = p.tiles[3 * tile + 2];
+  const int32_t* const entry = p.tiles + 3ll * tile;
+  t.e = entry[0];
+  t.slot0 = entry[1];
+  t.rows = entry[2];
   t.ok = t.e >= 0 && t.e < p.E && t.rows >= 1 && t.rows <= p.tile_m && t.slot0 >= 0 &&
          t.slot0 <= p.P - t.rows;
   return t;
