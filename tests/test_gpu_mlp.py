@@ -155,3 +155,24 @@ def test_swiglu_kernel():
     ref = O.silu(g) * u
     got = h.float().cpu().numpy()
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30)
+
+
+def test_mlp_offsets_past_2_gib():
+    """70,000 tokens x top-4 of 16 experts, H = I = 1024, native m-tile 256: the
+    per-pair gate|up accumulator is 280,000 x 2048 fp32 = 2.29 GB, so its rows
+    past 262,144 sit beyond 2^31 bytes (as do the SwiGLU's reads of them).
+    Sampled tokens against the oracle's whole MLP."""
+    E, k, n, H, I, L = 16, 4, 70000, 1024, 1024, 16
+    prob = moe_inputs.make_mlp_custom(E, k, n, H, I, L, seed=70000)
+    d = _mlp_dev(prob)
+    y, arm = tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"],
+                                   tile_m=tq.TILE_NATIVE, pin=tq.ARM_AUTO)
+    check_no_device_error()
+    assert arm == tq.ARM_GROUPED
+    rng = np.random.Generator(np.random.PCG64(12))
+    toks = np.unique(np.concatenate([[0, n - 1], rng.choice(n, 62, replace=False)]))
+    ref = O.moe_mlp(prob.x_bits[toks], prob.topk_ids[toks], prob.topk_w[toks], prob.packed_gu, prob.lut_gu,
+                    prob.packed_down, prob.lut_down, prob.L)
+    got = y[torch.from_numpy(toks).cuda()].float().cpu().numpy()
+    assert normwise(got, ref) <= TOL
+
