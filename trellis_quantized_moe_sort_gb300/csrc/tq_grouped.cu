@@ -16,6 +16,8 @@
 //               rows x 128 bytes (512 symbols = 8 k-steps of 64) per
 //               "super-stage", 128B-swizzled; wide rows keep the TMA unit's
 //               per-row cost low.
+//   (with E epilogue warps, 4 or 8: the decode warps start at 2 + E and the
+//   activation producer follows them; the numbers below are for E = 4)
 //   warp 14     TMA producer for activations, 64 columns per k-step into the
 //               MMA's 128B-swizzled B layout: gathered from the token rows of
 //               x, four rows per copy (small m-tiles), or, from the
@@ -26,7 +28,9 @@
 //               (N = pairs of the tile padded to 16), fp32 accumulator in
 //               tensor memory.
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator, scale by the router
-//               weight, 16-byte fp32 vector reductions into y32[token][rows].
+//               weight, 16-byte fp32 vector reductions into y32[token][rows];
+//               eight warps (2-9, two per lane quarter) when the m-tiles span
+//               both accumulator slots.
 //   warps 6-13  decode: thread (quarter q, half h) owns weight row 32q + lane
 //               and symbols [32h, 32h + 32) of each k-step; the state of each
 //               symbol is a shift + mask of a 64-bit window of the staged
@@ -68,20 +72,26 @@ constexpr int kActRowBytes = kKStep * 2;             // one 128-byte swizzle row
 constexpr int kATmemCols = kKStep / 2;               // bf16x2 columns per A stage
 constexpr int kNumAStages = 8;
 constexpr int kNumDecodeWarps = 8;
-constexpr int kNumEpiWarps = 4;
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpEpi0 = 2;
-constexpr int kWarpDec0 = kWarpEpi0 + kNumEpiWarps;
-constexpr int kWarpActProducer = kWarpDec0 + kNumDecodeWarps;
-constexpr int kThreads = 32 * (kWarpActProducer + 1);  // 480
 constexpr int kMaxPkStages = 6;
 constexpr int kActPrefetch = 8;                       // k-steps of activations asked into L2 ahead
 constexpr int kMaxActStages = 8;
 constexpr int kSmemLimit = 232448;                   // 227 KiB opt-in per block
 constexpr int kNumBars = 2 * kMaxPkStages + 2 * kMaxActStages + 2 * kNumAStages + 2 + 2 + 1 + 1;
 static_assert(kNumDecodeWarps == 8, "decode mapping assumes 2 warps per TMEM lane quarter");
-static_assert(kWarpEpi0 % 4 == 2 && kWarpDec0 % 4 == 2, "role warps must cover all four quarters");
+// Warp roles for kEpi epilogue warps (4: one per lane quarter; 8, used when
+// the units span both accumulator slots: two per quarter, each draining half
+// of the columns, so a drain the next large unit waits for takes half as long).
+// Four: 480 threads; eight: 608.
+template <int kEpi>
+struct Roles {
+  static constexpr int dec0 = kWarpEpi0 + kEpi;
+  static constexpr int act = dec0 + kNumDecodeWarps;
+  static constexpr int threads = 32 * (act + 1);
+  static_assert(kEpi % 4 == 0 && dec0 % 4 == 2, "role warps must cover all four quarters");
+};
 
 struct Params {
   const int32_t* sorted_pairs;
@@ -292,8 +302,8 @@ __device__ __forceinline__ void drain_ring(uint32_t bar0, Pipe pipe, int nstages
 // [E][N][K] through TMA (one 128 x 64 box per k-step into the same ring the
 // packed bytes use) and the MMA reads it from shared memory; the decode warps
 // and the LUT stay idle.
-template <int L, bool kDense>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int L, bool kDense, int kEpi>
+__global__ void __launch_bounds__(Roles<kEpi>::threads, 1)
 grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_constant__ CUtensorMap tm_xs,
                const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -342,7 +352,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_accfull + 8 * b, 1);
-      mbar_init(bar_accempty + 8 * b, kNumEpiWarps);
+      mbar_init(bar_accempty + 8 * b, kEpi);
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_lut, 1);
@@ -364,7 +374,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
       __syncthreads();
       const bool in = mbar_wait(bar_lut, 0, abort_flag, p.err, kWhereTableStage);
       uint4* dst = reinterpret_cast<uint4*>(lut_dst);
-      for (int i = threadIdx.x; in && i < kEntries / 8; i += kThreads) {
+      for (int i = threadIdx.x; in && i < kEntries / 8; i += Roles<kEpi>::threads) {
         uint4 v = dst[i];
         uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -377,7 +387,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
         dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
       }
     } else {
-      for (int i = threadIdx.x; i < kEntries; i += kThreads) {
+      for (int i = threadIdx.x; i < kEntries; i += Roles<kEpi>::threads) {
         const __nv_bfloat16 b = __float2bfloat16_rn(__half2float(__ushort_as_half(p.lut[i])));
         lut_dst[i] = *reinterpret_cast<const uint16_t*>(&b);
       }
@@ -438,7 +448,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     // Teardown: every copy issued must have landed before the CTA exits.
     __syncwarp();
     drain_ring(bar_pkfull, pk, SP, pk_issued, p.err);
-  } else if (warp == kWarpActProducer) {
+  } else if (warp == Roles<kEpi>::act) {
     // ------------------------------------------------------------ activation producer
     // Gathered (act_gather): the tile's rows are token rows of x, four per
     // gather copy; lane l copies row groups l and l + 32 (rows 4g .. 4g+3)
@@ -593,9 +603,10 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
       }
     }
     __syncwarp();
-  } else if (warp < kWarpDec0) {
+  } else if (warp < Roles<kEpi>::dec0) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
+    const int eh = (warp - kWarpEpi0) >> 2;   // with 8 epilogue warps: which half of the columns
     Pipe accp;
     AccSlots slots;
     Walk w = walk0;
@@ -604,6 +615,11 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
       const Tile tl = read_tile(p, sg.tile);
       if (!tl.ok) continue;
       const int slot0 = tl.slot0, rows = tl.rows;
+      const uint32_t n_mma = static_cast<uint32_t>((rows + 15) & ~15);
+      const bool two_slots = p.acc_slots && AccSlots::big(n_mma);
+      // the 32-column blocks this warp drains: all (4 warps); with 8, one slot
+      // each for a unit spanning both slots, else alternate blocks
+      auto mine = [&](int b) { return kEpi == 4 || (two_slots ? (b >> 2) == eh : (b & 1) == eh); };
       // Output row and weight of every column of the tile, loaded while the
       // MMAs run: lane j holds columns j + 32i (i < 8; tile_m <= 256), and the
       // drain below takes them by shuffle.  -1 = no output (past the tile, or
@@ -615,7 +631,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
         const int col = lane + 32 * i;
         orow[i] = -1;
         owt[i] = 0.f;
-        if (col < rows) {
+        if (col < rows && mine(i)) {
           if (p.pair_out) {
             orow[i] = slot0 + col;
             owt[i] = 1.f;
@@ -630,8 +646,6 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
           }
         }
       }
-      const uint32_t n_mma = static_cast<uint32_t>((rows + 15) & ~15);
-      const bool two_slots = p.acc_slots && AccSlots::big(n_mma);
       int acc_first, acc_done;   // full barrier to wait on; empty barrier to arrive on at the end
       uint32_t acc_ph;
       if (p.acc_slots) {
@@ -647,6 +661,12 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
       }
       if (!mbar_wait(bar_accfull + 8 * acc_first, acc_ph, abort_flag, p.err, kWhereGroupedEpilogue)) break;
       tc_fence_after();
+      if (kEpi == 8 && two_slots && eh == 1) {
+        // this half reads only the second slot: the first is free as far as it goes
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_accempty);
+      }
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(p.acc_slots ? 128 * acc_first : acc_first * p.n_mma_max);
       // Each 4x4 block (4 lanes = 4 consecutive rows, 4 pair columns) is
@@ -657,6 +677,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
         if (32 * b >= rows) break;
+        if (!mine(b)) continue;
         // both 16-column halves of the block in flight before one wait
         uint32_t v2[2][16];
         tmem_ld16(t_acc + 32 * b, v2[0]);
@@ -709,7 +730,7 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
     }
   } else if constexpr (!kDense) {
     // ------------------------------------------------------------ decode
-    const int dw = warp - kWarpDec0;
+    const int dw = warp - Roles<kEpi>::dec0;
     const int q = warp & 3;
     const int h = dw >> 2;
     const uint32_t row = static_cast<uint32_t>(32 * q + lane);
@@ -795,20 +816,21 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
 }
 
 template <int L>
-void* kernel_ptr() {
-  return reinterpret_cast<void*>(&grouped_kernel<L, false>);
+void* kernel_ptr(bool epi8) {
+  return epi8 ? reinterpret_cast<void*>(&grouped_kernel<L, false, 8>)
+              : reinterpret_cast<void*>(&grouped_kernel<L, false, 4>);
 }
 
-void* grouped_kernel_for(int L) {
+void* grouped_kernel_for(int L, bool epi8) {
   switch (L) {
-    case 2: return kernel_ptr<2>();
-    case 4: return kernel_ptr<4>();
-    case 6: return kernel_ptr<6>();
-    case 8: return kernel_ptr<8>();
-    case 10: return kernel_ptr<10>();
-    case 12: return kernel_ptr<12>();
-    case 14: return kernel_ptr<14>();
-    case 16: return kernel_ptr<16>();
+    case 2: return kernel_ptr<2>(epi8);
+    case 4: return kernel_ptr<4>(epi8);
+    case 6: return kernel_ptr<6>(epi8);
+    case 8: return kernel_ptr<8>(epi8);
+    case 10: return kernel_ptr<10>(epi8);
+    case 12: return kernel_ptr<12>(epi8);
+    case 14: return kernel_ptr<14>(epi8);
+    case 16: return kernel_ptr<16>(epi8);
     default: return nullptr;
   }
 }
@@ -837,8 +859,7 @@ int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
   auto encode = encode_fn();
   if (!encode) return TQ_ERR_CUDA;
   const bool dense = dense_w != nullptr;
-  void* kfn = dense ? reinterpret_cast<void*>(&grouped_kernel<2, true>) : grouped_kernel_for(L);
-  if (!kfn) return TQ_ERR_INVALID_ARG;
+  if (!dense && !grouped_kernel_for(L, false)) return TQ_ERR_INVALID_ARG;
 
   Params p{};
   p.sorted_pairs = sorted_pairs;
@@ -890,6 +911,10 @@ int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
   // m-tiles above 128 pairs beside the 8 A stages: two 128-column slots
   p.acc_slots = (!dense && p.nacc == 1) ? 1 : 0;
   p.acol0 = p.acc_slots ? 256 : p.nacc * p.n_mma_max;
+  // units above 128 pairs (both accumulator slots): eight epilogue warps
+  const bool epi8 = !dense && p.acc_slots;
+  void* kfn = dense ? reinterpret_cast<void*>(&grouped_kernel<2, true, 4>) : grouped_kernel_for(L, epi8);
+  const int threads = epi8 ? Roles<8>::threads : Roles<4>::threads;
   const int cols_needed = p.acol0 + a_cols;
   int cols = 32;
   while (cols < cols_needed) cols <<= 1;
@@ -969,7 +994,7 @@ int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
   void* args[] = {&tm_packed, &tm_xs, &p};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   // The kernel may start while the previous kernel on the stream finishes; it
