@@ -60,6 +60,7 @@ SMALL = {
     "one_expert_E1": (1, 1, 300, 256, 128, 16, 128, "uniform"),
     "E1024_k8_n64": (1024, 8, 64, 256, 128, 12, 16, "uniform"),
     "one_token_n1": (16, 4, 1, 256, 256, 16, 16, "uniform"),
+    "single_pair_k1": (4, 1, 1, 128, 128, 12, 16, "uniform"),
 }
 
 

@@ -176,3 +176,38 @@ def test_mlp_offsets_past_2_gib():
     got = y[torch.from_numpy(toks).cuda()].float().cpu().numpy()
     assert normwise(got, ref) <= TOL
 
+
+@pytest.mark.parametrize("tile_m,pin", [(16, tq.ARM_GROUPED), (tq.TILE_NATIVE, tq.ARM_GROUPED), (16, tq.ARM_GEMV)])
+def test_mlp_in_cuda_graph(tile_m, pin):
+    """The whole expert MLP captured in a CUDA graph (every launch a
+    programmatic dependent of the one before) and replayed on new inputs
+    copied into the captured buffers, on both arms and at the native m-tile
+    (256 here: 150 pairs per expert); every replay against the oracle."""
+    probs = [moe_inputs.make_mlp_custom(8, 2, 600, 256, 256, 12, seed=sd) for sd in (901, 902)]
+    p0 = probs[0]
+    n, k, E, H, I = p0.n, p0.top_k, p0.E, p0.H, p0.I
+    if tile_m == tq.TILE_NATIVE:
+        assert tq.tq_native_tile_m(n, k, E) == 256
+    devs = [_mlp_dev(p) for p in probs]
+    d = {key: v.clone() for key, v in devs[0].items()}
+    ws = torch.empty(tq.tq_moe_mlp_workspace_size(n, k, E, H, I, tile_m), dtype=torch.uint8, device="cuda")
+    y = torch.empty((n, H), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    call = lambda: tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"],
+                                         tile_m=tile_m, pin=pin, workspace=ws, y=y)
+    with torch.cuda.stream(stream):
+        call()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        call()
+    for prob, src in zip(probs + probs[:1], devs + devs[:1]):
+        for key in d:
+            d[key].copy_(src[key])
+        g.replay()
+        torch.cuda.synchronize()
+        check_no_device_error()
+        ref = O.moe_mlp(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed_gu, prob.lut_gu, prob.packed_down,
+                        prob.lut_down, prob.L)
+        assert normwise(y.float().cpu().numpy(), ref) <= TOL
+

@@ -175,3 +175,35 @@ def test_moe_forward_offsets_past_2_gib():
     got = y[torch.from_numpy(toks).cuda()][:, torch.from_numpy(rows).cuda()].float().cpu().numpy()
     assert normwise(got, ref) <= TOL
 
+
+def test_moe_forward_in_cuda_graph_native_tile():
+    """The whole product at its native m-tile 256 (the pair-sorted gather
+    launch, then the grouped kernel with eight epilogue warps) captured in a
+    CUDA graph and replayed on new inputs copied into the captured buffers;
+    every replay against the oracle on all outputs."""
+    probs = [moe_inputs.make_custom(16, 4, 2048, 512, 256, 12, seed=sd) for sd in (801, 802)]
+    s = probs[0].shape
+    assert tq.tq_native_tile_m(s.n, s.top_k, s.E) == 256
+    devs = [to_device(p) for p in probs]
+    d = {k: v.clone() for k, v in devs[0].items()}
+    ws = torch.empty(tq.tq_moe_workspace_size(s.n, s.top_k, s.E, s.K, s.N, tq.TILE_NATIVE), dtype=torch.uint8,
+                     device="cuda")
+    y = torch.empty((s.n, s.N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    call = lambda: tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=tq.TILE_NATIVE,
+                                     pin=tq.ARM_GROUPED, workspace=ws, y=y)
+    with torch.cuda.stream(stream):
+        call()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        call()
+    for prob, src in zip(probs + probs[:1], devs + devs[:1]):
+        for k in d:
+            d[k].copy_(src[k])
+        g.replay()
+        torch.cuda.synchronize()
+        check_no_device_error()
+        ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L)
+        assert normwise(y.float().cpu().numpy(), ref) <= TOL
+
