@@ -415,6 +415,10 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ packed-byte producer
     if (lane == 0) tma_prefetch_desc(&tm_packed);
+    // Packed bytes are read once per m-tile: mark them first to leave L2, so
+    // that the fp32 output slice the atomics add into stays resident (prefill
+    // DRAM traffic 1.774 -> 1.692 GB at the down projection, time unchanged).
+    const uint64_t pk_policy = l2_evict_first_policy();
     Pipe pk;
     long long pk_issued = 0;
     bool ok = true;
@@ -439,7 +443,8 @@ grouped_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_const
         if (lane == 0) {
           const uint32_t full = bar_pkfull + 8 * pk.stage;
           mbar_arrive_expect_tx(full, kPkStageBytes);
-          tma_load_2d(pk0 + pk.stage * kPkStageBytes, &tm_packed, kDense ? i * kKStep : i * kSSBytes, row_g, full);
+          tma_load_2d_hint(pk0 + pk.stage * kPkStageBytes, &tm_packed, kDense ? i * kKStep : i * kSSBytes, row_g,
+                           full, pk_policy);
         }
         ++pk_issued;
         pk.advance(SP);
