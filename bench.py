@@ -18,7 +18,6 @@ import os
 import argparse
 import concurrent.futures
 import json
-import math
 import multiprocessing
 import platform
 import shutil

@@ -41,7 +41,6 @@ R7  Gate.  tiles_amortize(n,k,E,T) := n > 0 and
 """
 from __future__ import annotations
 
-import math
 import numpy as np
 
 __all__ = [
