@@ -121,6 +121,40 @@ def test_grouped_accumulator_slots_all_outputs(reps, N, T, K):
     assert normwise(y, ref) <= TOL
 
 
+def _random_configs(count=24, seed=2026):
+    """Seeded shapes anywhere inside the documented limits (K % 64 == 0,
+    N % 128 == 0, L even in [2, 16], 1 <= tile_m <= 256, top_k <= E), small
+    enough for the oracle on every output: (E, top_k, n, K, N, L, tile_m)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    while len(out) < count:
+        E = int(rng.integers(1, 65))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        n = int(rng.integers(1, 301))
+        K = 64 * int(rng.integers(1, 41))
+        N = 128 * int(rng.integers(1, 5))
+        L = 2 * int(rng.integers(1, 9))
+        T = int(rng.choice([1, 2, 5, 16, 24, 48, 64, 100, 128, 160, 192, 256]))
+        if n * k * K * N <= 6e7:
+            out.append((E, k, n, K, N, L, T))
+    return out
+
+
+@pytest.mark.parametrize("cfg", _random_configs(), ids=lambda c: "E{}_k{}_n{}_K{}_N{}_L{}_T{}".format(*c))
+def test_random_shapes_all_outputs(cfg):
+    """Both arms, and the grouped arm on both activation layouts, on seeded
+    random shapes: every output against the oracle."""
+    E, k, n, K, N, L, T = cfg
+    prob = moe_inputs.make_custom(E, k, n, K, N, L, seed=zlib.crc32(repr(cfg).encode()) % 1000)
+    d = to_device(prob)
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, L)
+    for lay in (tq.X_TOKENS, tq.X_PAIR_SORTED):
+        y = grouped_y32(prob, d, T, lay).cpu().numpy()
+        assert normwise(y, ref) <= TOL, (lay, normwise(y, ref))
+    y = gemv_y32(prob, d).cpu().numpy()
+    assert normwise(y, ref) <= TOL_GEMV
+
+
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_gemv_small_all_outputs(name):
     prob, _ = _small(name)
