@@ -211,3 +211,37 @@ def test_mlp_in_cuda_graph(tile_m, pin):
                         prob.lut_down, prob.L)
         assert normwise(y.float().cpu().numpy(), ref) <= TOL
 
+
+def _random_mlp_configs(count=8, seed=77):
+    """Seeded expert-MLP shapes inside the documented limits (H % 128 == 0,
+    I % 64 == 0, L even): (E, top_k, n, H, I, L, tile_m, pin)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    while len(out) < count:
+        E = int(rng.integers(1, 17))
+        k = int(rng.integers(1, min(E, 4) + 1))
+        n = int(rng.integers(1, 121))
+        H = 128 * int(rng.integers(1, 5))
+        I = 64 * int(rng.integers(1, 9))
+        L = 2 * int(rng.integers(2, 9))
+        T = int(rng.choice([16, 64, 256, tq.TILE_NATIVE]))
+        pin = int(rng.choice([tq.ARM_GROUPED, tq.ARM_GEMV]))
+        out.append((E, k, n, H, I, L, T, pin))
+    return out
+
+
+@pytest.mark.parametrize("cfg", _random_mlp_configs(),
+                         ids=lambda c: "E{}_k{}_n{}_H{}_I{}_L{}_T{}_arm{}".format(*c))
+def test_mlp_random_shapes_all_outputs(cfg):
+    """The whole expert MLP on seeded random shapes, every output against the oracle."""
+    E, k, n, H, I, L, T, pin = cfg
+    prob = moe_inputs.make_mlp_custom(E, k, n, H, I, L, seed=sum(cfg) % 997)
+    d = _mlp_dev(prob)
+    y, arm = tq.tq_moe_mlp_forward(d["x"], d["pgu"], d["lgu"], d["pd"], d["ld"], d["ids"], d["w"], tile_m=T,
+                                   pin=pin)
+    check_no_device_error()
+    assert arm == pin
+    ref = O.moe_mlp(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed_gu, prob.lut_gu, prob.packed_down,
+                    prob.lut_down, prob.L)
+    assert normwise(y.float().cpu().numpy(), ref) <= TOL
+
