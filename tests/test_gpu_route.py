@@ -213,3 +213,56 @@ def test_prepare_bitexact_against_oracle(name, tile_m):
     assert np.array_equal(tiles[:got_n].cpu().numpy(), np.asarray(want, dtype=np.int32).reshape(-1, 3))
     if n * k:
         np.testing.assert_array_equal(xs[:n * k].cpu().numpy().view(np.uint16), x_bits[s // k])
+
+
+def _random_routings(count=16, seed=404):
+    """Seeded routings: E up to 1024, top_k up to 16, up to 40,000 tokens
+    (up to 640,000 pairs: the sort's largest grid), uniform, Zipf and
+    shuffled-rank Zipf popularity, a random m-tile: (ids, E, tile_m)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for _ in range(count):
+        E = int(rng.integers(1, 1025))
+        k = int(rng.integers(1, min(E, 16) + 1))
+        n = int(rng.choice([0, 1, int(rng.integers(2, 600)), int(rng.integers(600, 40001))],
+                           p=[0.06, 0.06, 0.44, 0.44]))
+        routing = str(rng.choice(["uniform", "zipf", "zipf_perm"]))
+        ids, _ = moe_inputs.draw_routing(rng, n, E, k, routing)
+        out.append((ids.reshape(n, k), E, int(rng.integers(1, 257))))
+    return out
+
+
+RANDOM_ROUTINGS = _random_routings()
+
+
+@pytest.mark.parametrize("i", range(len(RANDOM_ROUTINGS)))
+def test_prepare_random_routings_bitexact(i):
+    """The fused route + tile map launch and the gather against the oracle's
+    route and tile map, bit for bit, on seeded random routings."""
+    ids, E, tile_m = RANDOM_ROUTINGS[i]
+    n, k = ids.shape
+    K = 64
+    rng = np.random.Generator(np.random.PCG64(1000 + i))
+    x_bits = moe_inputs.fp32_to_bf16_bits(rng.standard_normal((n, K), dtype=np.float32))
+    d_ids = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32)).cuda()
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda()
+    cap = tq.tq_tile_map_capacity(n, k, E, tile_m)
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    sp = torch.empty(max(n * k, 1), dtype=torch.int32, device="cuda")
+    tiles = torch.empty((max(cap, 1), 3), dtype=torch.int32, device="cuda")
+    nt = torch.empty(1, dtype=torch.int32, device="cuda")
+    xs = torch.empty((max(n * k, 1), K), dtype=torch.int16, device="cuda")
+    tq.tq_prepare(d_ids, x, E, tile_m, max(cap, 1), counts, offsets, sp[:n * k], tiles, nt, xs[:n * k])
+    check_no_device_error()
+    c, o, s = O.route(ids, E)
+    assert np.array_equal(counts.cpu().numpy(), c)
+    assert np.array_equal(offsets.cpu().numpy(), o)
+    assert np.array_equal(sp[:n * k].cpu().numpy(), s)
+    want = O.tile_map(o, tile_m)
+    got_n = int(nt.item())
+    assert got_n == len(want)
+    assert np.array_equal(tiles[:got_n].cpu().numpy(), np.asarray(want, dtype=np.int32).reshape(-1, 3))
+    if n * k:
+        np.testing.assert_array_equal(xs[:n * k].cpu().numpy().view(np.uint16), x_bits[s // k])
+
