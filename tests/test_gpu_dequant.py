@@ -95,6 +95,26 @@ def test_dequantize_out_of_range_id_reports():
     np.testing.assert_array_equal(_bits(w[0]), _expected_bits(prob.packed[1], prob.lut_bits, 8))
 
 
+def _random_deq(count=12, seed=31):
+    """Seeded (E, N, K, L): K a multiple of 8 up to 4600 (partial passes and
+    several chunks), any N, every even L."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return [(int(rng.integers(1, 5)), int(rng.integers(1, 40)), 8 * int(rng.integers(1, 576)),
+             2 * int(rng.integers(1, 9))) for _ in range(count)]
+
+
+@pytest.mark.parametrize("cfg", _random_deq(), ids=lambda c: "E{}_N{}_K{}_L{}".format(*c))
+def test_dequantize_random_shapes_bit_exact(cfg):
+    E, N, K, L = cfg
+    prob = moe_inputs.make_custom(E, 1, 1, K, N, L, seed=zlib.crc32(repr(cfg).encode()) % 1000)
+    d = to_device(prob)
+    w = tq.tq_dequantize(d["packed"], d["lut"])
+    check_no_device_error()
+    got = _bits(w)
+    for e in range(E):
+        np.testing.assert_array_equal(got[e], _expected_bits(prob.packed[e], prob.lut_bits, L), err_msg=f"e={e}")
+
+
 # (E, top_k, n, K, N, L, tile_m, routing)
 FWD = {
     "tiny_T16": (8, 2, 16, 256, 128, 12, 16, "uniform"),

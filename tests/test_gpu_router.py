@@ -61,3 +61,33 @@ def test_route_logits_equals_route_of_oracle_ids():
     assert np.array_equal(counts.cpu().numpy(), c)
     assert np.array_equal(offsets.cpu().numpy(), o)
     assert np.array_equal(sp.cpu().numpy(), s)
+
+
+def _random_router_cases(count=10, seed=909):
+    """Seeded logits: E up to 1024, top_k up to min(E, 32), up to 3000 tokens;
+    half of them rounded to a few values so that exact ties are common."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for i in range(count):
+        E = int(rng.integers(1, 1025))
+        k = int(rng.integers(1, min(E, 32) + 1))
+        n = int(rng.integers(1, 3001))
+        logits = rng.standard_normal((n, E)).astype(np.float32)
+        if i % 2:
+            logits = np.round(logits * 2).astype(np.float32)
+        out.append((logits, k))
+    return out
+
+
+RANDOM_CASES = _random_router_cases()
+
+
+@pytest.mark.parametrize("i", range(len(RANDOM_CASES)))
+def test_router_topk_random_matches_oracle(i):
+    logits, k = RANDOM_CASES[i]
+    ids, w = tq.tq_router_topk(torch.from_numpy(logits).cuda(), k)
+    check_no_device_error()
+    want_ids, want_w = O.router_topk(logits, k)
+    assert np.array_equal(ids.cpu().numpy(), want_ids)
+    assert np.allclose(w.cpu().numpy().astype(np.float64), want_w, rtol=1e-6, atol=1e-7)
+
