@@ -316,7 +316,10 @@ int tq_combine(const float* y32, uint16_t* y, int64_t count, tq_stream_t stream)
  *   tq_moe_workspace_size(n, top_k, E, K, N, tile_m) bytes, 256-byte aligned.
  *   It holds counts, offsets, sorted pairs, the tile map, the fp32
  *   accumulator and, for a kernel m-tile above TQ_GATHER_MAX_TILE_M, the
- *   pair-sorted activations; its contents are undefined after the call.
+ *   pair-sorted activations and the sort's inverse (the sorted slot of each
+ *   pair, written by the routing launch, through which the activations are
+ *   copied in token order: each row of x read once); its contents are
+ *   undefined after the call.
  * tile_m: 1..256, the m-tile of both the arm selection and the kernel, or
  *   TQ_TILE_NATIVE (tq_native_tile_m for the kernel, TQ_GATE_TILE_M for the
  *   selection).
@@ -383,8 +386,9 @@ int tq_moe_forward_static(const uint16_t* x, const uint8_t* packed, const uint16
  * tq_moe_mlp_forward: the arm chosen as in tq_moe_forward (tq_select_arm with
  *   `pin`, the gate's TILE_M from `tile_m`; arm_used (host, may be NULL)
  *   receives it).  Grouped arm: route + tile map, gate|up (per pair; token
- *   rows gathered in the kernel, or by tq_gather_rows above
- *   TQ_GATHER_MAX_TILE_M), SwiGLU, down (combined per token with the router
+ *   rows gathered in the kernel, or, above TQ_GATHER_MAX_TILE_M, copied into
+ *   pair-sorted order in token order through the sort's inverse, as in
+ *   tq_moe_forward), SwiGLU, down (combined per token with the router
  *   weights).  GEMV arm:
  *   gate|up by per-pair GEMVs, SwiGLU, down by per-pair GEMVs on h combined
  *   per token.  Output bf16 y [n][H].  H % 128 == 0, I % 64 == 0 (and

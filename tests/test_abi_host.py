@@ -115,12 +115,13 @@ def test_host_functions_reject_invalid_arguments(tq):
     cap = tq.tq_tile_map_capacity(16, 2, 8, 16)
     assert tq.tq_moe_workspace_size(16, 2, 8, 256, 128, 16) == (
         a256(8 * 4) + a256(9 * 4) + a256(32 * 4) + a256(3 * cap * 4) + a256(4) + a256(16 * 128 * 4))
-    # above the in-kernel gather's m-tile, the pair-sorted activations too
+    # above the in-kernel gather's m-tile, the pair-sorted activations and the
+    # sort's inverse (one slot per pair) too
     T = tq.GATHER_MAX_TILE_M + 1
     cap = tq.tq_tile_map_capacity(16, 2, 8, T)
     assert tq.tq_moe_workspace_size(16, 2, 8, 256, 128, T) == (
         a256(8 * 4) + a256(9 * 4) + a256(32 * 4) + a256(3 * cap * 4) + a256(4) + a256(16 * 128 * 4)
-        + a256(32 * 256 * 2))
+        + a256(32 * 256 * 2) + a256(32 * 4))
 
 
 def test_device_calls_reject_bad_arguments_before_any_device_work(tq):

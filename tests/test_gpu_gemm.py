@@ -278,6 +278,30 @@ def test_moe_forward_dirty_workspace(pin, tile_m):
         assert normwise(y.float().cpu().numpy(), ref) <= TOL
 
 
+@pytest.mark.parametrize("tile_m,pin", [(16, tq.ARM_GROUPED), (64, tq.ARM_GROUPED), (16, tq.ARM_GEMV)])
+def test_moe_forward_out_of_range_expert(tile_m, pin):
+    """One pair routed to expert E (out of range): the call reports
+    TQ_ERR_INVALID_ARG in the device error word and drops that pair (at m-tile
+    64 its slot in the sort's inverse is -1 and the token-order copy skips it);
+    every output equals the product over the remaining pairs."""
+    prob = moe_inputs.make_custom(8, 2, 40, 256, 128, 12, seed=4040)
+    ids = prob.topk_ids.copy()
+    ids[5, 1] = 8
+    d = to_device(prob)
+    d["ids"] = torch.from_numpy(ids).cuda()
+    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=tile_m, pin=pin)
+    torch.cuda.synchronize()
+    assert arm == pin
+    code, _ = tq.tq_device_error()
+    assert code == -1
+    w = prob.topk_w.copy()
+    w[5, 1] = 0.0
+    keep = ids.copy()
+    keep[5, 1] = 0
+    ref = O.moe_forward(prob.x_bits, keep, w, prob.packed, prob.lut_bits, prob.shape.L)
+    assert normwise(y.float().cpu().numpy(), ref) <= TOL
+
+
 def test_moe_forward_gemv_ragged_output():
     """The GEMV arm of the whole product takes any N: 7 tokens x 130 rows is
     an odd accumulator length, cleared and combined through the scalar head

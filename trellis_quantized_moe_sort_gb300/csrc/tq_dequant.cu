@@ -241,9 +241,10 @@ int tq_moe_forward_dequant(const uint16_t* x, const uint8_t* packed, const uint1
   const MoeScratch ws = carve_moe_scratch(workspace, n, top_k, E, K, N, cap, tile_m);
   uint16_t* w_dense = reinterpret_cast<uint16_t*>(ws.end);   // [E][N][K]; slot e = expert e
   if ((rc = launch_route_tile_map(topk_ids, P, E, tile_m, ws.counts, ws.offsets, ws.sorted_pairs, ws.tiles,
-                                  ws.num_tiles, cap, err, s, ws.y32, static_cast<int64_t>(n) * N)) != TQ_OK)
+                                  ws.num_tiles, cap, err, s, ws.y32, static_cast<int64_t>(n) * N, ws.slot_of)) !=
+      TQ_OK)
     return rc;
-  if (ws.x_sorted && (rc = launch_gather(x, ws.sorted_pairs, P, top_k, K, ws.x_sorted, err, s)) != TQ_OK) return rc;
+  if (ws.x_sorted && (rc = launch_gather_tokens(x, ws.slot_of, n, top_k, K, ws.x_sorted, s)) != TQ_OK) return rc;
   // Materialize every woken expert (experts no pair routes to are skipped).
   if ((rc = launch_dequant(packed, lut, L, nullptr, ws.counts, E, E, N, K, w_dense, err, s)) != TQ_OK) return rc;
   if ((rc = launch_grouped(ws.x_sorted ? ws.x_sorted : x, nullptr, nullptr, 2, ws.sorted_pairs, topk_w, ws.tiles,

@@ -204,8 +204,10 @@ MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K
   m.num_tiles = reinterpret_cast<int32_t*>(w);     w += align256(sizeof(int32_t));
   m.y32 = reinterpret_cast<float*>(w);             w += align256(sizeof(float) * static_cast<size_t>(n) * N);
   m.x_sorted = nullptr;
+  m.slot_of = nullptr;
   if (!gathers_in_kernel(kernel_tile_m)) {
     m.x_sorted = reinterpret_cast<uint16_t*>(w);   w += align256(sizeof(uint16_t) * P * K);
+    m.slot_of = reinterpret_cast<int32_t*>(w);     w += align256(sizeof(int32_t) * std::max<size_t>(P, 1));
   }
   m.end = w;
   return m;
@@ -474,7 +476,10 @@ size_t tq_moe_workspace_size(int64_t n, int top_k, int E, int K, int N, int tile
   b += align256(sizeof(int32_t) * 3 * std::max<int64_t>(cap, 1));   // tiles
   b += align256(sizeof(int32_t));                                   // num_tiles
   b += align256(sizeof(float) * static_cast<size_t>(n) * N);        // y32
-  if (!gathers_in_kernel(kt)) b += align256(sizeof(uint16_t) * P * K);   // pair-sorted activations
+  if (!gathers_in_kernel(kt)) {
+    b += align256(sizeof(uint16_t) * P * K);                        // pair-sorted activations
+    b += align256(sizeof(int32_t) * std::max<size_t>(P, 1));        // pair -> sorted slot
+  }
   return b;
 }
 
@@ -517,10 +522,10 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
     // m-tiles the pair-sorted copy of x; then the grouped kernel as a
     // programmatic dependent (its prologue overlaps the previous launch's tail)
     rc = launch_route_tile_map(topk_ids, static_cast<int>(P), E, tile_m, counts, offsets, sorted_pairs, tiles,
-                               num_tiles, cap, err, s, y32, static_cast<int64_t>(n) * N);
+                               num_tiles, cap, err, s, y32, static_cast<int64_t>(n) * N, ws.slot_of);
     if (rc != TQ_OK) return rc;
     if (ws.x_sorted) {
-      rc = launch_gather(x, sorted_pairs, static_cast<int>(P), top_k, K, ws.x_sorted, err, s);
+      rc = launch_gather_tokens(x, ws.slot_of, n, top_k, K, ws.x_sorted, s);
       if (rc != TQ_OK) return rc;
     }
     rc = launch_grouped(ws.x_sorted ? ws.x_sorted : x, packed, lut, L, sorted_pairs, topk_w, tiles, num_tiles, cap,

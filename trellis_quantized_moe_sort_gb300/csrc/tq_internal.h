@@ -65,9 +65,16 @@ int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top
 // Route and tile map in one launch, also clearing y32[0 .. y32_count) (in
 // extra blocks of the same launch, or by a separate memset when y32 is not
 // 16-byte aligned or y32_count % 4 != 0).
+// With slot_of (device, [P]) the sort also writes its inverse: slot_of[p] =
+// the sorted slot of pair p, -1 for a pair whose expert is out of range.
 int launch_route_tile_map(const int32_t* topk_ids, int P, int E, int tile_m, int32_t* counts, int32_t* offsets,
                           int32_t* sorted_pairs, int32_t* tiles, int32_t* num_tiles, int64_t cap, int* err,
-                          cudaStream_t s, float* y32 = nullptr, int64_t y32_count = 0);
+                          cudaStream_t s, float* y32 = nullptr, int64_t y32_count = 0,
+                          int32_t* slot_of = nullptr);
+// x_sorted[slot_of[t * top_k + j]] = x[t]: the pair-sorted copy written in
+// token order (each row of x read once); slot -1 is skipped.
+int launch_gather_tokens(const uint16_t* x, const int32_t* slot_of, int64_t n, int top_k, int K, uint16_t* x_sorted,
+                         cudaStream_t s);
 // x: token rows [n][K], gathered by sorted pair inside the kernel; or, with
 // x_pair_sorted, the pair-sorted rows [n*top_k][K] (row = sorted slot).
 int launch_grouped(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
@@ -99,6 +106,7 @@ struct MoeScratch {
   int32_t* num_tiles;
   float* y32;
   uint16_t* x_sorted;   // nullptr when the kernel gathers
+  int32_t* slot_of;     // pair -> sorted slot, with x_sorted
   uint8_t* end;
 };
 MoeScratch carve_moe_scratch(void* workspace, int64_t n, int top_k, int E, int K, int N, int64_t cap,

@@ -109,7 +109,10 @@ size_t tq_moe_mlp_workspace_size(int64_t n, int top_k, int E, int H, int I, int 
   b += align256(sizeof(int32_t) * std::max<size_t>(P, 1));         // sorted pairs
   b += align256(sizeof(int32_t) * 3 * std::max<int64_t>(cap, 1));  // tiles
   b += align256(sizeof(int32_t));                                  // num_tiles
-  if (!gathers_in_kernel(kt)) b += align256(sizeof(uint16_t) * P * H);   // x, pair-sorted
+  if (!gathers_in_kernel(kt)) {
+    b += align256(sizeof(uint16_t) * P * H);                       // x, pair-sorted
+    b += align256(sizeof(int32_t) * std::max<size_t>(P, 1));       // pair -> sorted slot
+  }
   b += align256(sizeof(float) * P * 2 * I);                        // gate|up per pair
   b += align256(sizeof(uint16_t) * P * I);                         // h per pair
   b += align256(sizeof(float) * static_cast<size_t>(n) * H);       // y32
@@ -155,8 +158,10 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
   int32_t* tiles = reinterpret_cast<int32_t*>(w);       w += align256(sizeof(int32_t) * 3 * cap);
   int32_t* num_tiles = reinterpret_cast<int32_t*>(w);   w += align256(sizeof(int32_t));
   uint16_t* x_sorted = nullptr;   // large m-tiles: the gate|up input in pair-sorted order
+  int32_t* slot_of = nullptr;     // and the sort's inverse, to write it in token order
   if (!gathers_in_kernel(tile_m)) {
     x_sorted = reinterpret_cast<uint16_t*>(w);          w += align256(sizeof(uint16_t) * P * H);
+    slot_of = reinterpret_cast<int32_t*>(w);            w += align256(sizeof(int32_t) * std::max<size_t>(P, 1));
   }
   float* gate_up = reinterpret_cast<float*>(w);         w += align256(sizeof(float) * P * 2 * I);
   uint16_t* h = reinterpret_cast<uint16_t*>(w);         w += align256(sizeof(uint16_t) * P * I);
@@ -180,8 +185,8 @@ int tq_moe_mlp_forward(const uint16_t* x, const uint8_t* packed_gu, const uint16
   // gathered by the kernel, or copied into pair-sorted order first for large
   // m-tiles), SwiGLU, down reading h in sorted order, combine
   rc = launch_route_tile_map(topk_ids, static_cast<int>(P), E, tile_m, counts, offsets, sorted_pairs, tiles,
-                             num_tiles, cap, err, s, y32, static_cast<int64_t>(n) * H);
-  if (rc == TQ_OK && x_sorted) rc = launch_gather(x, sorted_pairs, static_cast<int>(P), top_k, H, x_sorted, err, s);
+                             num_tiles, cap, err, s, y32, static_cast<int64_t>(n) * H, slot_of);
+  if (rc == TQ_OK && x_sorted) rc = launch_gather_tokens(x, slot_of, n, top_k, H, x_sorted, s);
   if (rc == TQ_OK)
     rc = launch_grouped(x_sorted ? x_sorted : x, packed_gu, lut_gu, L, sorted_pairs, nullptr, tiles, num_tiles, cap,
                         n, top_k, E, H, 2 * I, tile_m, gate_up, err, s, /*pair_out=*/1, nullptr, true,

@@ -67,7 +67,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total) {
 __device__ __forceinline__ void route_chunk(const int32_t* __restrict__ ids, int P, int E, int sorters,
                                             int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                             int32_t* __restrict__ sorted_pairs, int* err, int* first,
-                                            int* count) {
+                                            int* count, int32_t* __restrict__ slot_of = nullptr) {
   // [kWarps][E] per-warp count, then per-warp base; [E] totals; [E] pairs before the chunk
   extern __shared__ int32_t wcnt[];
   int32_t* tot = wcnt + kWarps * E;
@@ -179,6 +179,8 @@ __device__ __forceinline__ void route_chunk(const int32_t* __restrict__ ids, int
         sorted_pairs[slot] = static_cast<int32_t>(p);   // p < end <= P < 2^31
         if (lane == __ffs(peers) - 1) mine[ex] += __popc(peers);
       }
+      // the inverse (pair -> sorted slot; -1 for a pair whose expert is out of range)
+      if (slot_of && p < end) slot_of[p] = ex >= 0 ? slot : -1;
       __syncwarp();
     }
   }
@@ -241,7 +243,7 @@ route_tile_map_kernel(const int32_t* __restrict__ ids, int P, int E, int sorters
                       int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                       int32_t* __restrict__ sorted_pairs, int32_t* __restrict__ tiles,
                       int32_t* __restrict__ num_tiles, long long cap, int* err, float4* __restrict__ zero4,
-                      long long zero_n4) {
+                      long long zero_n4, int32_t* __restrict__ slot_of) {
   pdl_wait();
   pdl_trigger();
   if (static_cast<int>(blockIdx.x) >= sorters) {
@@ -252,7 +254,7 @@ route_tile_map_kernel(const int32_t* __restrict__ ids, int P, int E, int sorters
     return;
   }
   int first, count;
-  route_chunk(ids, P, E, sorters, counts, offsets, sorted_pairs, err, &first, &count);
+  route_chunk(ids, P, E, sorters, counts, offsets, sorted_pairs, err, &first, &count, slot_of);
   if (blockIdx.x == 0) tile_map_block(E, first, count, tile_m, tiles, num_tiles, cap, err);
 }
 
@@ -326,6 +328,43 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* _
       for (int j = 0; j < kUnroll; ++j) {
         const int v = v0 + 32 * j + lane;
         if (v < row_vecs) __stcs(dst + v, t[j]);
+      }
+    }
+  }
+}
+
+// The same copy in token order: x_sorted[slot_of[t * top_k + j]] = x[t] for
+// every j.  One warp per token reads the row once (eight 16-byte loads per
+// lane in flight) and stores it into the sorted slots of the token's pairs;
+// slot -1 (a pair whose expert is out of range, reported by the route) is
+// skipped.  Read in sorted order instead, a row is fetched top_k times, far
+// apart, and the streaming writes push it out of L2 in between.
+__global__ void gather_tokens_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ slot_of, int n,
+                                     int top_k, int row_vecs, uint4* __restrict__ x_sorted) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int kUnroll = 8;
+  const int lane = threadIdx.x & 31;
+  const long long warp = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long t = warp; t < n; t += nwarps) {
+    const uint4* src = x + static_cast<size_t>(t) * row_vecs;
+    for (int v0 = 0; v0 < row_vecs; v0 += 32 * kUnroll) {
+      uint4 q[kUnroll];
+#pragma unroll
+      for (int i = 0; i < kUnroll; ++i) {
+        const int v = v0 + 32 * i + lane;
+        q[i] = v < row_vecs ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      for (int j = 0; j < top_k; ++j) {
+        const int slot = __ldg(slot_of + t * top_k + j);
+        if (slot < 0) continue;
+        uint4* dst = x_sorted + static_cast<size_t>(slot) * row_vecs;
+#pragma unroll
+        for (int i = 0; i < kUnroll; ++i) {
+          const int v = v0 + 32 * i + lane;
+          if (v < row_vecs) __stcs(dst + v, q[i]);
+        }
       }
     }
   }
@@ -419,6 +458,19 @@ int launch_gather(const uint16_t* x, const int32_t* sorted_pairs, int P, int top
   return st;
 }
 
+int launch_gather_tokens(const uint16_t* x, const int32_t* slot_of, int64_t n, int top_k, int K, uint16_t* x_sorted,
+                         cudaStream_t s) {
+  if (n == 0) return TQ_OK;
+  const int row_vecs = K / 8;
+  const int threads = 256;   // 8 warps, one token each per pass
+  const int blocks = static_cast<int>(std::max<long long>(1, std::min<long long>((n + 7) / 8, sm_count() * 8ll)));
+  int st = launch_pdl(gather_tokens_kernel, dim3(blocks), dim3(threads), 0, s, reinterpret_cast<const uint4*>(x),
+                      slot_of, static_cast<int>(n), top_k, row_vecs, reinterpret_cast<uint4*>(x_sorted));
+  if (st == TQ_OK) st = launch_status();
+  if (st == TQ_OK) count_launch(kCntGather);
+  return st;
+}
+
 // Blocks sharing the routing sort: one up to 8192 pairs (a block's own
 // histogram is all it needs), else one per 2048 pairs, at most 64.
 static int route_sorters(int P) {
@@ -430,7 +482,7 @@ static size_t route_smem(int E) { return sizeof(int32_t) * (kWarps + 2) * static
 
 int launch_route_tile_map(const int32_t* topk_ids, int P, int E, int tile_m, int32_t* counts, int32_t* offsets,
                           int32_t* sorted_pairs, int32_t* tiles, int32_t* num_tiles, int64_t cap, int* err,
-                          cudaStream_t s, float* y32, int64_t y32_count) {
+                          cudaStream_t s, float* y32, int64_t y32_count, int32_t* slot_of) {
   const size_t smem = route_smem(E);
   if (cudaFuncSetAttribute(route_tile_map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(route_smem(1024))) != cudaSuccess) {
@@ -455,7 +507,7 @@ int launch_route_tile_map(const int32_t* topk_ids, int P, int E, int tile_m, int
   const int sorters = route_sorters(P);
   int st = launch_pdl(route_tile_map_kernel, dim3(static_cast<unsigned>(sorters + clear_blocks)), dim3(kBlock), smem,
                       s, topk_ids, P, E, sorters, tile_m, counts, offsets, sorted_pairs, tiles, num_tiles,
-                      static_cast<long long>(cap), err, reinterpret_cast<float4*>(y32), z4);
+                      static_cast<long long>(cap), err, reinterpret_cast<float4*>(y32), z4, slot_of);
   if (st == TQ_OK) st = launch_status();
   if (st == TQ_OK) count_launch(kCntRouteTileMap);
   return st;
