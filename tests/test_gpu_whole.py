@@ -207,3 +207,27 @@ def test_moe_forward_in_cuda_graph_native_tile():
         ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L)
         assert normwise(y.float().cpu().numpy(), ref) <= TOL
 
+
+@pytest.mark.parametrize("tile_m", [16, tq.TILE_NATIVE])
+def test_moe_forward_concurrent_streams(tile_m):
+    """Two whole-product calls enqueued on two streams at once, each with its
+    own workspace and output: the library keeps no per-call state of its own
+    (the workspace holds it all), so each result matches its oracle."""
+    probs = [moe_inputs.make_custom(16, 4, 2048, 512, 256, 12, seed=sd) for sd in (811, 812)]
+    s = probs[0].shape
+    devs = [to_device(p) for p in probs]
+    wss = [torch.empty(tq.tq_moe_workspace_size(s.n, s.top_k, s.E, s.K, s.N, tile_m), dtype=torch.uint8,
+                       device="cuda") for _ in probs]
+    ys = [torch.empty((s.n, s.N), dtype=torch.bfloat16, device="cuda") for _ in probs]
+    streams = [torch.cuda.Stream() for _ in probs]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for d, ws, y, st in zip(devs, wss, ys, streams):
+            tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=tile_m, pin=tq.ARM_GROUPED,
+                              workspace=ws, y=y, stream=st)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    for prob, y in zip(probs, ys):
+        ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L)
+        assert normwise(y.float().cpu().numpy(), ref) <= TOL
+
