@@ -185,3 +185,17 @@ def test_native_tile(tq):
     with pytest.raises(tq.TQError):
         tq.tq_native_tile_m(4, 9, 8)
     assert tq.tq_moe_workspace_size(16, 2, 8, 256, 128, 257) == 0
+
+
+def test_device_calls_fail_loudly_without_a_gpu(tq):
+    """No CPU fallback: without a CUDA device every device call raises before
+    the library is asked to do anything (with one, a host tensor is refused
+    as not a CUDA tensor)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    with pytest.raises(RuntimeError, match="needs a CUDA device"):
+        tq.tq_route(torch.zeros((4, 2), dtype=torch.int32), 8)
+    with pytest.raises(RuntimeError, match="needs a CUDA device"):
+        tq.tq_combine(torch.zeros(8, dtype=torch.float32))
+

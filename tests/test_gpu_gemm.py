@@ -346,3 +346,21 @@ def test_moe_forward_measured_policy():
         assert after[ran] == before[ran] + 1
         ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, 12)
         assert normwise(y.float().cpu().numpy(), ref) <= TOL
+
+
+def test_binding_refuses_wrong_dtype_and_strides():
+    """A tensor of the wrong dtype or a non-contiguous view is refused by the
+    binding (TypeError / ValueError naming the argument), never read with the
+    wrong layout."""
+    prob, T = _small("tiny_e8_k2_n16_T16")
+    d = to_device(prob)
+    with pytest.raises(ValueError, match="topk_ids must be a CUDA tensor"):
+        tq.tq_route(d["ids"].cpu(), prob.shape.E)
+    with pytest.raises(TypeError, match="topk_ids"):
+        tq.tq_route(d["ids"].long(), prob.shape.E)
+    wide = torch.zeros((prob.shape.n, 2 * prob.shape.K), dtype=torch.int16, device="cuda")
+    with pytest.raises(ValueError, match="must be contiguous"):
+        tq.tq_gemv(wide[:, ::2], d["packed"], d["lut"], d["ids"], d["w"],
+                   torch.zeros((prob.shape.n, prob.shape.N), dtype=torch.float32, device="cuda"))
+    check_no_device_error()
+
