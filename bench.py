@@ -817,6 +817,64 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_step_latency(args):
+    """Latency of one whole decode step through tq_moe_forward (route + tile
+    map clearing y32, [copy,] arm, combine) at the V4 up shape across token
+    counts, under the default selection, the measured policy and the grouped
+    pin, each at the native m-tile: the call captured in a CUDA graph and
+    replayed after an L2 flush (median), clocks sampled."""
+    import torch
+    import trellis_quantized_moe_sort_gb300 as tq
+    from trellis_quantized_moe_sort_gb300 import build as b
+    b.build()
+    torch.cuda.set_device(0)
+    tq.tq_init(0)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    base = moe_inputs.make_problem("v4_decode_n32")
+    packed = _cuda(torch, base.packed)
+    lut = _cuda(torch, base.lut_bits.view(np.int16))
+    names = {tq.ARM_AUTO: "auto", tq.ARM_MEASURED: "measured", tq.ARM_GROUPED: "grouped"}
+    for n in [int(v) for v in args.gate_ns.split(",")]:
+        prob = moe_inputs.make_problem("v4_decode_n32", n=n, with_packed=False)
+        s = prob.shape
+        x, ids, w = _cuda(torch, prob.x_bits.view(np.int16)), _cuda(torch, prob.topk_ids), _cuda(torch, prob.topk_w)
+        clocks = ClockSampler(0)
+        clocks.start()
+        time.sleep(0.3)
+        row = {"n": n, "native_tile_m": tq.tq_native_tile_m(n, s.top_k, s.E)}
+        for pin in (tq.ARM_AUTO, tq.ARM_MEASURED, tq.ARM_GROUPED):
+            ws = torch.empty(max(256, tq.tq_moe_workspace_size(n, s.top_k, s.E, s.K, s.N, tq.TILE_NATIVE)),
+                             dtype=torch.uint8, device="cuda")
+            y = torch.empty((n, s.N), dtype=torch.bfloat16, device="cuda")
+            stream = torch.cuda.Stream()
+            call = lambda: tq.tq_moe_forward(x, packed, lut, ids, w, tile_m=tq.TILE_NATIVE, pin=pin, workspace=ws,
+                                             y=y)
+            with torch.cuda.stream(stream):
+                _, arm = call()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                call()
+            ts = []
+            for _ in range(args.steps):
+                flush.zero_()
+                torch.cuda.synchronize()
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b_.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b_) * 1e3)
+            us = float(np.median(ts))
+            row[names[pin]] = {"arm": {1: "gemv", 2: "grouped"}[arm], "us_per_step": round(us, 1),
+                               "tokens_per_s": round(n / (us * 1e-6), 1)}
+        row["clocks"] = clocks.stop()
+        code, where = tq.tq_device_error()
+        if code:
+            raise RuntimeError(f"device error {code} at {where} (n={n})")
+        print(json.dumps(row), flush=True)
+
+
 def run_gate_study(args):
     """GB300 gate study: both arms of the routed-expert product (grouped GEMM
     at TILE_M 16 and 128, per-pair GEMV) across token counts at the
@@ -998,6 +1056,8 @@ def main(argv=None):
                     help="add the dequantize-materialize comparator (dense bf16 experts + the same grouped GEMM) to --sweep")
     ap.add_argument("--gate-study", action="store_true", help="both arms across token counts (V4 up shape)")
     ap.add_argument("--mlp-sweep", action="store_true", help="whole SwiGLU expert MLP per workload")
+    ap.add_argument("--step-latency", action="store_true",
+                    help="whole decode-step latency through tq_moe_forward across token counts (V4 up shape)")
     ap.add_argument("--gate-ns", default="1,2,4,8,9,16,32,64,128,256,512,682,683,1024")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes (read+write) per grouped launch, if captured for the current kernel source")
@@ -1023,6 +1083,9 @@ def main(argv=None):
         return
     if args.mlp_sweep:
         run_mlp_sweep(args)
+        return
+    if args.step_latency:
+        run_step_latency(args)
         return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
