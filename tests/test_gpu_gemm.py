@@ -80,6 +80,28 @@ def test_grouped_small_all_outputs(name, lay):
     assert err <= TOL, err
 
 
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_moe_forward_gemv_arm_small_all_outputs(name):
+    """The whole product pinned to the GEMV arm (one launch: each warp sums a
+    token's top_k pairs in registers and rounds once to bf16) on every small
+    problem, all outputs: each within half a bf16 ulp of the oracle's value
+    (round to nearest) plus the fp32 accumulation's slack."""
+    prob, _ = _small(name)
+    d = to_device(prob)
+    before = tq.tq_launch_counts()
+    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=16, pin=tq.ARM_GEMV)
+    check_no_device_error()
+    after = tq.tq_launch_counts()
+    assert arm == tq.ARM_GEMV
+    assert after["gemv"] == before["gemv"] + 1
+    assert {k: after[k] - before[k] for k in after if k != "gemv"} == {k: 0 for k in after if k != "gemv"}
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, prob.shape.L)
+    got = y.float().cpu().numpy().astype(np.float64)
+    bound = np.abs(ref) * 2.0 ** -8 + 1e-5 * np.abs(ref).max()
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), (int(bad.sum()), np.argwhere(bad)[:4].tolist())
+
+
 # Expert sizes whose m-tiles at TILE_M 256 run through every transition of the
 # accumulator slots (m-tiles above 128 pairs take both 128-column slots, the
 # others one, alternating): 296 -> 256 + 40 (big -> small), 40 -> 200 (small ->
@@ -245,13 +267,16 @@ def test_moe_forward_gate_and_arms():
         other = "gemv" if arm == 2 else "grouped"
         assert after[ran] == before[ran] + 1 and after[other] == before[other]
         # the grouped arm: one routing launch (clearing y32), the kernel gathers
-        # activations itself; the GEMV arm: a clear launch before the GEMV
-        assert after["gather"] == before["gather"]
+        # activations itself, one combine; the GEMV arm: the GEMV alone (it
+        # sums each token's pairs and writes bf16 y, so nothing to clear or
+        # combine)
+        assert after["gather"] == before["gather"] and after["clear"] == before["clear"]
         if arm == 2:
             assert after["route_tile_map"] == before["route_tile_map"] + 1
-            assert after["clear"] == before["clear"]
+            assert after["combine"] == before["combine"] + 1
         else:
-            assert after["clear"] == before["clear"] + 1
+            assert after["route_tile_map"] == before["route_tile_map"]
+            assert after["combine"] == before["combine"]
         ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, 12)
         got = y.float().cpu().numpy()
         assert normwise(got, ref) <= TOL
@@ -261,8 +286,9 @@ def test_moe_forward_gate_and_arms():
 @pytest.mark.parametrize("tile_m", [16, 64])
 def test_moe_forward_dirty_workspace(pin, tile_m):
     """A workspace full of NaN bit patterns: every call clears what must start
-    at zero itself (the accumulator, in the routing launch or by the clear
-    kernel), so the result matches the oracle on every call."""
+    at zero itself (the grouped arm's accumulator, in the routing launch; the
+    GEMV arm reads no workspace), so the result matches the oracle on every
+    call."""
     prob = moe_inputs.make_custom(8, 2, 40, 256, 256, 12, seed=55)
     d = to_device(prob)
     s = prob.shape
@@ -283,12 +309,15 @@ def test_moe_forward_out_of_range_expert(tile_m, pin):
     """One pair routed to expert E (out of range): the call reports
     TQ_ERR_INVALID_ARG in the device error word and drops that pair (at m-tile
     64 its slot in the sort's inverse is -1 and the token-order copy skips it);
-    every output equals the product over the remaining pairs."""
+    every output equals the product over the remaining pairs.  The dropped
+    pair's router weight is NaN: dropping means it is never multiplied in."""
     prob = moe_inputs.make_custom(8, 2, 40, 256, 128, 12, seed=4040)
     ids = prob.topk_ids.copy()
     ids[5, 1] = 8
     d = to_device(prob)
     d["ids"] = torch.from_numpy(ids).cuda()
+    d["w"] = d["w"].clone()
+    d["w"][5, 1] = float("nan")
     y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=tile_m, pin=pin)
     torch.cuda.synchronize()
     assert arm == pin
@@ -303,9 +332,9 @@ def test_moe_forward_out_of_range_expert(tile_m, pin):
 
 
 def test_moe_forward_gemv_ragged_output():
-    """The GEMV arm of the whole product takes any N: 7 tokens x 130 rows is
-    an odd accumulator length, cleared and combined through the scalar head
-    and tail paths, from a NaN-filled workspace."""
+    """The GEMV arm of the whole product takes any N: 7 tokens x 130 rows (an
+    odd output length, so the warps' ranges of (token, row) items start and
+    end at odd rows), with a NaN-filled workspace that the arm never reads."""
     prob = moe_inputs.make_custom(8, 2, 7, 256, 130, 12, seed=61)
     d = to_device(prob)
     s = prob.shape

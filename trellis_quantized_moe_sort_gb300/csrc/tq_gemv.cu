@@ -8,7 +8,11 @@
 //
 // GB300 design: one CTA per SM holds the fp16 LUT (and, for small batches,
 // every token's activations) in shared memory.  A warp takes a contiguous
-// range of (pair, weight row) items.  It keeps the current token's
+// range of (pair, weight row) items, or, when the output is the per-token
+// bf16 product itself, of (token, weight row) items whose top_k pairs it
+// walks in order, summing w_j times each pair's partial dot product in
+// registers and writing the rounded sum once (no fp32 accumulator to clear,
+// no atomics, no separate combine launch).  It keeps the current token's
 // activations in registers (lane l holds the 64-element chunks l, l+32, ...
 // of x[t]) and, for each row, loads the row's packed bytes with coalesced
 // 16-byte loads (lane l takes bytes [16c, 16c+16) of chunk c) one row ahead,
@@ -16,6 +20,7 @@
 // from lane 31 of the previous pass, zero at the row start), decodes its 64
 // symbols by window identity, multiplies in fp32 (fp16 weights widened
 // exactly) and reduces the row over the warp with xor shuffles.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -37,7 +42,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
             const uint16_t* __restrict__ lut, const int32_t* __restrict__ topk_ids,
             const float* __restrict__ topk_w, int P, int top_k, int E, int K, int N, int x_in_smem,
-            int pair_in, int pair_out, int early_prologue, float* __restrict__ y32, int* err, int bar_off) {
+            int pair_in, int pair_out, int early_prologue, float* __restrict__ y32, uint16_t* __restrict__ y_tok,
+            int* err, int bar_off) {
   extern __shared__ __align__(16) uint16_t lut_s[];
   constexpr int kEntries = 1 << L;
   constexpr int kLutBytes = (kEntries * 2 + 15) & ~15;
@@ -53,9 +59,11 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
   const long long nwarps = static_cast<long long>(gridDim.x) * warps_per_block;
   const int nchunks = K / kChunkSyms;
   const size_t row_bytes = static_cast<size_t>(K / 4);
-  // This warp's contiguous range of (pair, row) items: consecutive rows of
-  // one pair share the token's activations.
-  const long long items = static_cast<long long>(P) * N;
+  // This warp's contiguous range of items: (pair, row), consecutive rows of
+  // one pair sharing the token's activations; or, with y_tok, (token, row),
+  // each walked as its top_k (pair, row) steps.
+  const bool tok_out = y_tok != nullptr;
+  const long long items = static_cast<long long>(tok_out ? P / top_k : P) * N;
   const long long i0 = items * gwarp / nwarps, i1 = items * (gwarp + 1) / nwarps;
 
   // packed bytes of item `it` (zeros for a bad expert id, reported once per pair)
@@ -75,7 +83,24 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
   if (i0 < i1) {
     p0 = static_cast<int>(i0 / N);
     r0 = static_cast<int>(i0 - static_cast<long long>(p0) * N);
+    if (tok_out) p0 *= top_k;   // the token's first pair
   }
+  // the (pair, row) step after (p, r)
+  auto next = [&](int& p, int& r) {
+    if (tok_out) {
+      if (++p % top_k == 0) {   // past the token's last pair: next row, same token
+        p -= top_k;
+        if (++r == N) {
+          r = 0;
+          p += top_k;
+        }
+      }
+    } else if (++r == N) {
+      r = 0;
+      ++p;
+    }
+  };
+  const long long steps = (i1 - i0) * (tok_out ? top_k : 1);
   // The first row's bytes are in flight while the tables are staged.
   uint4 qa[CPL], qb[CPL];
   if (i0 < i1) load_row(p0, r0, qa);
@@ -121,18 +146,22 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
   if (early_prologue) pdl_wait();
   pdl_trigger();
 
-  int cur_pair = -1, tok = 0;
+  int cur_pair = -1, cur_tok = -1;
   float wt = 0.f;
   bool pair_ok = false;
   uint32_t xr[CPL][32];
-  auto process = [&](bool first_item, int pair, int r, const uint4 (&qv)[CPL]) {
+  // this lane's share of pair . row (fp32, not yet reduced over the warp)
+  auto process = [&](bool first_item, int pair, int r, const uint4 (&qv)[CPL]) -> float {
     if (pair != cur_pair) {
       cur_pair = pair;
-      tok = pair_in ? pair : pair / top_k;   // the row of x this pair multiplies
       const int e = __ldg(topk_ids + pair);
       pair_ok = e >= 0 && e < E;
       if (!pair_ok && lane == 0 && (r == 0 || first_item)) record_error(err, TQ_ERR_INVALID_ARG, kWhereRoute);
       wt = pair_out ? 1.f : __ldg(topk_w + pair);   // per-pair outputs carry no router weight
+    }
+    const int tok = pair_in ? pair : pair / top_k;   // the row of x this pair multiplies
+    if (tok != cur_tok) {
+      cur_tok = tok;
       // activations of this token: chunk c = lane + 32 i, 64 bf16 = 32 words
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
@@ -156,7 +185,7 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
         }
       }
     }
-    if (!pair_ok) return;
+    if (!pair_ok) return 0.f;
     float acc = 0.f;
     uint32_t carry = 0u;  // last word of chunk (32 i - 1), held by lane 31
 #pragma unroll
@@ -185,42 +214,54 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
         }
       }
     }
+    return acc;
+  };
+  // fold one (pair, row) step into the output
+  float item_acc = 0.f;   // tok_out: this lane's share of sum_j w_j (pair_j . row)
+  // (a pair with an out-of-range expert id adds nothing and writes nothing)
+  auto finish = [&](int pair, int r, float acc) {
+    if (tok_out) {
+      if (pair_ok) item_acc = fmaf(wt, acc, item_acc);
+      if ((pair + 1) % top_k != 0) return;   // more pairs of this token to come
+      acc = item_acc;
+      item_acc = 0.f;
+    } else if (!pair_ok) {
+      return;
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) {
-      if (pair_out)
+      if (tok_out) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(acc);
+        y_tok[static_cast<size_t>(pair / top_k) * N + r] = __bfloat16_as_ushort(b);   // one writer per (token, row)
+      } else if (pair_out) {
         y32[static_cast<size_t>(pair) * N + r] = acc;   // one writer per (pair, row)
-      else
+      } else {
         atomicAdd(y32 + static_cast<size_t>(pair / top_k) * N + r, acc * wt);
+      }
     }
   };
 
   // The next row's bytes are in flight while this row decodes (two register
   // sets used in turn, so no copy waits for a load).
   int pa = p0, ra = r0;
-  for (long long it = i0; it < i1; it += 2) {
-    int pb = pa, rb = ra + 1;
-    if (rb == N) {
-      rb = 0;
-      ++pb;
-    }
-    if (it + 1 < i1) load_row(pb, rb, qb);
-    process(it == i0, pa, ra, qa);
-    if (it + 1 >= i1) break;
+  for (long long it = 0; it < steps; it += 2) {
+    int pb = pa, rb = ra;
+    next(pb, rb);
+    if (it + 1 < steps) load_row(pb, rb, qb);
+    finish(pa, ra, process(it == 0, pa, ra, qa));
+    if (it + 1 >= steps) break;
     pa = pb;
-    ra = rb + 1;
-    if (ra == N) {
-      ra = 0;
-      ++pa;
-    }
-    if (it + 2 < i1) load_row(pa, ra, qa);
-    process(false, pb, rb, qb);
+    ra = rb;
+    next(pa, ra);
+    if (it + 2 < steps) load_row(pa, ra, qa);
+    finish(pb, rb, process(false, pb, rb, qb));
   }
 }
 
 template <int L, int CPL>
 int launch_one(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, const int32_t* ids,
-               const float* w, int P, int top_k, int E, int K, int N, float* y32, int* err,
+               const float* w, int P, int top_k, int E, int K, int N, float* y32, uint16_t* y_tok, int* err,
                cudaStream_t s, int pair_in, int pair_out, int early) {
   constexpr int kThreads = (CPL >= 4) ? 256 : 512;
   auto kfn = gemv_kernel<L, CPL, kThreads>;
@@ -239,38 +280,40 @@ int launch_one(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, co
   const long long items = static_cast<long long>(P) * N;
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(sms, (items + kThreads / 32 - 1) / (kThreads / 32))));
   const int st = launch_pdl(kfn, dim3(grid), dim3(kThreads), smem, s, x, packed, lut, ids, w, P, top_k, E, K, N,
-                            x_in_smem, pair_in, pair_out, early, y32, err, static_cast<int>(bar_off));
+                            x_in_smem, pair_in, pair_out, early, y32, y_tok, err, static_cast<int>(bar_off));
   return st == TQ_OK ? launch_status() : st;
 }
 
 template <int L>
 int launch_L(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, const int32_t* ids,
-             const float* w, int P, int top_k, int E, int K, int N, float* y32, int* err,
+             const float* w, int P, int top_k, int E, int K, int N, float* y32, uint16_t* yt, int* err,
              cudaStream_t s, int pi, int po, int early) {
   const int nchunks = K / kChunkSyms;
-  if (nchunks <= 32) return launch_one<L, 1>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s, pi, po, early);
-  if (nchunks <= 64) return launch_one<L, 2>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s, pi, po, early);
-  return launch_one<L, 4>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, err, s, pi, po, early);
+  if (nchunks <= 32) return launch_one<L, 1>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, yt, err, s, pi, po, early);
+  if (nchunks <= 64) return launch_one<L, 2>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, yt, err, s, pi, po, early);
+  return launch_one<L, 4>(x, packed, lut, ids, w, P, top_k, E, K, N, y32, yt, err, s, pi, po, early);
 }
 
 }  // namespace
 
 int launch_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
                 const int32_t* topk_ids, const float* topk_w, int64_t n, int top_k, int E, int K,
-                int N, float* y32, int* err, cudaStream_t s, int pair_in, int pair_out, bool early_prologue) {
+                int N, float* y32, int* err, cudaStream_t s, int pair_in, int pair_out, bool early_prologue,
+                uint16_t* y_tok) {
   const int P = static_cast<int>(n * top_k);
   if (P == 0) return TQ_OK;
+  if (y_tok && (pair_in || pair_out)) return TQ_ERR_INVALID_ARG;   // per-token output: x per token
   const int early = early_prologue ? 1 : 0;
   int st;
   switch (L) {
-    case 2: st = launch_L<2>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
-    case 4: st = launch_L<4>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
-    case 6: st = launch_L<6>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
-    case 8: st = launch_L<8>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
-    case 10: st = launch_L<10>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
-    case 12: st = launch_L<12>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
-    case 14: st = launch_L<14>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
-    case 16: st = launch_L<16>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, err, s, pair_in, pair_out, early); break;
+    case 2: st = launch_L<2>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, y_tok, err, s, pair_in, pair_out, early); break;
+    case 4: st = launch_L<4>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, y_tok, err, s, pair_in, pair_out, early); break;
+    case 6: st = launch_L<6>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, y_tok, err, s, pair_in, pair_out, early); break;
+    case 8: st = launch_L<8>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, y_tok, err, s, pair_in, pair_out, early); break;
+    case 10: st = launch_L<10>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, y_tok, err, s, pair_in, pair_out, early); break;
+    case 12: st = launch_L<12>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, y_tok, err, s, pair_in, pair_out, early); break;
+    case 14: st = launch_L<14>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, y_tok, err, s, pair_in, pair_out, early); break;
+    case 16: st = launch_L<16>(x, packed, lut, topk_ids, topk_w, P, top_k, E, K, N, y32, y_tok, err, s, pair_in, pair_out, early); break;
     default: return TQ_ERR_INVALID_ARG;
   }
   if (st == TQ_OK) count_launch(kCntGemv);

@@ -542,15 +542,13 @@ int tq_moe_forward(const uint16_t* x, const uint8_t* packed, const uint16_t* lut
                    static_cast<long long>(n), top_k, E, 100.0 * ppw / gate_tile, ppw, gate_tile,
                    static_cast<long long>(tq_grouped_min_tokens(top_k, E, gate_tile)), tile_m);
     });
-  } else {
-    // clear y32, then the GEMV, whose prologue (LUT and activation staging,
-    // first row) overlaps the clear
-    rc = launch_clear(y32, static_cast<int64_t>(n) * N, s);
-    if (rc != TQ_OK) return rc;
-    rc = launch_gemv(x, packed, lut, L, topk_ids, topk_w, n, top_k, E, K, N, y32, err, s, 0, 0, true);
-    if (rc != TQ_OK) return rc;
+    return launch_combine(y32, y, static_cast<int64_t>(n) * N, s);
   }
-  return launch_combine(y32, y, static_cast<int64_t>(n) * N, s);
+  // The GEMV arm in one launch: each warp sums a token's top_k pairs for its
+  // output rows in registers and writes the bf16 product (y32 is not used).
+  // Its predecessor on the stream is the caller's, which may have written
+  // the inputs, so the kernel waits for it before staging anything.
+  return launch_gemv(x, packed, lut, L, topk_ids, topk_w, n, top_k, E, K, N, nullptr, err, s, 0, 0, false, y);
 }
 
 int tq_device_error(int* code, int* where) {

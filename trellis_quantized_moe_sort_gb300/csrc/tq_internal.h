@@ -120,14 +120,16 @@ bool resolve_tile(int64_t n, int top_k, int E, int tile_m, int* kernel_tile, int
 int launch_swiglu(const float* gate_up, int64_t P, int I, uint16_t* h, cudaStream_t s);
 // pair_in: x holds one row per pair (x[pair]) instead of per token;
 // pair_out: out[pair][row] = the row's dot product (plain store, no router
-// weight) instead of y32[token][row] += w * dot.  Launched as a programmatic
-// dependent of the previous kernel; early_prologue: that kernel writes none
-// of x, topk_ids, the LUT or packed, so the kernel stages them (and loads its
-// first row) before waiting for it.
+// weight) instead of y32[token][row] += w * dot; y_tok (x per token, neither
+// pair_in nor pair_out): y_tok[token][row] = bf16(sum_j w_j dot_j) written
+// once per element, y32 unused.  Launched as a programmatic dependent of the
+// previous kernel; early_prologue: that kernel writes none of x, topk_ids,
+// the LUT or packed, so the kernel stages them (and loads its first row)
+// before waiting for it.
 int launch_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L,
                 const int32_t* topk_ids, const float* topk_w, int64_t n, int top_k, int E, int K,
                 int N, float* y32, int* err, cudaStream_t s, int pair_in = 0, int pair_out = 0,
-                bool early_prologue = false);
+                bool early_prologue = false, uint16_t* y_tok = nullptr);
 // TQ_FORCE_ARM (auto|gemv|grouped|measured) applied to an automatic pin.
 int env_pin(int pin);
 
