@@ -879,7 +879,9 @@ def run_gate_study(args):
     """GB300 gate study: both arms of the routed-expert product (grouped GEMM
     at TILE_M 16 and 128, per-pair GEMV) across token counts at the
     DeepSeek-V4 up shape, each kernel launch timed alone after an L2 flush.
-    The tile-fill predicate's choice (TILE_M 16) is printed beside."""
+    The GEMV is timed twice: tq_gemv (fp32 atomics into y32) and the
+    one-launch arm of tq_moe_forward (bf16 y).  The tile-fill predicate's
+    choice (TILE_M 16) is printed beside."""
     import torch
     import trellis_quantized_moe_sort_gb300 as tq
     from trellis_quantized_moe_sort_gb300 import build as b
@@ -934,6 +936,13 @@ def run_gate_study(args):
                "measured_policy_arm": {1: "gemv", 2: "grouped"}[tq.tq_select_arm(n, s.top_k, s.E, 16,
                                                                                   tq.ARM_MEASURED)]}
         row["gemv_us"] = round(timed(lambda: tq.tq_gemv(x, packed, lut, ids, w, y32)), 1)
+        # the GEMV arm as tq_moe_forward runs it: one launch that sums each
+        # token's pairs in registers and writes bf16 y
+        ws = torch.empty(max(256, tq.tq_moe_workspace_size(n, s.top_k, s.E, s.K, s.N, 16)), dtype=torch.uint8,
+                         device="cuda")
+        y = torch.empty((n, s.N), dtype=torch.bfloat16, device="cuda")
+        row["gemv_forward_us"] = round(timed(lambda: tq.tq_moe_forward(x, packed, lut, ids, w, tile_m=16,
+                                                                         pin=tq.ARM_GEMV, workspace=ws, y=y)), 1)
         for T in (16, 128):
             _, offsets, sp = tq.tq_route(ids, s.E)
             cap = tq.tq_tile_map_capacity(n, s.top_k, s.E, T)
