@@ -80,13 +80,26 @@ def test_grouped_small_all_outputs(name, lay):
     assert err <= TOL, err
 
 
-@pytest.mark.parametrize("name", sorted(SMALL))
+# The GEMV arm's largest K with activations too large to stage beside the
+# LUT (read from global memory, four 64-symbol chunks per lane), with one
+# and with several pairs per token.
+GEMV_EXTRA = {
+    "gemv_K8192_n8_global_x": (2, 1, 8, 8192, 128, 16, 16, "uniform"),
+    "gemv_K8192_n20_k3_global_x": (6, 3, 20, 8192, 256, 14, 16, "uniform"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL) + sorted(GEMV_EXTRA))
 def test_moe_forward_gemv_arm_small_all_outputs(name):
     """The whole product pinned to the GEMV arm (one launch: each warp sums a
     token's top_k pairs in registers and rounds once to bf16) on every small
     problem, all outputs: each within half a bf16 ulp of the oracle's value
     (round to nearest) plus the fp32 accumulation's slack."""
-    prob, _ = _small(name)
+    if name in GEMV_EXTRA:
+        E, k, n, K, N, L, _, routing = GEMV_EXTRA[name]
+        prob = moe_inputs.make_custom(E, k, n, K, N, L, seed=zlib.crc32(name.encode()) % 1000, routing=routing)
+    else:
+        prob, _ = _small(name)
     d = to_device(prob)
     before = tq.tq_launch_counts()
     y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=16, pin=tq.ARM_GEMV)
