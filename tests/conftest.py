@@ -15,5 +15,5 @@ def pytest_configure(config):
 
 def pytest_collection_modifyitems(config, items):
     # GPU tests must fail loudly (not skip) when CUDA is missing on a GPU run;
-    # on a CPU-only run the driver deselects them with -m "not gpu".
+    # a CPU-only run deselects them with -m "not gpu".
     pass
