@@ -72,6 +72,29 @@ def test_gate_and_flip_bitexact(tq):
     assert tq.tq_grouped_min_tokens(6, 256, 16) == 683
 
 
+def test_gate_random_shapes_bitexact(tq):
+    """2000 seeded random routing shapes (E up to 1024, k up to min(E, 16),
+    TILE_M 1..256, n log-uniform up to 50,000 and around each shape's flip):
+    the amortization predicate, the flip, the tile-map capacity, the pairs
+    per woken expert and the arm under each pin agree with the oracle."""
+    rng = np.random.default_rng(20261203)
+    for _ in range(2000):
+        E = int(rng.integers(1, 1025))
+        k = int(rng.integers(1, min(E, 16) + 1))
+        T = int(rng.integers(1, 257))
+        flip = tq.tq_grouped_min_tokens(k, E, T)
+        assert flip == O.grouped_min_tokens(k, E, T), (k, E, T)
+        ns = {int(np.exp(rng.uniform(0.0, np.log(50_000)))), int(rng.integers(0, 10)), flip - 1, flip}
+        for n in sorted(v for v in ns if v >= 0):
+            assert tq.tq_tiles_amortize(n, k, E, T) == O.tiles_amortize(n, k, E, T), (n, k, E, T)
+            assert tq.tq_tile_map_capacity(n, k, E, T) == O.tile_map_capacity(n, k, E, T), (n, k, E, T)
+            got, want = tq.tq_pairs_per_woken_expert(n, k, E), O.pairs_per_woken_expert(n, k, E)
+            assert got == want or (np.isnan(got) and np.isnan(want)), (n, k, E, got, want)
+            for pin, name in ((0, "auto"), (1, "gemv"), (2, "grouped")):
+                arm = tq.tq_select_arm(n, k, E, T, pin)
+                assert {1: "gemv", 2: "grouped"}[arm] == O.dispatch_arm(n, k, E, T, name), (n, k, E, T, name)
+
+
 def _header_crossover():
     """The measured policy's threshold as the header defines it (a library
     tuning value, read from the header rather than restated here)."""
