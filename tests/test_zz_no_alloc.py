@@ -91,6 +91,8 @@ def test_static_matches_workspace_entry_point_two_calls(name, tile_m, pin):
         assert arm == want_arm
         if arm == tq.ARM_GROUPED:
             assert after["gather"] - before["gather"] == (1 if tile_m > tq.GATHER_MAX_TILE_M else 0)
+        else:   # the GEMV arm is one launch: nothing else runs
+            assert {k: after[k] - before[k] for k in after} == {k: int(k == "gemv") for k in after}
         assert _normwise(y, want) <= TOL
         rows = _sample_rows(s.N, 24, seed=11)
         got = y[:, torch.from_numpy(rows).cuda()]
