@@ -66,7 +66,8 @@ gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ packed,
   const long long items = static_cast<long long>(tok_out ? P / top_k : P) * N;
   const long long i0 = items * gwarp / nwarps, i1 = items * (gwarp + 1) / nwarps;
 
-  // packed bytes of item `it` (zeros for a bad expert id, reported once per pair)
+  // packed bytes of row r of the pair's expert (zeros for a bad expert id,
+  // which process() reports)
   auto load_row = [&](int pair, int r, uint4 (&q)[CPL]) {
     const int e = __ldg(topk_ids + pair);
     const bool ok = e >= 0 && e < E;
