@@ -784,6 +784,14 @@ def run_sweep(args):
                          "dense_gemm_weight_GBps": round(ntiles * s.N * s.K * 2 / (gemm_us * 1e-6) / 1e9, 1)}
             else:
                 us = timed(lambda: tq.tq_gemv(d["x"], d["packed"], d["lut"], d["ids"], d["w"], y32))
+                # the same arm as tq_moe_forward runs it: one launch writing bf16 y
+                ws = torch.empty(max(256, tq.tq_moe_workspace_size(s.n, s.top_k, s.E, s.K, s.N, 16)),
+                                 dtype=torch.uint8, device="cuda")
+                y = torch.empty((s.n, s.N), dtype=torch.bfloat16, device="cuda")
+                extra["forward_us"] = round(timed(lambda: tq.tq_moe_forward(
+                    d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=16, pin=tq.ARM_GEMV, workspace=ws,
+                    y=y)), 1)
+                del ws, y
                 ntiles = None
                 staged = s.pairs * s.N * s.K // 4
             code, where = tq.tq_device_error()
