@@ -874,8 +874,16 @@ def run_step_latency(args):
                 torch.cuda.synchronize()
                 ts.append(a.elapsed_time(b_) * 1e3)
             us = float(np.median(ts))
+            # host cost of one eager call (binding + C ABI + launches), the GPU kept busy
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                h0 = time.perf_counter()
+                for _ in range(20):
+                    call()
+                host_us = (time.perf_counter() - h0) / 20 * 1e6
+            stream.synchronize()
             row[names[pin]] = {"arm": {1: "gemv", 2: "grouped"}[arm], "us_per_step": round(us, 1),
-                               "tokens_per_s": round(n / (us * 1e-6), 1)}
+                               "tokens_per_s": round(n / (us * 1e-6), 1), "host_us_per_call": round(host_us, 1)}
         row["clocks"] = clocks.stop()
         code, where = tq.tq_device_error()
         if code:
