@@ -175,10 +175,12 @@ def _random_configs(count=24, seed=2026):
     return out
 
 
-@pytest.mark.parametrize("cfg", _random_configs(), ids=lambda c: "E{}_k{}_n{}_K{}_N{}_L{}_T{}".format(*c))
+@pytest.mark.parametrize("cfg", _random_configs(count=160), ids=lambda c: "E{}_k{}_n{}_K{}_N{}_L{}_T{}".format(*c))
 def test_random_shapes_all_outputs(cfg):
     """Both arms, and the grouped arm on both activation layouts, on seeded
-    random shapes: every output against the oracle."""
+    random shapes: every output against the oracle; then the whole product
+    on each arm at the shape's m-tile (the GEMV arm's bf16 outputs each within
+    half a bf16 ulp of the oracle plus the fp32 slack)."""
     E, k, n, K, N, L, T = cfg
     prob = moe_inputs.make_custom(E, k, n, K, N, L, seed=zlib.crc32(repr(cfg).encode()) % 1000)
     d = to_device(prob)
@@ -188,6 +190,14 @@ def test_random_shapes_all_outputs(cfg):
         assert normwise(y, ref) <= TOL, (lay, normwise(y, ref))
     y = gemv_y32(prob, d).cpu().numpy()
     assert normwise(y, ref) <= TOL_GEMV
+    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=T, pin=tq.ARM_GROUPED)
+    check_no_device_error()
+    assert arm == tq.ARM_GROUPED and normwise(y.float().cpu().numpy(), ref) <= TOL
+    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=T, pin=tq.ARM_GEMV)
+    check_no_device_error()
+    got = y.float().cpu().numpy().astype(np.float64)
+    bad = np.abs(got - ref) > np.abs(ref) * 2.0 ** -8 + 1e-5 * np.abs(ref).max()
+    assert arm == tq.ARM_GEMV and not bad.any(), (int(bad.sum()), np.argwhere(bad)[:4].tolist())
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
