@@ -230,7 +230,7 @@ def _random_mlp_configs(count=8, seed=77):
     return out
 
 
-@pytest.mark.parametrize("cfg", _random_mlp_configs(),
+@pytest.mark.parametrize("cfg", _random_mlp_configs(count=32),
                          ids=lambda c: "E{}_k{}_n{}_H{}_I{}_L{}_T{}_arm{}".format(*c))
 def test_mlp_random_shapes_all_outputs(cfg):
     """The whole expert MLP on seeded random shapes, every output against the oracle."""

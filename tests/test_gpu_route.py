@@ -215,31 +215,26 @@ def test_prepare_bitexact_against_oracle(name, tile_m):
         np.testing.assert_array_equal(xs[:n * k].cpu().numpy().view(np.uint16), x_bits[s // k])
 
 
-def _random_routings(count=16, seed=404):
-    """Seeded routings: E up to 1024, top_k up to 16, up to 40,000 tokens
-    (up to 640,000 pairs: the sort's largest grid), uniform, Zipf and
-    shuffled-rank Zipf popularity, a random m-tile: (ids, E, tile_m)."""
-    rng = np.random.Generator(np.random.PCG64(seed))
-    out = []
-    for _ in range(count):
-        E = int(rng.integers(1, 1025))
-        k = int(rng.integers(1, min(E, 16) + 1))
-        n = int(rng.choice([0, 1, int(rng.integers(2, 600)), int(rng.integers(600, 40001))],
-                           p=[0.06, 0.06, 0.44, 0.44]))
-        routing = str(rng.choice(["uniform", "zipf", "zipf_perm"]))
-        ids, _ = moe_inputs.draw_routing(rng, n, E, k, routing)
-        out.append((ids.reshape(n, k), E, int(rng.integers(1, 257))))
-    return out
+def _random_routing(i, seed=404):
+    """Seeded routing number i: E up to 1024, top_k up to 16, up to 40,000
+    tokens (up to 640,000 pairs: the sort's largest grid), uniform, Zipf and
+    shuffled-rank Zipf popularity, a random m-tile: (ids, E, tile_m).  Drawn
+    when the test runs, so collecting the tests costs nothing."""
+    rng = np.random.Generator(np.random.PCG64([seed, i]))
+    E = int(rng.integers(1, 1025))
+    k = int(rng.integers(1, min(E, 16) + 1))
+    n = int(rng.choice([0, 1, int(rng.integers(2, 600)), int(rng.integers(600, 40001))],
+                       p=[0.06, 0.06, 0.44, 0.44]))
+    routing = str(rng.choice(["uniform", "zipf", "zipf_perm"]))
+    ids, _ = moe_inputs.draw_routing(rng, n, E, k, routing)
+    return ids.reshape(n, k), E, int(rng.integers(1, 257))
 
 
-RANDOM_ROUTINGS = _random_routings()
-
-
-@pytest.mark.parametrize("i", range(len(RANDOM_ROUTINGS)))
+@pytest.mark.parametrize("i", range(64))
 def test_prepare_random_routings_bitexact(i):
     """The fused route + tile map launch and the gather against the oracle's
     route and tile map, bit for bit, on seeded random routings."""
-    ids, E, tile_m = RANDOM_ROUTINGS[i]
+    ids, E, tile_m = _random_routing(i)
     n, k = ids.shape
     K = 64
     rng = np.random.Generator(np.random.PCG64(1000 + i))

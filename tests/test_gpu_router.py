@@ -63,28 +63,23 @@ def test_route_logits_equals_route_of_oracle_ids():
     assert np.array_equal(sp.cpu().numpy(), s)
 
 
-def _random_router_cases(count=10, seed=909):
-    """Seeded logits: E up to 1024, top_k up to min(E, 32), up to 3000 tokens;
-    half of them rounded to a few values so that exact ties are common."""
-    rng = np.random.Generator(np.random.PCG64(seed))
-    out = []
-    for i in range(count):
-        E = int(rng.integers(1, 1025))
-        k = int(rng.integers(1, min(E, 32) + 1))
-        n = int(rng.integers(1, 3001))
-        logits = rng.standard_normal((n, E)).astype(np.float32)
-        if i % 2:
-            logits = np.round(logits * 2).astype(np.float32)
-        out.append((logits, k))
-    return out
+def _random_router_case(i, seed=909):
+    """Seeded logits number i: E up to 1024, top_k up to min(E, 32), up to
+    3000 tokens; every second case rounded to a few values so that exact ties
+    are common.  Drawn when the test runs."""
+    rng = np.random.Generator(np.random.PCG64([seed, i]))
+    E = int(rng.integers(1, 1025))
+    k = int(rng.integers(1, min(E, 32) + 1))
+    n = int(rng.integers(1, 3001))
+    logits = rng.standard_normal((n, E)).astype(np.float32)
+    if i % 2:
+        logits = np.round(logits * 2).astype(np.float32)
+    return logits, k
 
 
-RANDOM_CASES = _random_router_cases()
-
-
-@pytest.mark.parametrize("i", range(len(RANDOM_CASES)))
+@pytest.mark.parametrize("i", range(40))
 def test_router_topk_random_matches_oracle(i):
-    logits, k = RANDOM_CASES[i]
+    logits, k = _random_router_case(i)
     ids, w = tq.tq_router_topk(torch.from_numpy(logits).cuda(), k)
     check_no_device_error()
     want_ids, want_w = O.router_topk(logits, k)
