@@ -501,13 +501,16 @@ def run_e2e(args, tq, torch, sets, n, k, E, K, N, T):
     def run(steps, first):
         h2d(first)
         for i in range(first, first + steps):
-            if i + 1 < first + steps:
-                h2d(i + 1)   # after step i-1's output copy on the same stream: that buffer set is free
             b = bufs[i % 2]
             compute.wait_event(b["in_ready"])
             tq.tq_moe_forward(b["x"], sets[i % args.weight_sets]["packed"], sets[i % args.weight_sets]["lut"],
                               b["ids"], b["w"], tile_m=T, pin=tq.ARM_GROUPED, workspace=b["ws"], y=b["y"])
             b["done"].record(compute)
+            # step i+1's inputs: issued after step i's call (so the GPU starts
+            # step i first), queued on the copy stream after step i-1's output
+            # copy, which waited for step i-1: that buffer set is free
+            if i + 1 < first + steps:
+                h2d(i + 1)
             copies.wait_event(b["done"])
             with torch.cuda.stream(copies):
                 b["yh"].copy_(b["y"], non_blocking=True)
