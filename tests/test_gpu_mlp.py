@@ -48,6 +48,8 @@ def test_mlp_tiny_all_outputs(tile_m, pin):
     # copy (one gather launch) above the in-kernel gather's m-tile
     gathers = 1 if pin == tq.ARM_GROUPED and tile_m > tq.GATHER_MAX_TILE_M else 0
     assert after["gather"] == before["gather"] + gathers
+    # SwiGLU: one launch between the projections on either arm
+    assert after["swiglu"] == before["swiglu"] + 1
     ref = O.moe_mlp(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed_gu, prob.lut_gu, prob.packed_down,
                     prob.lut_down, prob.L)
     assert normwise(y.float().cpu().numpy(), ref) <= TOL
