@@ -73,6 +73,13 @@ def pin_gate_points():
     assert all(T.dispatch_arm(n, 6, 256, 16) == "grouped" for n in range(683, 1200))
     assert T.dispatch_arm(1, 6, 256, 16, pin="grouped") == "grouped"
     assert T.dispatch_arm(5000, 6, 256, 16, pin="gemv") == "gemv"
+    # the post-merge note's decode floor at its edge: up to 8 tokens the
+    # per-pair GEMV runs even where the tiles amortize (TILE_M 1; and k = E,
+    # where pairs per woken expert = n reaches TILE_M 8 exactly at n = 8);
+    # from 9 tokens the predicate decides
+    for k, E, tm in ((6, 256, 1), (8, 8, 8)):
+        assert T.tiles_amortize(8, k, E, tm)
+        assert [T.dispatch_arm(n, k, E, tm) for n in range(1, 10)] == ["gemv"] * 8 + ["grouped"]
 
 
 def pin_gate_closed_forms():

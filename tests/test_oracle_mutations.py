@@ -2,7 +2,10 @@
 catches each one: off-by-one symbol, wrong state mask, off-by-one seed,
 shift-by-1 (the four mutation classes the arch-specialisation page reports),
 plus reversed window order, dropped router weight, wrong token index, unstable
-route, tile-map off-by-one, '>' for '>=', and a wrong exponent in the fill."""
+route, tile-map off-by-one, '>' for '>=', a wrong exponent in the fill, an
+undersized capacity bound, a late flip, a strict decode floor, the
+with-replacement woken-expert formula, reversed symbol order, an unweighted
+MLP, activations read as fp16, the wrong expert and reversed output rows."""
 import numpy as np
 import pytest
 
@@ -144,7 +147,62 @@ def _mlp_swapped_halves(x_bits, topk_ids, topk_w, packed_gu, lut_gu, packed_down
     return orig["moe_mlp"](x_bits, topk_ids, topk_w, swapped, lut_gu, packed_down, lut_down, L, tokens)
 
 
+def _capacity_too_small(n, top_k, E, tile_m):
+    return max(orig["tile_map_capacity"](n, top_k, E, tile_m) - 1, 0)
+
+
+def _flip_late(top_k, E, tile_m, limit=1 << 26):
+    f = orig["grouped_min_tokens"](top_k, E, tile_m, limit)
+    return f + 1 if f > 0 else f
+
+
+def _dispatch_floor_strict(n, top_k, E, tile_m, pin="auto"):
+    if pin in ("gemv", "grouped"):
+        return pin
+    if n < T.DECODE_REGIME_MAX_TOKENS or not T.tiles_amortize(n, top_k, E, tile_m):
+        return "gemv"
+    return "grouped"
+
+
+def _ppw_with_replacement(n, top_k, E):
+    if n <= 0:
+        return 0.0
+    return n * top_k / (E * (1 - (1 - 1 / E) ** (n * top_k)))
+
+
+def _decode_symbols_reversed(packed_rows, lut_bits, L):
+    lut = orig["lut_values"](lut_bits)
+    c = np.ascontiguousarray(orig["symbols"](packed_rows)[..., ::-1])
+    return lut[orig["states_window"](c, L)]
+
+
+def _mlp_down_unweighted(x_bits, topk_ids, topk_w, *rest, **kw):
+    return orig["moe_mlp"](x_bits, topk_ids, np.ones_like(topk_w), *rest, **kw)
+
+
+def _activations_as_fp16(bits):
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def _forward_expert_off_by_one(x_bits, topk_ids, topk_w, packed, lut_bits, L, rows=None):
+    E = packed.shape[0]
+    return orig["moe_forward"](x_bits, (np.asarray(topk_ids) + 1) % E, topk_w, packed, lut_bits, L, rows)
+
+
+def _forward_rows_reversed(x_bits, topk_ids, topk_w, packed, lut_bits, L, rows=None):
+    return orig["moe_forward"](x_bits, topk_ids, topk_w, np.ascontiguousarray(packed[:, ::-1]), lut_bits, L, rows)
+
+
 MUTATIONS = {
+    "capacity_too_small": ("tile_map_capacity", _capacity_too_small),
+    "flip_one_late": ("grouped_min_tokens", _flip_late),
+    "decode_floor_strict": ("dispatch_arm", _dispatch_floor_strict),
+    "woken_with_replacement": ("pairs_per_woken_expert", _ppw_with_replacement),
+    "symbols_reversed_in_row": ("decode_rows", _decode_symbols_reversed),
+    "mlp_down_unweighted": ("moe_mlp", _mlp_down_unweighted),
+    "activations_as_fp16": ("bf16_bits_to_f64", _activations_as_fp16),
+    "expert_off_by_one": ("moe_forward", _forward_expert_off_by_one),
+    "output_rows_reversed": ("moe_forward", _forward_rows_reversed),
     "mlp_sigmoid_for_silu": ("moe_mlp", _mlp_sigmoid_only),
     "mlp_gate_up_swapped": ("moe_mlp", _mlp_swapped_halves),
     "topk_ties_high": ("router_topk", _topk_ties_high),
