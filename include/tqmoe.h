@@ -309,8 +309,11 @@ int tq_gemv(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, int L
 int tq_combine(const float* y32, uint16_t* y, int64_t count, tq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
- * Whole routed-expert product: zero y32, route, tile map, arm selection
- * (tq_select_arm with `pin`), the selected arm, combine to bf16 y [n][N].
+ * Whole routed-expert product: arm selection (tq_select_arm with `pin`),
+ * then on the grouped arm route + tile map (clearing the fp32 accumulator),
+ * the grouped kernel and the combine to bf16 y [n][N]; on the GEMV arm one
+ * launch that sums each token's top_k pairs in fp32 registers and writes
+ * bf16 y [n][N] directly (the workspace is not touched).
  *
  * workspace (device): caller-owned scratch of at least
  *   tq_moe_workspace_size(n, top_k, E, K, N, tile_m) bytes, 256-byte aligned.
