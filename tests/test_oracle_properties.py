@@ -1,0 +1,167 @@
+"""Property-based checks of the oracle (CPU): hypothesis searches the inputs,
+and each property is fixed by the mathematics or by an independent
+implementation, never by restating the oracle's own formula:
+
+- the window identity equals big-integer bit slicing of the row's stream
+  (page "perf(qtip): arch-specialise the trellis grouped GEMM ...", section
+  "Contiguous-run decode": a state is the window of the last L/2 symbols);
+- a contiguous run seeded by the window identity and stepped by the
+  recurrence reproduces the window identity at every symbol;
+- the tile map covers each expert's slot range in order with 1..TILE_M rows
+  per tile, and no routing of n*k pairs over E experts needs more tiles than
+  the capacity bound (hypothesis picks adversarial expert counts);
+- bf16 round-to-nearest-even agrees with torch's CPU cast;
+- the product scales exactly with x, and relabelling tokens or experts
+  permutes (or leaves) the output accordingly;
+- the router's picks are distinct, ordered by logit with ties to the lower
+  id, and their softmax weights sum to one;
+- pairs per woken expert never falls as n grows, so the flip point is where
+  the predicate first holds (page "fix(qtip): gate the trellis grouped GEMM on
+  m-tile occupancy, not token count", section "The fix")."""
+import numpy as np
+import pytest
+
+hyp = pytest.importorskip("hypothesis")
+from hypothesis import given, settings, strategies as st, HealthCheck  # noqa: E402
+
+import oracle.trellis_moe as O  # noqa: E402
+
+SETTINGS = settings(max_examples=120, deadline=None, suppress_health_check=[HealthCheck.too_slow])
+even_L = st.sampled_from([2, 4, 6, 8, 10, 12, 14, 16])
+
+
+@SETTINGS
+@given(row=st.binary(min_size=1, max_size=24), L=even_L)
+def test_window_identity_is_bit_slicing(row, L):
+    packed = np.frombuffer(row, dtype=np.uint8)[None, :]
+    s = O.states_window(O.symbols(packed), L)[0]
+    stream = int.from_bytes(row, "little")          # symbol j = bits [2j, 2j+2)
+    K = 4 * len(row)
+    for j in range(K):
+        hi = 2 * j + 2                               # the window ends after symbol j
+        lo = hi - L
+        want = (stream >> lo) & ((1 << L) - 1) if lo >= 0 else (stream & ((1 << hi) - 1)) << (-lo)
+        assert int(s[j]) == want, (j, L)
+
+
+@SETTINGS
+@given(row=st.binary(min_size=2, max_size=24), L=even_L, data=st.data())
+def test_run_decode_reproduces_window_identity(row, L, data):
+    c = O.symbols(np.frombuffer(row, dtype=np.uint8)[None, :])
+    K = c.shape[-1]
+    start = data.draw(st.integers(0, K - 1))
+    length = data.draw(st.integers(1, K - start))
+    run = O.run_states(c, L, start, length)[0]
+    assert np.array_equal(run, O.states_window(c, L)[0, start:start + length])
+
+
+@SETTINGS
+@given(counts=st.lists(st.integers(0, 40), min_size=1, max_size=24), T=st.integers(1, 48))
+def test_tile_map_invariants(counts, T):
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    tiles = O.tile_map(offsets, T)
+    assert len(tiles) == sum(-(-c // T) for c in counts)
+    i = 0
+    for e, c in enumerate(counts):
+        slot = int(offsets[e])
+        for _ in range(-(-c // T)):
+            te, ts, tr = (int(v) for v in tiles[i])
+            assert te == e and ts == slot and 1 <= tr <= T
+            slot += tr
+            i += 1
+        assert slot == offsets[e + 1]
+
+
+@SETTINGS
+@given(E=st.integers(1, 64), k=st.integers(1, 8), n=st.integers(0, 60), T=st.integers(1, 64), data=st.data())
+def test_capacity_bound_holds_for_any_routing(E, k, n, T, data):
+    """Any split of the P = n*k pairs over the E experts (a superset of the
+    routings, whose per-token distinct experts cap a count at n) fits."""
+    k = min(k, E)
+    P = n * k
+    cuts = sorted(data.draw(st.lists(st.integers(0, P), min_size=E - 1, max_size=E - 1)))
+    counts = np.diff([0] + cuts + [P])
+    need = sum(-(-int(c) // T) for c in counts)
+    assert need <= O.tile_map_capacity(n, k, E, T)
+
+
+@SETTINGS
+@given(v=st.lists(st.floats(width=32, allow_nan=False, allow_infinity=False), min_size=1, max_size=64))
+def test_bf16_rne_matches_torch(v):
+    torch = pytest.importorskip("torch")
+    y = np.asarray(v, dtype=np.float32)
+    y = y[np.abs(y.astype(np.float64)) < 3.38e38]   # rounds to a finite bf16
+    if y.size == 0:
+        return
+    want = torch.from_numpy(y).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.bf16_rne_bits(y), want)
+
+
+def _problem(seed, E, k, n, K, N, L):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((n, K)).astype(np.float32)
+    x_bits = (x.view(np.uint32) >> 16).astype(np.uint16)            # bf16 by truncation: any bf16 works here
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(n)]).astype(np.int32)
+    w = rng.random((n, k)).astype(np.float32)
+    packed = rng.integers(0, 256, (E, N, K // 4), dtype=np.uint8)
+    lut = (rng.standard_normal(1 << L) * 0.1).astype(np.float16).view(np.uint16)
+    return x_bits, ids, w, packed, lut
+
+
+@settings(max_examples=25, deadline=None)
+@given(seed=st.integers(0, 10_000), E=st.integers(2, 6), k=st.integers(1, 2), n=st.integers(1, 5),
+       L=st.sampled_from([4, 8, 12]))
+def test_product_scaling_and_relabelling(seed, E, k, n, L):
+    k = min(k, E)
+    K, N = 64, 16
+    x_bits, ids, w, packed, lut = _problem(seed, E, k, n, K, N, L)
+    Y = O.moe_forward(x_bits, ids, w, packed, lut, L)
+    # doubling x (one more in each bf16 exponent; N(0,1) draws are normal
+    # numbers far from overflow) doubles every product and partial sum
+    # exactly, so Y doubles bit for bit
+    assert np.all((x_bits & 0x7F80) != 0)
+    x2 = (x_bits + 0x80).astype(np.uint16)
+    assert np.array_equal(O.bf16_bits_to_f64(x2), 2 * O.bf16_bits_to_f64(x_bits))
+    assert np.array_equal(O.moe_forward(x2, ids, w, packed, lut, L), 2 * Y)
+    tol = 1e-12 * max(1.0, float(np.abs(Y).max()))
+    # tokens relabelled: the output rows follow
+    perm = np.random.default_rng(seed + 1).permutation(n)
+    Yp = O.moe_forward(x_bits[perm], ids[perm], w[perm], packed, lut, L)
+    assert np.allclose(Yp, Y[perm], rtol=0, atol=tol)
+    # experts relabelled (ids and weights moved together): the output is unchanged
+    rel = np.random.default_rng(seed + 2).permutation(E)
+    packed_rel = np.empty_like(packed)
+    packed_rel[rel] = packed
+    Yr = O.moe_forward(x_bits, rel[ids].astype(np.int32), w, packed_rel, lut, L)
+    assert np.allclose(Yr, Y, rtol=0, atol=tol)
+
+
+@SETTINGS
+@given(E=st.integers(1, 40), k=st.integers(1, 8), n=st.integers(1, 6), ties=st.booleans(),
+       seed=st.integers(0, 10_000))
+def test_router_picks_and_weights(E, k, n, ties, seed):
+    k = min(k, E)
+    lg = np.random.default_rng(seed).standard_normal((n, E)).astype(np.float32)
+    if ties:
+        lg = np.round(lg).astype(np.float32)
+    ids, w = O.router_topk(lg, k)
+    for t in range(n):
+        picked = list(ids[t])
+        assert len(set(picked)) == k
+        rest = [e for e in range(E) if e not in picked]
+        for a, b in zip(picked, picked[1:]):                # descending, ties to the lower id
+            assert lg[t, a] > lg[t, b] or (lg[t, a] == lg[t, b] and a < b)
+        for e in rest:                                      # nothing left out beats a pick
+            assert lg[t, e] < lg[t, picked[-1]] or (lg[t, e] == lg[t, picked[-1]] and e > picked[-1])
+        assert abs(w[t].sum() - 1.0) < 1e-12 and np.all(np.diff(w[t]) <= 1e-15)
+
+
+@settings(max_examples=60, deadline=None)
+@given(E=st.integers(1, 256), k=st.integers(1, 16), T=st.integers(1, 32))
+def test_fill_monotone_and_flip(E, k, T):
+    k = min(k, E)
+    vals = [O.pairs_per_woken_expert(n, k, E) for n in range(1, 200)]
+    assert all(b >= a * (1 - 1e-12) for a, b in zip(vals, vals[1:]))
+    flip = O.grouped_min_tokens(k, E, T, limit=1 << 14)
+    if flip > 0:
+        assert O.tiles_amortize(flip, k, E, T) and (flip == 1 or not O.tiles_amortize(flip - 1, k, E, T))
