@@ -115,6 +115,23 @@ def test_moe_forward_gemv_arm_small_all_outputs(name):
     assert not bad.any(), (int(bad.sum()), np.argwhere(bad)[:4].tolist())
 
 
+def test_moe_forward_gemv_arm_is_bit_reproducible():
+    """The GEMV arm sums each token's pairs in a fixed order and writes each
+    output once, so repeated calls (and a call on another stream) give the
+    same bits (V4 up shape, 8 tokens)."""
+    prob = moe_inputs.make_problem("v4_decode_n32", n=8)
+    d = to_device(prob)
+    outs = []
+    for stream in (None, None, torch.cuda.Stream()):
+        with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
+            y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=16, pin=tq.ARM_GEMV)
+        torch.cuda.synchronize()
+        assert arm == tq.ARM_GEMV
+        outs.append(y.view(torch.int16).clone())
+    check_no_device_error()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
 # Expert sizes whose m-tiles at TILE_M 256 run through every transition of the
 # accumulator slots (m-tiles above 128 pairs take both 128-column slots, the
 # others one, alternating): 296 -> 256 + 40 (big -> small), 40 -> 200 (small ->
