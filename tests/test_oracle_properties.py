@@ -26,7 +26,9 @@ from hypothesis import given, settings, strategies as st, HealthCheck  # noqa: E
 
 import oracle.trellis_moe as O  # noqa: E402
 
-SETTINGS = settings(max_examples=120, deadline=None, suppress_health_check=[HealthCheck.too_slow])
+# derandomized: the same examples on every run (no flaky suite), no example database written
+SETTINGS = settings(max_examples=120, deadline=None, suppress_health_check=[HealthCheck.too_slow],
+                    derandomize=True, database=None)
 even_L = st.sampled_from([2, 4, 6, 8, 10, 12, 14, 16])
 
 
@@ -108,7 +110,7 @@ def _problem(seed, E, k, n, K, N, L):
     return x_bits, ids, w, packed, lut
 
 
-@settings(max_examples=25, deadline=None)
+@settings(max_examples=25, deadline=None, derandomize=True, database=None)
 @given(seed=st.integers(0, 10_000), E=st.integers(2, 6), k=st.integers(1, 2), n=st.integers(1, 5),
        L=st.sampled_from([4, 8, 12]))
 def test_product_scaling_and_relabelling(seed, E, k, n, L):
@@ -156,7 +158,7 @@ def test_router_picks_and_weights(E, k, n, ties, seed):
         assert abs(w[t].sum() - 1.0) < 1e-12 and np.all(np.diff(w[t]) <= 1e-15)
 
 
-@settings(max_examples=60, deadline=None)
+@settings(max_examples=60, deadline=None, derandomize=True, database=None)
 @given(E=st.integers(1, 256), k=st.integers(1, 16), T=st.integers(1, 32))
 def test_fill_monotone_and_flip(E, k, T):
     k = min(k, E)
