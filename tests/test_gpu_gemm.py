@@ -115,6 +115,25 @@ def test_moe_forward_gemv_arm_small_all_outputs(name):
     assert not bad.any(), (int(bad.sum()), np.argwhere(bad)[:4].tolist())
 
 
+@pytest.mark.parametrize("N", [1, 3, 200])
+def test_moe_forward_gemv_arm_any_output_width(N):
+    """The GEMV arm of the whole product takes any N >= 1 (one (token, row)
+    item per output element; a warp's range may wrap from a token's last row
+    to the next token's first): all outputs within half a bf16 ulp of the
+    oracle plus the fp32 slack; the grouped pin at such an N is refused."""
+    prob = moe_inputs.make_custom(8, 2, 7, 256, N, 12, seed=900 + N)
+    d = to_device(prob)
+    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=16, pin=tq.ARM_GEMV)
+    check_no_device_error()
+    assert arm == tq.ARM_GEMV and tuple(y.shape) == (7, N)
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, 12)
+    got = y.float().cpu().numpy().astype(np.float64)
+    assert not (np.abs(got - ref) > np.abs(ref) * 2.0 ** -8 + 1e-5 * np.abs(ref).max()).any()
+    if N % 128:
+        with pytest.raises(tq.TQError):
+            tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=16, pin=tq.ARM_GROUPED)
+
+
 def test_moe_forward_gemv_arm_is_bit_reproducible():
     """The GEMV arm sums each token's pairs in a fixed order and writes each
     output once, so repeated calls (and a call on another stream) give the
