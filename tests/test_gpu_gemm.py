@@ -134,6 +134,24 @@ def test_moe_forward_gemv_arm_any_output_width(N):
             tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=16, pin=tq.ARM_GROUPED)
 
 
+@pytest.mark.parametrize("name", ["v4_fill_n1024", "v4_n128_down"])
+def test_moe_forward_gemv_arm_full_size_sampled_rows(name):
+    """The forward's GEMV arm at full V4 sizes (1024 tokens: 2 M (token, row)
+    items with the activations read from global memory; the down projection
+    at 128 tokens, K = 2048 -> N = 4096): sampled output columns within half a
+    bf16 ulp of the oracle plus the fp32 slack."""
+    prob = moe_inputs.make_problem(name)
+    d = to_device(prob)
+    s = prob.shape
+    y, arm = tq.tq_moe_forward(d["x"], d["packed"], d["lut"], d["ids"], d["w"], tile_m=16, pin=tq.ARM_GEMV)
+    check_no_device_error()
+    assert arm == tq.ARM_GEMV
+    rows = sample_rows(s.N, 24, seed=77)
+    ref = O.moe_forward(prob.x_bits, prob.topk_ids, prob.topk_w, prob.packed, prob.lut_bits, s.L, rows=rows)
+    got = y.float().cpu().numpy()[:, rows].astype(np.float64)
+    assert not (np.abs(got - ref) > np.abs(ref) * 2.0 ** -8 + 1e-5 * np.abs(ref).max()).any()
+
+
 def test_moe_forward_gemv_arm_is_bit_reproducible():
     """The GEMV arm sums each token's pairs in a fixed order and writes each
     output once, so repeated calls (and a call on another stream) give the
